@@ -1,0 +1,282 @@
+/*
+ * kvi_oracle.c -- plain, slow, single-threaded float64 CPU oracle for the
+ * retrieve-and-inject path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) includes, links or calls this file; only the tests,
+ * the smoke check and the benchmark's CPU-baseline leg do.  It shares no code,
+ * header, table or constant with the CUDA path.
+ *
+ * What it follows (page: "InferScale: GPU-Native KV Injection for
+ * Personalized LLM Serving", the pith.science review of arXiv 2607.27090):
+ *   - Figure 2 caption: each fact has a retrieval embedding and a pre-RoPE K/V
+ *     tensor under one fact_id; at serving time the top-k retrieved facts are
+ *     resolved to their KV and positioned by Chunked RoPE.
+ *   - Section 5.1 / Theorem 6 (Chunked RoPE): keys are stored before rotary
+ *     encoding and rotated to their serving positions on injection; exact
+ *     relocation follows from R_a^T R_b = R_{b-a}.
+ *   - Section 3.4 (KV-connector premise): K/V are scatter-copied into the
+ *     engine's paged blocks (vLLM PagedAttention layout) before the forward
+ *     pass.
+ *
+ * Readings where the page is silent (each one is listed with its reason in the
+ * design notes):
+ *   - similarity is the plain dot product (equal to cosine for the unit-norm
+ *     embeddings used), computed exactly up to float64 rounding; the exact
+ *     scan stands in for the paper's approximate GPU index;
+ *   - top-k order is the total order (score descending, fact id ascending);
+ *   - rotary pairing is rotate-half: element i pairs with i + D/2, with
+ *     frequency omega_i = theta^(-2i/D) (RoFormer frequencies, no scaling);
+ *   - facts are placed contiguously in rank order from a start position.
+ *
+ * Every function below is pinned by the CPU tests against closed forms,
+ * invariants or brute force; none is checked only against itself.
+ *
+ * Build: plain C11, -ffp-contract=off so that no multiply-add is fused and
+ * the results are the same on x86-64 and aarch64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Status codes returned by the oracle (independent of the library's own). */
+enum { KVO_OK = 0, KVO_BAD_ARG = 1, KVO_OUT_OF_RANGE = 2, KVO_CAPACITY = 3 };
+
+/* bf16 -> double: a bf16 value is the upper 16 bits of an IEEE binary32. */
+double kvo_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Step 1, scores.  s_i = sum_j q_j * e_ij, summed left to right in float64,
+ * for every fact i < n.  The embeddings are the "retrieval space" of the
+ * Figure 2 caption; the dot product is the similarity (reading above). */
+void kvo_scores(const float *q, const float *emb, int64_t n, int64_t e,
+                double *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const float *row = emb + i * e;
+        double s = 0.0;
+        for (int64_t j = 0; j < e; ++j)
+            s += (double)q[j] * (double)row[j];
+        out[i] = s;
+    }
+}
+
+typedef struct { double s; int32_t id; } kvo_key;
+
+/* (score descending, id ascending): a total order over distinct ids. */
+static int kvo_key_cmp(const void *a, const void *b)
+{
+    const kvo_key *x = (const kvo_key *)a, *y = (const kvo_key *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/* Step 2, select.  Sort all ids by (score descending, id ascending) and keep
+ * the first k; sel[] receives them in rank order.  "Top-k retrieved facts"
+ * of the Figure 2 caption, taken exactly.  Returns KVO_BAD_ARG for k <= 0 or
+ * k > n. */
+int kvo_topk(const double *s, int64_t n, int32_t k, int32_t *sel)
+{
+    if (k <= 0 || (int64_t)k > n) return KVO_BAD_ARG;
+    kvo_key *keys = (kvo_key *)malloc((size_t)n * sizeof *keys);
+    if (!keys) return KVO_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i) { keys[i].s = s[i]; keys[i].id = (int32_t)i; }
+    qsort(keys, (size_t)n, sizeof *keys, kvo_key_cmp);
+    for (int32_t j = 0; j < k; ++j) sel[j] = keys[j].id;
+    free(keys);
+    return KVO_OK;
+}
+
+/* Step 3, place.  pos_0 = start, pos_{j+1} = pos_j + len[sel_j]: the facts
+ * sit back to back in rank order from `start` (reading of the truncated
+ * Figure 2 caption, "positioned by chunked RoPE").  Writes pos[0..k) and
+ * returns the total number of tokens placed, or -1 if an id is out of range
+ * or a length is negative. */
+int64_t kvo_place(const int32_t *sel, int32_t k, const int32_t *fact_len,
+                  int64_t n_facts, int64_t start, int64_t *pos)
+{
+    int64_t p = start;
+    for (int32_t j = 0; j < k; ++j) {
+        if (sel[j] < 0 || (int64_t)sel[j] >= n_facts) return -1;
+        if (fact_len[sel[j]] < 0) return -1;
+        pos[j] = p;
+        p += fact_len[sel[j]];
+    }
+    return p - start;
+}
+
+/* Step 4, frequencies.  omega_i = theta^(-2i/D) for i < D/2. */
+void kvo_rope_omega(double theta, int32_t d, double *omega)
+{
+    for (int32_t i = 0; i < d / 2; ++i)
+        omega[i] = pow(theta, -2.0 * (double)i / (double)d);
+}
+
+/* Step 5, rotate one head vector x[D] to position p (Section 5.1, Chunked
+ * RoPE; rotate-half pairing).  For each i < D/2, with a = p * omega_i:
+ *   y_i       = x_i cos a - x_{i+D/2} sin a
+ *   y_{i+D/2} = x_{i+D/2} cos a + x_i sin a
+ * p is a double so that the relocation identity can be checked at any real
+ * offset; the path itself uses integer positions. */
+void kvo_rotate(const double *x, int32_t d, double theta, double p, double *y)
+{
+    const int32_t half = d / 2;
+    for (int32_t i = 0; i < half; ++i) {
+        const double w = pow(theta, -2.0 * (double)i / (double)d);
+        const double a = p * w;
+        const double c = cos(a), s = sin(a);
+        const double x0 = x[i], x1 = x[i + half];
+        y[i] = x0 * c - x1 * s;
+        y[i + half] = x1 * c + x0 * s;
+    }
+}
+
+/* Paged slot of token position p: block table entry p div B, offset p mod B
+ * (vLLM PagedAttention layout behind the Section 3.4 scatter-copy).  Returns
+ * KVO_OUT_OF_RANGE if p lies beyond the table or the entry is not a block of
+ * the pool. */
+int kvo_slot(int64_t p, const int32_t *block_table, int32_t table_len,
+             int32_t block_size, int32_t num_blocks, int32_t *blk, int32_t *off)
+{
+    if (p < 0 || block_size <= 0) return KVO_OUT_OF_RANGE;
+    const int64_t e = p / block_size;
+    if (e >= table_len) return KVO_OUT_OF_RANGE;
+    const int32_t b = block_table[e];
+    if (b < 0 || b >= num_blocks) return KVO_OUT_OF_RANGE;
+    *blk = b;
+    *off = (int32_t)(p % block_size);
+    return KVO_OK;
+}
+
+/* Expected rows of one injected token: fact `fact`, token t of that fact, at
+ * position p.  Store layout kv[L][2][n_tokens][H][D] (bf16 bits), fact f's
+ * token t at store row fact_start[f] + t.
+ *   k_out[L][H][D]: float64 rotated K (unrounded),
+ *   v_out[L][H][D]: V bits, copied unchanged.
+ * Returns KVO_OUT_OF_RANGE if the row lies outside the store. */
+int kvo_token_rows(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                   int64_t n_tokens, int64_t row, double theta, int64_t p,
+                   double *k_out, uint16_t *v_out)
+{
+    if (row < 0 || row >= n_tokens) return KVO_OUT_OF_RANGE;
+    double *x = (double *)malloc((size_t)D * sizeof *x);
+    if (!x) return KVO_BAD_ARG;
+    const int64_t hd = (int64_t)H * D;
+    for (int32_t l = 0; l < L; ++l) {
+        const uint16_t *krow = kv + (((int64_t)l * 2 + 0) * n_tokens + row) * hd;
+        const uint16_t *vrow = kv + (((int64_t)l * 2 + 1) * n_tokens + row) * hd;
+        for (int32_t h = 0; h < H; ++h) {
+            for (int32_t i = 0; i < D; ++i)
+                x[i] = kvo_bf16_to_double(krow[(int64_t)h * D + i]);
+            kvo_rotate(x, D, theta, (double)p, k_out + ((int64_t)l * H + h) * D);
+            for (int32_t i = 0; i < D; ++i)
+                v_out[((int64_t)l * H + h) * D + i] = vrow[(int64_t)h * D + i];
+        }
+    }
+    free(x);
+    return KVO_OK;
+}
+
+/* Step 6, expected cache for one request (Section 3.4 scatter-copy).
+ *
+ * Inputs: store kv bits [L][2][n_tokens][H][D]; per fact start row and length;
+ * the injected facts `ids[n]` with their start positions `starts[n]`; the
+ * request's block table; the pool geometry (num_blocks, block_size).
+ *
+ * Outputs, both laid out like the pool [L][2][num_blocks][B][H][D]:
+ *   expect[]  float64 expected value of every written element,
+ *   written[] 1 for every element the injection writes, 0 elsewhere (those
+ *             elements must keep their pre-call contents).
+ * A K element is the rotated pre-RoPE key at the token's position; a V
+ * element is the stored bits read as a number.
+ *
+ * Returns KVO_OK, KVO_OUT_OF_RANGE (id, store row or slot out of range) or
+ * KVO_CAPACITY (a slot written twice: overlapping positions). */
+int kvo_inject_expected(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                        int64_t n_tokens, const int64_t *fact_start,
+                        const int32_t *fact_len, int64_t n_facts,
+                        const int32_t *ids, const int64_t *starts, int32_t n,
+                        const int32_t *block_table, int32_t table_len,
+                        int32_t num_blocks, int32_t block_size, double theta,
+                        double *expect, uint8_t *written)
+{
+    const int64_t hd = (int64_t)H * D;
+    const int64_t tok_per_kv = (int64_t)num_blocks * block_size;
+    const int64_t n_el = (int64_t)L * 2 * tok_per_kv * hd;
+    memset(written, 0, (size_t)n_el);
+    for (int64_t e = 0; e < n_el; ++e) expect[e] = 0.0;
+
+    double *kr = (double *)malloc((size_t)(L * hd) * sizeof *kr);
+    uint16_t *vr = (uint16_t *)malloc((size_t)(L * hd) * sizeof *vr);
+    if (!kr || !vr) { free(kr); free(vr); return KVO_BAD_ARG; }
+    int rc = KVO_OK;
+    for (int32_t j = 0; j < n && rc == KVO_OK; ++j) {
+        const int32_t f = ids[j];
+        if (f < 0 || (int64_t)f >= n_facts) { rc = KVO_OUT_OF_RANGE; break; }
+        for (int32_t t = 0; t < fact_len[f]; ++t) {
+            const int64_t p = starts[j] + t;
+            int32_t blk, off;
+            if (kvo_slot(p, block_table, table_len, block_size, num_blocks,
+                         &blk, &off) != KVO_OK) { rc = KVO_OUT_OF_RANGE; break; }
+            if (kvo_token_rows(kv, L, H, D, n_tokens, fact_start[f] + t, theta,
+                               p, kr, vr) != KVO_OK) { rc = KVO_OUT_OF_RANGE; break; }
+            for (int32_t l = 0; l < L; ++l) {
+                for (int32_t c = 0; c < 2; ++c) {
+                    const int64_t base =
+                        ((((int64_t)l * 2 + c) * num_blocks + blk) * block_size + off) * hd;
+                    if (written[base]) { rc = KVO_CAPACITY; break; }
+                    for (int64_t x = 0; x < hd; ++x) {
+                        written[base + x] = 1;
+                        expect[base + x] = c == 0 ? kr[l * hd + x]
+                                                  : kvo_bf16_to_double(vr[l * hd + x]);
+                    }
+                }
+                if (rc != KVO_OK) break;
+            }
+            if (rc != KVO_OK) break;
+        }
+    }
+    free(kr);
+    free(vr);
+    return rc;
+}
+
+/* The whole request as one call (steps 1-6), used to time the oracle as a
+ * CPU baseline: score all facts, select the top k, place them from `start`,
+ * and produce every injected token's rows.  k_out must hold
+ * (sum of selected lengths) * L * H * D doubles and v_out as many uint16.
+ * Returns the number of tokens produced, or -1 on error. */
+int64_t kvo_request(const float *q, const float *emb, int64_t n_facts, int64_t e,
+                    int32_t k, const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                    int64_t n_tokens, const int64_t *fact_start,
+                    const int32_t *fact_len, int64_t start, double theta,
+                    int32_t *sel, int64_t *pos, double *k_out, uint16_t *v_out,
+                    int64_t max_tokens)
+{
+    double *s = (double *)malloc((size_t)n_facts * sizeof *s);
+    if (!s) return -1;
+    kvo_scores(q, emb, n_facts, e, s);
+    const int rc = kvo_topk(s, n_facts, k, sel);
+    free(s);
+    if (rc != KVO_OK) return -1;
+    const int64_t T = kvo_place(sel, k, fact_len, n_facts, start, pos);
+    if (T < 0 || T > max_tokens) return -1;
+    const int64_t per_tok = (int64_t)L * H * D;
+    int64_t tok = 0;
+    for (int32_t j = 0; j < k; ++j) {
+        for (int32_t t = 0; t < fact_len[sel[j]]; ++t, ++tok) {
+            if (kvo_token_rows(kv, L, H, D, n_tokens, fact_start[sel[j]] + t,
+                               theta, pos[j] + t, k_out + tok * per_tok,
+                               v_out + tok * per_tok) != KVO_OK)
+                return -1;
+        }
+    }
+    return tok;
+}

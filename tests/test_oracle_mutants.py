@@ -1,0 +1,61 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins fail.
+
+Each mutant is a one-line edit of oracle/kvi_oracle.c (a dropped term, a
+flipped sign, a wrong frequency, a reversed tie-break, an off-by-one in
+placement, a div/mod swap in paging, a stride slip, a bad bf16 decode),
+compiled to a temporary library on the CPU; the pin suite is then run against
+it in a subprocess and must fail.  Nothing here touches a GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "kvi_oracle.c")
+
+MUTANTS = {
+    "scores_drop_first_term": (
+        "for (int64_t j = 0; j < e; ++j)\n            s += ",
+        "for (int64_t j = 1; j < e; ++j)\n            s += "),
+    "topk_tie_to_higher_id": (
+        "return (x->id > y->id) - (x->id < y->id);",
+        "return (x->id < y->id) - (x->id > y->id);"),
+    "place_off_by_one": (
+        "pos[j] = p;\n        p += fact_len[sel[j]];",
+        "p += fact_len[sel[j]];\n        pos[j] = p;"),
+    "rotate_sign_flip": (
+        "y[i] = x0 * c - x1 * s;", "y[i] = x0 * c + x1 * s;"),
+    "rotate_drop_term": (
+        "y[i + half] = x1 * c + x0 * s;", "y[i + half] = x1 * c;"),
+    "rotate_wrong_frequency": (
+        "const double w = pow(theta, -2.0 * (double)i / (double)d);",
+        "const double w = pow(theta, -1.0 * (double)i / (double)d);"),
+    "rotate_interleaved_pairing": (
+        "const double x0 = x[i], x1 = x[i + half];\n        y[i] = x0 * c - x1 * s;\n        y[i + half] = x1 * c + x0 * s;",
+        "const double x0 = x[2 * i], x1 = x[2 * i + 1];\n        y[2 * i] = x0 * c - x1 * s;\n        y[2 * i + 1] = x1 * c + x0 * s;"),
+    "slot_div_mod_swap": (
+        "*off = (int32_t)(p % block_size);", "*off = (int32_t)(p / block_size);"),
+    "token_rows_v_reads_k": (
+        "const uint16_t *vrow = kv + (((int64_t)l * 2 + 1) * n_tokens + row) * hd;",
+        "const uint16_t *vrow = kv + (((int64_t)l * 2 + 0) * n_tokens + row) * hd;"),
+    "bf16_decode_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-shared",
+                           "-fPIC", "-o", str(lib), str(mut), "-lm"])
+    env = dict(os.environ, KVI_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
