@@ -1,0 +1,516 @@
+#!/usr/bin/env python
+"""Benchmark of the fused retrieve-and-inject step on GB300.
+
+One step = one kvi_retrieve_and_inject call for one request of the
+Llama-3-8B KV workload (10k facts of 12-48 tokens, 1024-d embeddings, k = 50,
+64-token system prefix, 16-token pages): exact top-k scoring of all 10k
+embeddings, placement, Chunked-RoPE rotation of the selected keys and the
+paged scatter of K and V ("InferScale: GPU-Native KV Injection for
+Personalized LLM Serving", Figure 2 caption, Section 5.1, Section 3.4).
+
+Prints one JSON line (rank 0): injected KV GB/s (the metric), the fraction
+of the measured HBM peak that the step's algorithmic bytes reach, per-request
+latency at k = 5, 10, 20, 50, the dominant kernel's roofline, an end-to-end
+figure through the C ABI with host buffers, clocks sampled during the timed
+region, and the oracle's CPU baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (launched by torchrun) every rank runs its own independent
+replica of the workload (requests shard across GPUs with no data exchange):
+weak scaling, value = bytes of all ranks / the slowest rank's time.
+--impl reference times the float64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "injected KV GB/s (% of HBM peak) and inject latency/request at k=5..50"
+WORKLOAD = "llama3_8b_10k"
+N_QUERIES = 8          # distinct queries / block tables cycled through the steps
+FLUSH_BYTES = 256 << 20  # > 129 MB L2, written between timed steps
+SWEEP_KS = (5, 10, 20, 50)
+PROFILE = os.path.join(ROOT, "profiles", "inject_kernel_llama3_8b_10k.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--k", type=int, default=50)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over ranks (every rank returns it)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def replica_seed(base: int, rank: int) -> int:
+    """Each rank's replica draws its own requests."""
+    return base + 1000 * rank
+
+
+# ----------------------------------------------------------------- peaks
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic():
+    """dram bytes per inject launch from the committed ncu summary, when it
+    was taken on the current kernel source (else None)."""
+    if not os.path.exists(PROFILE):
+        return None
+    src = os.path.join(ROOT, "pre_rope_kv_gb300", "csrc", "kvi_inject.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.startswith("- "):
+            key, _, v = line[2:].partition(":")
+            vals[key.strip()] = v.strip().strip("`")
+    if vals.get("kvi_inject.cu sha256[:16]") != digest:
+        return None
+    try:
+        return float(vals["dram bytes per launch (scaled to the bench launch)"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.strip().split(",") for l in open(self.path) if l.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- our arm
+
+class Bench:
+    """The workload on this rank's GPU and everything one step needs."""
+
+    def __init__(self, rank: int, k: int):
+        import torch
+
+        from tests import synth
+        import pre_rope_kv_gb300 as kvi
+        from pre_rope_kv_gb300 import build as kbuild
+
+        kbuild.build()
+        kvi.load_library()
+        self.torch, self.kvi, self.synth = torch, kvi, synth
+        w = synth.WORKLOADS[WORKLOAD]
+        if rank:
+            import dataclasses
+            w = dataclasses.replace(w, seed=replica_seed(w.seed, rank))
+        self.w = w
+        self.k = k
+        b = synth.build_workload(w, k=max(SWEEP_KS + (k,)))
+        self.b = b
+        rng = np.random.default_rng(w.seed + 17)
+        # distinct queries and block tables (shuffled free lists) per step
+        self.queries = torch.from_numpy(synth.query_rows(rng, N_QUERIES, w.embed_dim)).cuda()
+        tl = int(b.table_lens[0])
+        tables = np.stack([rng.permutation(b.num_blocks)[:tl] for _ in range(N_QUERIES)])
+        self.tables = torch.from_numpy(tables.astype(np.int32)).cuda()
+        self.table_len = torch.full((1,), tl, dtype=torch.int32, device="cuda")
+        self.start = torch.from_numpy(b.start_pos).cuda()
+        self.g = kvi.geometry(w.layers, w.kv_heads, w.head_dim, w.embed_dim)
+        views = [kvi.store_view(self.g, b.kv, st.emb, st.fact_start, st.fact_len)
+                 for st in b.stores]
+        self.d_views = torch.frombuffer(bytearray(kvi.pack_store_views(views)),
+                                        dtype=torch.uint8).cuda()
+        self.cache = kvi.paged_cache([b.pool[l] for l in range(w.layers)], w.block_size)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.stream = torch.cuda.current_stream()
+        kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, tl * w.block_size)
+        self.bufs = {}
+
+    def buffers(self, k):
+        if k not in self.bufs:
+            t = self.torch
+            self.bufs[k] = dict(
+                ids=t.empty((1, k), dtype=t.int32, device="cuda"),
+                scores=t.empty((1, k), dtype=t.float32, device="cuda"),
+                pos=t.empty((1, k), dtype=t.int32, device="cuda"),
+                ws=t.empty(self.kvi.kvi_workspace_bytes(1, self.w.n_facts, k), dtype=t.uint8,
+                           device="cuda"))
+        return self.bufs[k]
+
+    def step(self, i, k, query=None):
+        bf = self.buffers(k)
+        q = self.queries[i % N_QUERIES:i % N_QUERIES + 1] if query is None else query
+        self.kvi.kvi_retrieve_and_inject(
+            self.g, 1, self.d_views, self.w.n_facts, q, k, self.start,
+            self.tables[i % N_QUERIES:i % N_QUERIES + 1], self.table_len, int(self.tables.shape[1]),
+            self.cache, self.w.rope_theta, bf["ids"], bf["scores"], bf["pos"], bf["ws"],
+            self.status, self.stream)
+
+    def injected_tokens(self, k):
+        """Tokens each query injects (from the step's own outputs)."""
+        lens = self.b.stores[0].len_np
+        out = []
+        for i in range(N_QUERIES):
+            self.step(i, k)
+            self.torch.cuda.synchronize()
+            ids = self.buffers(k)["ids"].cpu().numpy()[0]
+            out.append(int(lens[ids].sum()))
+        assert int(self.status.item()) == 0
+        return out
+
+    def timed(self, k, steps, warmup, trace=False):
+        """Per-step device times (s) with an L2 flush between steps."""
+        t = self.torch
+        for i in range(warmup):
+            self.flush.zero_()
+            self.step(i, k)
+        t.cuda.synchronize()
+        ev = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True),
+               t.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if trace:
+            for e in ev:
+                for x in e:
+                    x.record()  # creates the event handles
+            t.cuda.synchronize()
+        times, stages = [], []
+        for i in range(steps):
+            self.flush.zero_()
+            if trace:
+                self.kvi.kvi_trace_stages(list(ev[i]))
+                self.step(i, k)
+            else:
+                ev[i][0].record()
+                self.step(i, k)
+                ev[i][2].record()
+        if trace:
+            self.kvi.kvi_trace_stages([])
+        t.cuda.synchronize()
+        for e in ev:
+            times.append(e[0].elapsed_time(e[2]) / 1e3)
+            if trace:
+                stages.append((e[0].elapsed_time(e[1]) / 1e3, e[1].elapsed_time(e[2]) / 1e3))
+        return times, stages
+
+    def e2e(self, k, steps, warmup):
+        """Same step through the C ABI from pinned host buffers: the query,
+        start position and block table go host->device and the ids, scores,
+        positions and status come back, inside the timed region."""
+        t = self.torch
+        tl = int(self.tables.shape[1])
+        h_q = t.from_numpy(self.queries.cpu().numpy()).pin_memory()
+        h_bt = t.from_numpy(self.tables.cpu().numpy()).pin_memory()
+        h_start = t.from_numpy(self.b.start_pos.copy()).pin_memory()
+        d_q = t.empty((1, self.w.embed_dim), dtype=t.float32, device="cuda")
+        d_bt = t.empty((1, tl), dtype=t.int32, device="cuda")
+        bf = self.buffers(k)
+        h_ids = t.empty((1, k), dtype=t.int32).pin_memory()
+        h_scores = t.empty((1, k), dtype=t.float32).pin_memory()
+        h_pos = t.empty((1, k), dtype=t.int32).pin_memory()
+        h_status = t.empty(1, dtype=t.int32).pin_memory()
+        times = []
+        for i in range(warmup + steps):
+            self.flush.zero_()
+            t.cuda.synchronize()
+            t0 = time.perf_counter()
+            j = i % N_QUERIES
+            d_q.copy_(h_q[j:j + 1], non_blocking=True)
+            d_bt.copy_(h_bt[j:j + 1], non_blocking=True)
+            self.start.copy_(h_start, non_blocking=True)
+            self.kvi.kvi_retrieve_and_inject(
+                self.g, 1, self.d_views, self.w.n_facts, d_q, k, self.start, d_bt,
+                self.table_len, tl, self.cache, self.w.rope_theta, bf["ids"], bf["scores"],
+                bf["pos"], bf["ws"], self.status, self.stream)
+            h_ids.copy_(bf["ids"], non_blocking=True)
+            h_scores.copy_(bf["scores"], non_blocking=True)
+            h_pos.copy_(bf["pos"], non_blocking=True)
+            h_status.copy_(self.status, non_blocking=True)
+            t.cuda.synchronize()
+            if i >= warmup:
+                times.append(time.perf_counter() - t0)
+        h2d = self.w.embed_dim * 4 + tl * 4 + 4
+        d2h = k * 12 + 4
+        return times, h2d, d2h
+
+
+def cpu_baseline_sample(w, k: int, n_requests: int, seed: int):
+    """Time the oracle as it stands (one thread) on n_requests requests of the
+    workload: scoring all facts, top-k, placement and the rotation/copy of
+    every injected token.  The K/V rows it rotates are drawn on the host
+    outside the timed parts and reused across tokens (their values do not
+    change the work)."""
+    import oracle
+    from tests import synth
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    emb = synth.unit_rows(rng, w.n_facts, w.embed_dim)
+    lens = synth.fact_lengths(rng, w, w.n_facts)
+    shape = (w.layers, w.kv_heads, w.head_dim)
+    rows = [(synth.bf16_normal_bits(rng, shape), synth.bf16_normal_bits(rng, shape))
+            for _ in range(64)]
+    total_t, total_tokens = 0.0, 0
+    for r in range(n_requests):
+        q = synth.query_rows(rng, 1, w.embed_dim)[0]
+        t0 = time.perf_counter()
+        s = oracle.scores(q, emb)
+        sel = oracle.topk(s, k)
+        pos, T = oracle.place(sel, lens, w.start or 0)
+        total_t += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        tok = 0
+        for j, f in enumerate(sel):
+            for t in range(int(lens[f])):
+                kr, vr = rows[tok % len(rows)]
+                oracle.token_rows_from_rows(kr, vr, w.rope_theta, int(pos[j]) + t)
+                tok += 1
+        total_t += time.perf_counter() - t0
+        total_tokens += T
+    gbs = total_tokens * w.token_bytes / total_t / 1e9
+    return gbs, total_t, total_tokens
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, "nccl")
+    peak, peak_kind = load_peaks()
+    bench = Bench(rank, args.k)
+    w, k = bench.w, args.k
+    dev = torch.device("cuda", local)
+
+    tokens = bench.injected_tokens(k)
+    step_tokens = [tokens[i % N_QUERIES] for i in range(args.steps)]
+
+    clocks = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    times, _ = bench.timed(k, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(dist)
+    clk = clocks.stop()
+    st = int(bench.status.item())
+    assert st == 0, f"device status {st}"
+
+    my_time = sum(times)
+    my_bytes = sum(step_tokens) * w.token_bytes
+    t_max = max_over_ranks(dist, my_time, dev)
+    all_bytes = sum_over_ranks(dist, my_bytes, dev)
+    value = all_bytes / t_max / 1e9
+    ms_per_step = t_max / args.steps * 1e3
+
+    # algorithmic HBM bytes: read + write of every injected byte, plus every
+    # embedding row scored
+    emb_bytes = w.n_facts * w.embed_dim * 4
+    alg = 2 * my_bytes + args.steps * emb_bytes
+    hbm_frac = alg / my_time / 1e9 / peak
+
+    # stage times (trace events) -> roofline of the inject kernel
+    _, stages = bench.timed(k, args.steps, args.warmup, trace=True)
+    inj = [s[1] for s in stages]
+    ret = [s[0] for s in stages]
+    inj_alg = [2 * step_tokens[i] * w.token_bytes for i in range(args.steps)]
+    achieved = sum(inj_alg) / sum(inj) / 1e9
+    traffic = profile_traffic()
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: Llama-3-8B KV geometry (32 layers, 8 KV heads, "
+                               f"d=128, theta 5e5), 10k facts of 12-48 tokens, 1024-d "
+                               f"embeddings, 1 request per step, k={k}, start 64, 16-token "
+                               f"pages",
+                   "requests_per_step": 1, "k": k, "parallelism": f"replicas x{world}",
+                   "l2": "256 MB write between steps, outside the timed events",
+                   "queries": f"{N_QUERIES} distinct queries and block tables cycled"},
+        "hbm_frac_of_measured_peak": round(hbm_frac, 4),
+        "peak_gbs": peak, "peak_kind": peak_kind,
+        "latency_us_per_request": {str(k): round(statistics.median(times) * 1e6, 2)},
+        "facts_per_s": round(world * args.steps * k / t_max, 1),
+        "stages_us": {"retrieve_place_median": round(statistics.median(ret) * 1e6, 2),
+                      "inject_median": round(statistics.median(inj) * 1e6, 2)},
+        "roofline": {"kernel": "inject_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(statistics.mean(inj_alg))},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if not args.no_sweep:
+        lat = {}
+        for kk in SWEEP_KS:
+            ts, _ = bench.timed(kk, max(10, args.steps), args.warmup)
+            lat[str(kk)] = round(statistics.median(ts) * 1e6, 2)
+        out["latency_us_per_request"] = lat
+    e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
+    e_max = max_over_ranks(dist, sum(e_times), dev)
+    out["e2e"] = {"value": round(all_bytes / e_max / 1e9, 2), "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "latency_us_median": round(statistics.median(e_times) * 1e6, 2)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, secs, toks = cpu_baseline_sample(w, k, 6, w.seed + 99)
+        out["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"6 requests of the same workload at k={k} ({toks} "
+                                         f"tokens, {secs:.1f} s): float64 scoring of all 10k "
+                                         f"facts, top-k, placement, rotation of every token"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle arm: the float64 CPU oracle timed on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from tests import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    k = args.k
+    for _ in range(args.warmup):
+        cpu_baseline_sample(w, k, 1, w.seed + 7)
+    secs_all, toks_all = 0.0, 0
+    for i in range(args.steps):
+        _gbs, secs, toks = cpu_baseline_sample(w, k, 1, w.seed + 100 + i)
+        secs_all += secs
+        toks_all += toks
+    value = toks_all * w.token_bytes / secs_all / 1e9
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs_all / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: Llama-3-8B KV geometry, 10k facts of 12-48 "
+                               f"tokens, 1024-d embeddings, 1 request per step, k={k}",
+                   "requests_per_step": 1, "k": k},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one request per step ({toks_all} tokens over "
+                                   f"{args.steps} steps), single-threaded float64 oracle"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

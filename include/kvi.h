@@ -1,0 +1,234 @@
+/*
+ * kvi.h -- C ABI of the GB300 (sm_103a) retrieve-and-inject library.
+ *
+ * The operation is the serving-time path of "InferScale: GPU-Native KV
+ * Injection for Personalized LLM Serving" (pith.science review of arXiv
+ * 2607.27090):
+ *   - Figure 2 caption: every memory fact is stored twice under one fact_id,
+ *     as a retrieval embedding and as pre-RoPE key/value tensors; at serving
+ *     time the top-k retrieved facts are resolved to their KV and positioned
+ *     by Chunked RoPE;
+ *   - Section 5.1 / Theorem 6 (Chunked RoPE): keys are kept before rotary
+ *     encoding and rotated to their serving positions on injection, which is
+ *     exact because R_a^T R_b = R_{b-a};
+ *   - Section 3.4 (KV-connector premise): the engine allocates paged blocks
+ *     for the memory prefix without prefilling them and the K/V are
+ *     scatter-copied into them before the forward pass.
+ *
+ * Conventions of this library (readings where the page is silent):
+ *   - similarity = dot product of float32 vectors, accumulated so that the
+ *     selection key is float64-accurate; exact top-k, ties to the lower id;
+ *   - rotary pairing is rotate-half (element i with i + D/2), frequency
+ *     omega_i = theta^(-2i/D), angle p * omega_i for token position p;
+ *   - retrieved facts are placed back to back, in rank order, from the
+ *     request's start position.
+ *
+ * Memory and ownership.  Every pointer named d_* or described as "device"
+ * is device memory owned by the caller and only borrowed for the enqueued
+ * work; the library never frees or keeps it.  The only state the library
+ * owns is a per-device table of RoPE cos/sin values (see kvi_prepare_rope).
+ * All compute calls are asynchronous on the given stream and never
+ * synchronise it; results and device-side status are valid once the stream
+ * reaches that point.
+ *
+ * Errors.  A call first validates its host-visible arguments and returns a
+ * status without enqueuing anything when they are wrong.  Data-dependent
+ * problems that only the GPU can see (a fact id >= n_facts, a block id
+ * outside the pool, a position beyond the block table) are recorded in the
+ * caller's device word *d_status (the first error wins, via compare-and-swap;
+ * the library never clears it) and the offending item is skipped: no kernel
+ * writes out of bounds, traps or waits.  kvi_last_error() returns a message
+ * for the calling thread's last failing call.
+ *
+ * Layouts (row-major, innermost last):
+ *   store K/V   kv[L][2][n_tokens][H][D]  bf16, index 0 = K (pre-RoPE), 1 = V
+ *   embeddings  emb[n_facts][E]           float32
+ *   fact extent fact_start[n_facts] int64 (first store row), fact_len int32
+ *   paged cache one buffer per layer,     bf16 [2][num_blocks][B][H][D]
+ *               (vLLM's flash-attention layout, K then V)
+ *   block table block_table[table_len]    int32 block ids, position p lives in
+ *               block block_table[p / B] at offset p % B.
+ */
+#ifndef KVI_H
+#define KVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVI_API __attribute__((visibility("default")))
+#else
+#define KVI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA handles, ABI-compatible with cudaStream_t / cudaEvent_t. */
+typedef struct CUstream_st *kvi_stream_t;
+typedef struct CUevent_st *kvi_event_t;
+
+typedef enum {
+    KVI_OK = 0,
+    KVI_ERR_INVALID_ARG = 1,  /* bad pointer, size, geometry or limit */
+    KVI_ERR_OUT_OF_RANGE = 2, /* fact id, store row, block id or position out of range */
+    KVI_ERR_CAPACITY = 3,     /* the facts do not fit the request's block table */
+    KVI_ERR_CUDA = 4          /* a CUDA runtime call failed (see kvi_last_error) */
+} kvi_status;
+
+/* Limits of this build. */
+#define KVI_MAX_LAYERS 128        /* L */
+#define KVI_MAX_K 256             /* facts retrieved per request */
+#define KVI_MAX_INJECT_FACTS 4096 /* facts per kvi_inject_paged call */
+#define KVI_MAX_HEAD_DIM 512      /* D, a multiple of 16 */
+#define KVI_MAX_EMBED_DIM 8192    /* E, a multiple of 4 */
+
+typedef struct {
+    int32_t layers;    /* L */
+    int32_t kv_heads;  /* H, KV heads (GQA) */
+    int32_t head_dim;  /* D, multiple of 16, <= KVI_MAX_HEAD_DIM */
+    int32_t embed_dim; /* E, multiple of 4, <= KVI_MAX_EMBED_DIM */
+} kvi_geometry;
+
+/* A fact store (Figure 2 caption: retrieval embedding and pre-RoPE K/V under
+ * one fact_id; fact_id = index).  The struct itself lives in host memory for
+ * the single-request calls and in device memory (an array of R of them) for
+ * kvi_retrieve_and_inject; the pointers inside are device pointers. */
+typedef struct {
+    kvi_geometry g;
+    int64_t n_facts;           /* N */
+    int64_t n_tokens;          /* rows per (layer, K|V) plane of kv */
+    const void *kv;            /* bf16 [L][2][n_tokens][H][D] */
+    const float *emb;          /* float32 [N][E] */
+    const int64_t *fact_start; /* [N] first store row of each fact */
+    const int32_t *fact_len;   /* [N] tokens of each fact, >= 0 */
+} kvi_store_view;
+
+typedef struct {
+    int64_t n_tokens;      /* total rows = sum of fact_len */
+    size_t kv_bytes;       /* L * 2 * n_tokens * H * D * 2 */
+    size_t emb_bytes;      /* N * E * 4 */
+    size_t offsets_bytes;  /* (N + 1) * 8 */
+} kvi_store_sizes;
+
+/* The engine's paged KV pool (Section 3.4): one device buffer per layer,
+ * each bf16 [2][num_blocks][block_size][H][D].  layer_base is a HOST array
+ * of `layers` device pointers, read during the call only. */
+typedef struct {
+    void *const *layer_base;
+    int32_t layers;
+    int32_t num_blocks;
+    int32_t block_size; /* B, tokens per block */
+} kvi_paged_cache;
+
+/* Store layout (host only, no device work).  Dense CSR layout of a store
+ * whose facts are written back to back: token_offsets_out[i] = sum of
+ * fact_len[0..i), token_offsets_out[n_facts] = n_tokens, plus the byte sizes
+ * of the buffers the caller allocates.  fact_len (host, [n_facts]) must be
+ * >= 0.  token_offsets_out (host, [n_facts + 1]) may be NULL.  Errors:
+ * KVI_ERR_INVALID_ARG for a bad geometry, n_facts < 0 or a negative length. */
+KVI_API kvi_status kvi_store_layout(const kvi_geometry *g, const int32_t *fact_len,
+                            int64_t n_facts, int64_t *token_offsets_out,
+                            kvi_store_sizes *sizes_out);
+
+/* Build (or extend) this device's RoPE table for (rope_theta, head_dim)
+ * covering positions [0, max_position).  cos/sin of p * omega_i are
+ * computed in float64 on the host and kept as hi/lo float32 pairs, so that
+ * the kernels rotate bf16 keys to within one rounding of the exact result at
+ * any position (Section 5.1, Chunked RoPE).  Synchronous; allocates device
+ * memory owned by the library until process exit.  The inject calls build
+ * the table on first use when needed, which blocks the host and is refused
+ * (KVI_ERR_INVALID_ARG) while the stream is being captured; call this first
+ * to keep them asynchronous.  Errors: KVI_ERR_INVALID_ARG (theta <= 0,
+ * head_dim not a multiple of 16, max_position <= 0 or > 2^22),
+ * KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim,
+                            int32_t max_position);
+
+/* Device scratch bytes needed by kvi_retrieve_topk (R = 1) and
+ * kvi_retrieve_and_inject for R requests of at most max_facts facts and k
+ * retrieved facts each.  Returns 0 for invalid sizes. */
+KVI_API size_t kvi_workspace_bytes(int32_t R, int64_t max_facts, int32_t k);
+
+/* Retrieve (Figure 2 caption, "top-k retrieved facts"): score every fact
+ * embedding against d_query ([E] float32, device) and return the exact
+ * top-k under (score descending, fact id ascending).
+ *   d_ids    [k] int32, rank order      d_scores [k] float32 similarity
+ *   d_ws     scratch of >= kvi_workspace_bytes(1, store->n_facts, k) bytes,
+ *            256-byte aligned; its contents need no initialisation.
+ * Errors: KVI_ERR_INVALID_ARG (null pointers, k < 1, k > KVI_MAX_K,
+ * k > n_facts, bad geometry, workspace too small), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query,
+                             int32_t k, int32_t *d_ids, float *d_scores,
+                             void *d_ws, size_t ws_bytes, kvi_stream_t stream);
+
+/* Place (Figure 2 caption, "positioned by chunked RoPE"; rank-order reading):
+ * d_pos[j] = start + sum of fact_len[d_ids[j']] for j' < j.  n <= KVI_MAX_K.
+ * An id outside [0, n_facts) records KVI_ERR_OUT_OF_RANGE in *d_status and
+ * counts as length 0.  Errors: KVI_ERR_INVALID_ARG, KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_place(const kvi_store_view *store, const int32_t *d_ids,
+                     int32_t n, int32_t start, int32_t *d_pos,
+                     int32_t *d_status, kvi_stream_t stream);
+
+/* Inject (Section 5.1 Chunked RoPE + Section 3.4 scatter-copy): for each of
+ * the n facts d_fact_ids[j] ([n] int32, device) and each of its tokens t,
+ * rotate the pre-RoPE K rows of every layer and head to position
+ * p = d_start_pos[j] + t and write K and V (unchanged) into the paged cache
+ * slot (d_block_table[p / B], p % B).  d_block_table: [table_len] int32
+ * device.  Positions must not overlap (overlaps are caller error; the
+ * result is then unspecified).  n <= KVI_MAX_INJECT_FACTS.  Device-side
+ * errors (recorded in *d_status, item skipped): fact id or store row out of
+ * range, p < 0 or p >= table_len * B, block id outside [0, num_blocks).
+ * Errors: KVI_ERR_INVALID_ARG (null pointers, geometry, cache mismatch,
+ * theta <= 0, limits), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_inject_paged(const kvi_store_view *store,
+                            const int32_t *d_fact_ids,
+                            const int32_t *d_start_pos, int32_t n,
+                            const int32_t *d_block_table, int32_t table_len,
+                            const kvi_paged_cache *cache, double rope_theta,
+                            int32_t *d_status, kvi_stream_t stream);
+
+/* Fused retrieve + place + inject for R independent requests (Figure 2
+ * serving path; Section 6.4's concurrent users).  Request r scores its own
+ * store d_stores[r] (device array of R kvi_store_view, all with geometry g)
+ * against d_queries[r] ([R][E] float32), keeps the top-k, places them back
+ * to back from d_start_pos[r] and injects them through block table row r
+ * (d_block_tables [R][max_blocks] int32, d_table_lens [R] int32 <=
+ * max_blocks).  Outputs: d_ids, d_scores, d_pos, each [R][k] (rank order).
+ *   max_facts  host upper bound of every store's n_facts (sizes the grid);
+ *   d_ws       >= kvi_workspace_bytes(R, max_facts, k) bytes, 256-aligned,
+ *              no initialisation needed.
+ * Device-side errors, recorded in *d_status: a store with n_facts < k or
+ * > max_facts, another geometry, or a bad fact extent (KVI_ERR_OUT_OF_RANGE;
+ * that request retrieves nothing); facts that do not fit the request's
+ * block table (KVI_ERR_CAPACITY; that request injects nothing); block ids
+ * outside the pool (KVI_ERR_OUT_OF_RANGE; that token is skipped).
+ * Errors: KVI_ERR_INVALID_ARG, KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_retrieve_and_inject(
+    const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+    int64_t max_facts, const float *d_queries, int32_t k,
+    const int32_t *d_start_pos, const int32_t *d_block_tables,
+    const int32_t *d_table_lens, int32_t max_blocks,
+    const kvi_paged_cache *cache, double rope_theta, int32_t *d_ids,
+    float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
+    int32_t *d_status, kvi_stream_t stream);
+
+/* Tracing: when n_events == 3, the calling thread's next
+ * kvi_retrieve_and_inject calls record events[0] before the first kernel,
+ * events[1] once retrieval and placement are enqueued and events[2] after
+ * the inject kernel, on the call's stream, so that the stages can be timed
+ * with cudaEventElapsedTime.  n_events == 0 turns tracing off.  The events
+ * are created and owned by the caller.  Errors: KVI_ERR_INVALID_ARG. */
+KVI_API kvi_status kvi_trace_stages(const kvi_event_t *events, int32_t n_events);
+
+/* Static description of a status code. */
+KVI_API const char *kvi_status_str(kvi_status s);
+
+/* Message of the calling thread's last failing call ("" if none). */
+KVI_API const char *kvi_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVI_H */

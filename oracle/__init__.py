@@ -71,6 +71,8 @@ def _load():
         lib.kvo_rotate.restype = None
         lib.kvo_slot.argtypes = [i64, P, i32, i32, i32, P, P]
         lib.kvo_slot.restype = ctypes.c_int
+        lib.kvo_slots.argtypes = [P, i64, P, i32, i32, i32, P, P]
+        lib.kvo_slots.restype = None
         lib.kvo_token_rows.argtypes = [P, i32, i32, i32, i64, i64, f64, i64, P, P]
         lib.kvo_token_rows.restype = ctypes.c_int
         lib.kvo_inject_expected.argtypes = [
@@ -150,6 +152,17 @@ def slot(p: int, block_table: np.ndarray, block_size: int, num_blocks: int):
     rc = _load().kvo_slot(int(p), _p(bt), bt.shape[0], int(block_size),
                           int(num_blocks), ctypes.byref(blk), ctypes.byref(off))
     return None if rc != OK else (blk.value, off.value)
+
+
+def slots(positions, block_table, block_size: int, num_blocks: int):
+    """(blk[n], off[n]) int32 arrays for many positions; -1 where out of range."""
+    p = _c(positions, np.int64)
+    bt = _c(block_table, np.int32)
+    blk = np.empty(p.shape[0], np.int32)
+    off = np.empty(p.shape[0], np.int32)
+    _load().kvo_slots(_p(p), p.shape[0], _p(bt), bt.shape[0], int(block_size),
+                      int(num_blocks), _p(blk), _p(off))
+    return blk, off
 
 
 def token_rows(kv_bits: np.ndarray, row: int, theta: float, p: int):

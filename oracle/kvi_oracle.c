@@ -280,3 +280,18 @@ int64_t kvo_request(const float *q, const float *emb, int64_t n_facts, int64_t e
     }
     return tok;
 }
+
+/* kvo_slot over n positions (for checking large pools): blk[i], off[i] of
+ * position p[i], or -1/-1 when it is out of range. */
+void kvo_slots(const int64_t *p, int64_t n, const int32_t *block_table,
+               int32_t table_len, int32_t block_size, int32_t num_blocks,
+               int32_t *blk, int32_t *off)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        if (kvo_slot(p[i], block_table, table_len, block_size, num_blocks,
+                     &blk[i], &off[i]) != KVO_OK) {
+            blk[i] = -1;
+            off[i] = -1;
+        }
+    }
+}

@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) retrieve-and-inject library for pre-RoPE KV facts.
+
+Serving-time path of "InferScale: GPU-Native KV Injection for Personalized
+LLM Serving": exact top-k retrieval of memory facts by embedding similarity
+(Figure 2 caption), Chunked RoPE rotation of their pre-RoPE keys to the
+prompt positions they take (Section 5.1 / Theorem 6), and scatter-copy of K/V
+into a vLLM-style paged KV cache through a block table (Section 3.4).
+
+The compute is in ``libkvi.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/kvi.h``); this package is a ctypes binding with the same function
+names.  Build the library with ``pre_rope_kv_gb300.build.build()``.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED_SYMBOLS, ERR_CAPACITY, ERR_CUDA, ERR_INVALID_ARG, ERR_OUT_OF_RANGE, LIB_PATH,
+    MAX_INJECT_FACTS, MAX_K, MAX_LAYERS, OK, Geometry, KviError, PagedCache, StoreSizes,
+    StoreView, geometry, kvi_inject_paged, kvi_last_error, kvi_place, kvi_prepare_rope,
+    kvi_retrieve_and_inject, kvi_retrieve_topk, kvi_status_str, kvi_store_layout,
+    kvi_trace_stages, kvi_workspace_bytes, load_library, pack_store_views, paged_cache,
+    store_view,
+)

@@ -1,0 +1,232 @@
+"""ctypes binding of libkvi (include/kvi.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: it turns torch tensors into device pointers,
+Python numbers into C scalars, and raises KviError when the library returns
+a non-zero status.  All compute runs in libkvi's CUDA kernels.  There is no
+fallback: if the library is missing or fails to load, the import of this
+module's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+from . import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_OUT_OF_RANGE = 2
+ERR_CAPACITY = 3
+ERR_CUDA = 4
+
+MAX_LAYERS = 128
+MAX_K = 256
+MAX_INJECT_FACTS = 4096
+
+EXPORTED_SYMBOLS = (
+    "kvi_store_layout", "kvi_prepare_rope", "kvi_workspace_bytes", "kvi_retrieve_topk",
+    "kvi_place", "kvi_inject_paged", "kvi_retrieve_and_inject", "kvi_trace_stages",
+    "kvi_status_str", "kvi_last_error",
+)
+
+
+class KviError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: status {status} ({message})")
+        self.status = status
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("embed_dim", ctypes.c_int32)]
+
+
+class StoreView(ctypes.Structure):
+    _fields_ = [("g", Geometry), ("n_facts", ctypes.c_int64), ("n_tokens", ctypes.c_int64),
+                ("kv", ctypes.c_void_p), ("emb", ctypes.c_void_p),
+                ("fact_start", ctypes.c_void_p), ("fact_len", ctypes.c_void_p)]
+
+
+class StoreSizes(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int64), ("kv_bytes", ctypes.c_size_t),
+                ("emb_bytes", ctypes.c_size_t), ("offsets_bytes", ctypes.c_size_t)]
+
+
+class PagedCache(ctypes.Structure):
+    _fields_ = [("layer_base", ctypes.POINTER(ctypes.c_void_p)), ("layers", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libkvi.so (built by pre_rope_kv_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libkvi is not built ({p} missing): run pre_rope_kv_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    P, i32, i64, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
+                           ctypes.c_size_t)
+    S = ctypes.c_int
+    sig = {
+        "kvi_store_layout": (S, [ctypes.POINTER(Geometry), P, i64, P, ctypes.POINTER(StoreSizes)]),
+        "kvi_prepare_rope": (S, [f64, i32, i32]),
+        "kvi_workspace_bytes": (sz, [i32, i64, i32]),
+        "kvi_retrieve_topk": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P, sz, P]),
+        "kvi_place": (S, [ctypes.POINTER(StoreView), P, i32, i32, P, P, P]),
+        "kvi_inject_paged": (S, [ctypes.POINTER(StoreView), P, P, i32, P, i32,
+                                 ctypes.POINTER(PagedCache), f64, P, P]),
+        "kvi_retrieve_and_inject": (S, [ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P, P,
+                                        i32, ctypes.POINTER(PagedCache), f64, P, P, P, P, sz,
+                                        P, P]),
+        "kvi_trace_stages": (S, [P, i32]),
+        "kvi_status_str": (ctypes.c_char_p, [S]),
+        "kvi_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        lib = load_library()
+        raise KviError(status, where, lib.kvi_last_error().decode() or
+                       lib.kvi_status_str(status).decode())
+
+
+def _ptr(t) -> int | None:
+    """Device (or host) address of a tensor, or None."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- helpers
+
+def geometry(layers: int, kv_heads: int, head_dim: int, embed_dim: int) -> Geometry:
+    return Geometry(layers, kv_heads, head_dim, embed_dim)
+
+
+def store_view(g: Geometry, kv, emb, fact_start, fact_len, n_tokens: int | None = None) -> StoreView:
+    """Describe a store held in torch tensors (kv bf16 [L][2][T][H][D],
+    emb float32 [N][E], fact_start int64 [N], fact_len int32 [N])."""
+    n_facts = (emb.shape[0] if emb is not None else fact_len.shape[0])
+    T = n_tokens if n_tokens is not None else (kv.shape[2] if kv is not None else 0)
+    return StoreView(g, n_facts, T, _ptr(kv), _ptr(emb), _ptr(fact_start), _ptr(fact_len))
+
+
+def pack_store_views(views: Sequence[StoreView]) -> bytes:
+    """Bytes of an array of kvi_store_view, to copy into device memory for
+    kvi_retrieve_and_inject."""
+    arr = (StoreView * len(views))(*views)
+    return ctypes.string_at(ctypes.addressof(arr), ctypes.sizeof(arr))
+
+
+class _Cache:
+    """Keeps the host array of layer pointers alive next to the struct."""
+
+    def __init__(self, layer_tensors, block_size: int):
+        ptrs = [t.data_ptr() for t in layer_tensors]
+        self._arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        nb = layer_tensors[0].shape[1]
+        self.struct = PagedCache(ctypes.cast(self._arr, ctypes.POINTER(ctypes.c_void_p)),
+                                 len(ptrs), nb, block_size)
+        self.layer_tensors = list(layer_tensors)
+
+
+def paged_cache(layer_tensors, block_size: int) -> _Cache:
+    """Describe a paged pool: one bf16 tensor [2][num_blocks][B][H][D] per layer."""
+    return _Cache(layer_tensors, block_size)
+
+
+# ------------------------------------------------------------- entry points
+
+def kvi_store_layout(g: Geometry, fact_len):
+    """Host-only CSR layout: returns (token_offsets list[int], StoreSizes)."""
+    lib = load_library()
+    n = len(fact_len)
+    lens = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in fact_len])
+    offs = (ctypes.c_int64 * (n + 1))()
+    sizes = StoreSizes()
+    _check(lib.kvi_store_layout(ctypes.byref(g), lens, n, offs, ctypes.byref(sizes)),
+           "kvi_store_layout")
+    return list(offs), sizes
+
+
+def kvi_prepare_rope(rope_theta: float, head_dim: int, max_position: int) -> None:
+    _check(load_library().kvi_prepare_rope(float(rope_theta), int(head_dim), int(max_position)),
+           "kvi_prepare_rope")
+
+
+def kvi_workspace_bytes(R: int, max_facts: int, k: int) -> int:
+    return int(load_library().kvi_workspace_bytes(int(R), int(max_facts), int(k)))
+
+
+def kvi_retrieve_topk(store: StoreView, query, k: int, ids, scores, ws, stream=None) -> None:
+    _check(load_library().kvi_retrieve_topk(
+        ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)), "kvi_retrieve_topk")
+
+
+def kvi_place(store: StoreView, ids, n: int, start: int, pos, status=None, stream=None) -> None:
+    _check(load_library().kvi_place(ctypes.byref(store), _ptr(ids), int(n), int(start), _ptr(pos),
+                                    _ptr(status), _stream(stream)), "kvi_place")
+
+
+def kvi_inject_paged(store: StoreView, fact_ids, start_pos, n: int, block_table, table_len: int,
+                     cache: _Cache, rope_theta: float, status=None, stream=None) -> None:
+    _check(load_library().kvi_inject_paged(
+        ctypes.byref(store), _ptr(fact_ids), _ptr(start_pos), int(n), _ptr(block_table),
+        int(table_len), ctypes.byref(cache.struct), float(rope_theta), _ptr(status),
+        _stream(stream)), "kvi_inject_paged")
+
+
+def kvi_retrieve_and_inject(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,
+                            start_pos, block_tables, table_lens, max_blocks: int, cache: _Cache,
+                            rope_theta: float, ids, scores, pos, ws, status=None,
+                            stream=None) -> None:
+    _check(load_library().kvi_retrieve_and_inject(
+        ctypes.byref(g), int(R), _ptr(stores_dev), int(max_facts), _ptr(queries), int(k),
+        _ptr(start_pos), _ptr(block_tables), _ptr(table_lens), int(max_blocks),
+        ctypes.byref(cache.struct), float(rope_theta), _ptr(ids), _ptr(scores), _ptr(pos),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+        "kvi_retrieve_and_inject")
+
+
+def kvi_trace_stages(events) -> None:
+    """events: three torch.cuda.Event (enable_timing=True), or [] to stop."""
+    lib = load_library()
+    if not events:
+        _check(lib.kvi_trace_stages(None, 0), "kvi_trace_stages")
+        return
+    handles = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    _check(lib.kvi_trace_stages(handles, 3), "kvi_trace_stages")
+
+
+def kvi_status_str(status: int) -> str:
+    return load_library().kvi_status_str(int(status)).decode()
+
+
+def kvi_last_error() -> str:
+    return load_library().kvi_last_error().decode()

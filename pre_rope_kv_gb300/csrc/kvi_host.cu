@@ -1,0 +1,542 @@
+// kvi_host.cu -- the C ABI: argument validation, workspace layout, the
+// per-device RoPE table, and the launch sequences of the four calls.
+//
+// Path ("InferScale: GPU-Native KV Injection for Personalized LLM Serving"):
+// retrieve the top-k facts for a query (Figure 2 caption), position them by
+// Chunked RoPE (Section 5.1 / Theorem 6) and scatter-copy their K/V into the
+// engine's paged blocks (Section 3.4).  Every step runs in this library's
+// kernels; the host only validates, sizes grids and enqueues.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "kvi_internal.cuh"
+
+namespace kvi {
+cudaError_t inject_occupancy(int *ctas_per_sm);
+}
+
+using namespace kvi;
+
+namespace {
+
+constexpr int32_t kMaxRopePositions = 1 << 22;
+
+thread_local std::string t_last_error;
+thread_local cudaEvent_t t_trace[3] = {nullptr, nullptr, nullptr};
+thread_local int t_trace_n = 0;
+
+kvi_status fail(kvi_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+#define KVI_CUDA(call)                                                              \
+    do {                                                                            \
+        const cudaError_t e_ = (call);                                              \
+        if (e_ != cudaSuccess)                                                      \
+            return fail(KVI_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));     \
+    } while (0)
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvi_status check_geometry(const kvi_geometry *g)
+{
+    if (!g) return fail(KVI_ERR_INVALID_ARG, "geometry is NULL");
+    if (g->layers < 1 || g->layers > KVI_MAX_LAYERS)
+        return fail(KVI_ERR_INVALID_ARG, "layers=%d outside [1, %d]", g->layers, KVI_MAX_LAYERS);
+    if (g->kv_heads < 1 || g->kv_heads > 4096)
+        return fail(KVI_ERR_INVALID_ARG, "kv_heads=%d outside [1, 4096]", g->kv_heads);
+    if (g->head_dim < 16 || g->head_dim > KVI_MAX_HEAD_DIM || g->head_dim % 16)
+        return fail(KVI_ERR_INVALID_ARG, "head_dim=%d must be a multiple of 16 in [16, %d]",
+                    g->head_dim, KVI_MAX_HEAD_DIM);
+    if (g->embed_dim < 4 || g->embed_dim > KVI_MAX_EMBED_DIM || g->embed_dim % 4)
+        return fail(KVI_ERR_INVALID_ARG, "embed_dim=%d must be a multiple of 4 in [4, %d]",
+                    g->embed_dim, KVI_MAX_EMBED_DIM);
+    return KVI_OK;
+}
+
+kvi_status check_store(const kvi_store_view *s, bool retrieval, bool inject)
+{
+    if (!s) return fail(KVI_ERR_INVALID_ARG, "store is NULL");
+    kvi_status st = check_geometry(&s->g);
+    if (st != KVI_OK) return st;
+    if (s->n_facts < 1 || s->n_facts > 0x7fffffff)
+        return fail(KVI_ERR_INVALID_ARG, "n_facts=%lld outside [1, 2^31)", (long long)s->n_facts);
+    if (s->n_tokens < 0) return fail(KVI_ERR_INVALID_ARG, "n_tokens < 0");
+    if (retrieval && (!s->emb || !aligned(s->emb, 16)))
+        return fail(KVI_ERR_INVALID_ARG, "emb must be a 16-byte aligned device pointer");
+    if ((inject || !retrieval) && (!s->fact_len))
+        return fail(KVI_ERR_INVALID_ARG, "fact_len is NULL");
+    if (inject && (!s->kv || !aligned(s->kv, 16) || !s->fact_start))
+        return fail(KVI_ERR_INVALID_ARG, "kv (16-byte aligned) and fact_start are required");
+    return KVI_OK;
+}
+
+kvi_status check_cache(const kvi_paged_cache *c, const kvi_geometry &g)
+{
+    if (!c || !c->layer_base) return fail(KVI_ERR_INVALID_ARG, "cache or cache->layer_base is NULL");
+    if (c->layers != g.layers)
+        return fail(KVI_ERR_INVALID_ARG, "cache has %d layers, store %d", c->layers, g.layers);
+    if (c->num_blocks < 1 || c->block_size < 1)
+        return fail(KVI_ERR_INVALID_ARG, "num_blocks and block_size must be >= 1");
+    for (int l = 0; l < c->layers; ++l)
+        if (!c->layer_base[l] || !aligned(c->layer_base[l], 16))
+            return fail(KVI_ERR_INVALID_ARG, "layer_base[%d] is NULL or not 16-byte aligned", l);
+    return KVI_OK;
+}
+
+// ------------------------------------------------------------- device facts
+
+std::mutex g_dev_mu;
+std::vector<DeviceInfo> g_dev;  // indexed by device ordinal; sms == 0 = unknown
+
+// ---------------------------------------------------------------- RoPE table
+
+struct RopeEntry {
+    int device;
+    double theta;
+    int32_t head_dim;
+    int32_t positions;
+    float4 *table;
+};
+std::mutex g_rope_mu;
+std::vector<RopeEntry> g_rope;
+
+// Round a double to 16 significant bits (head) and keep the float32 tail.
+void split16(double x, float &hi, float &lo)
+{
+    float f = (float)x;
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    u = (u + 0x80u) & 0xffffff00u;
+    std::memcpy(&hi, &u, 4);
+    lo = (float)(x - (double)hi);
+}
+
+void fill_rope_rows(double theta, int32_t D, int32_t p0, int32_t p1, float4 *out)
+{
+    const int32_t half = D / 2;
+    std::vector<double> omega(half);
+    for (int32_t i = 0; i < half; ++i) omega[i] = std::pow(theta, -2.0 * (double)i / (double)D);
+    for (int32_t p = p0; p < p1; ++p) {
+        for (int32_t i = 0; i < half; ++i) {
+            const double a = (double)p * omega[i];
+            float4 e;
+            split16(std::cos(a), e.x, e.y);
+            split16(std::sin(a), e.z, e.w);
+            out[(size_t)p * half + i] = e;
+        }
+    }
+}
+
+// Returns the table of the current device covering >= needed positions.
+kvi_status rope_get(double theta, int32_t D, int32_t needed, cudaStream_t stream,
+                    const float4 **table, int32_t *positions)
+{
+    int dev = 0;
+    KVI_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lock(g_rope_mu);
+    RopeEntry *hit = nullptr;
+    for (auto &e : g_rope)
+        if (e.device == dev && e.theta == theta && e.head_dim == D) hit = &e;
+    if (hit && hit->positions >= needed) {
+        *table = hit->table;
+        *positions = hit->positions;
+        return KVI_OK;
+    }
+    if (stream) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        KVI_CUDA(cudaStreamIsCapturing(stream, &cap));
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(KVI_ERR_INVALID_ARG,
+                        "RoPE table for theta=%g, D=%d, %d positions is missing during stream "
+                        "capture; call kvi_prepare_rope first", theta, D, needed);
+    }
+    const int32_t P = std::min(kMaxRopePositions, ((needed + 1023) / 1024) * 1024);
+    const int32_t half = D / 2;
+    std::vector<float4> host((size_t)P * half);
+    const unsigned hw = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+    const int32_t nthr = (int32_t)std::min<unsigned>(hw, (unsigned)((P + 1023) / 1024));
+    std::vector<std::thread> pool;
+    for (int32_t t = 0; t < nthr; ++t) {
+        const int32_t a = (int32_t)((int64_t)P * t / nthr), b = (int32_t)((int64_t)P * (t + 1) / nthr);
+        pool.emplace_back(fill_rope_rows, theta, D, a, b, host.data());
+    }
+    for (auto &th : pool) th.join();
+    float4 *d = nullptr;
+    KVI_CUDA(cudaMalloc(&d, host.size() * sizeof(float4)));
+    const cudaError_t ce = cudaMemcpy(d, host.data(), host.size() * sizeof(float4), cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) {
+        cudaFree(d);
+        return fail(KVI_ERR_CUDA, "RoPE table upload: %s", cudaGetErrorString(ce));
+    }
+    if (hit) {
+        // The old table may still be read by enqueued kernels.
+        KVI_CUDA(cudaDeviceSynchronize());
+        KVI_CUDA(cudaFree(hit->table));
+        hit->table = d;
+        hit->positions = P;
+    } else {
+        g_rope.push_back(RopeEntry{dev, theta, D, P, d});
+    }
+    *table = d;
+    *positions = P;
+    return KVI_OK;
+}
+
+int32_t clamp_rope(int64_t needed)
+{
+    return (int32_t)std::max<int64_t>(1, std::min<int64_t>(needed, kMaxRopePositions));
+}
+
+}  // namespace
+
+// --------------------------------------------------------------- internals
+
+namespace kvi {
+
+cudaError_t device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1, DeviceInfo{0, 0});
+    if (g_dev[dev].sms == 0) {
+        int sms = 0, occ = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = inject_occupancy(&occ);
+        if (e != cudaSuccess) return e;
+        g_dev[dev] = DeviceInfo{sms, std::max(1, occ)};
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+WsLayout ws_layout(int32_t R, int64_t max_facts, int32_t k)
+{
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    WsLayout w{};
+    size_t at = 0;
+    w.hist = at;    at = up(at + (size_t)R * kHistBins * 4);
+    w.counter = at; at = up(at + 4);
+    w.keys = at;
+    w.key_stride = (max_facts + 31) & ~(int64_t)31;
+    at = up(at + (size_t)R * (size_t)w.key_stride * 8);
+    w.cum = at;     at = up(at + (size_t)R * (size_t)(k + 1) * 4);
+    w.tok = at;     at = up(at + (size_t)R * 8);
+    w.req_off = at; at = up(at + (size_t)(R + 1) * 8);
+    w.total = at;
+    return w;
+}
+
+}  // namespace kvi
+
+// ------------------------------------------------------------------ the ABI
+
+extern "C" {
+
+const char *kvi_status_str(kvi_status s)
+{
+    switch (s) {
+    case KVI_OK: return "ok";
+    case KVI_ERR_INVALID_ARG: return "invalid argument";
+    case KVI_ERR_OUT_OF_RANGE: return "index out of range";
+    case KVI_ERR_CAPACITY: return "facts do not fit the block table";
+    case KVI_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char *kvi_last_error(void) { return t_last_error.c_str(); }
+
+kvi_status kvi_store_layout(const kvi_geometry *g, const int32_t *fact_len, int64_t n_facts,
+                            int64_t *token_offsets_out, kvi_store_sizes *sizes_out)
+{
+    kvi_status st = check_geometry(g);
+    if (st != KVI_OK) return st;
+    if (n_facts < 0 || (n_facts > 0 && !fact_len) || !sizes_out)
+        return fail(KVI_ERR_INVALID_ARG, "n_facts < 0, fact_len or sizes_out NULL");
+    int64_t run = 0;
+    for (int64_t i = 0; i < n_facts; ++i) {
+        if (fact_len[i] < 0) return fail(KVI_ERR_INVALID_ARG, "fact_len[%lld] < 0", (long long)i);
+        if (token_offsets_out) token_offsets_out[i] = run;
+        run += fact_len[i];
+    }
+    if (token_offsets_out) token_offsets_out[n_facts] = run;
+    sizes_out->n_tokens = run;
+    sizes_out->kv_bytes = (size_t)g->layers * 2 * (size_t)run * g->kv_heads * g->head_dim * 2;
+    sizes_out->emb_bytes = (size_t)n_facts * g->embed_dim * 4;
+    sizes_out->offsets_bytes = (size_t)(n_facts + 1) * 8;
+    return KVI_OK;
+}
+
+kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim, int32_t max_position)
+{
+    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
+        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    if (head_dim < 16 || head_dim > KVI_MAX_HEAD_DIM || head_dim % 16)
+        return fail(KVI_ERR_INVALID_ARG, "head_dim=%d must be a multiple of 16 in [16, %d]",
+                    head_dim, KVI_MAX_HEAD_DIM);
+    if (max_position <= 0 || max_position > kMaxRopePositions)
+        return fail(KVI_ERR_INVALID_ARG, "max_position=%d outside [1, 2^22]", max_position);
+    const float4 *t;
+    int32_t n;
+    return rope_get(rope_theta, head_dim, max_position, nullptr, &t, &n);
+}
+
+size_t kvi_workspace_bytes(int32_t R, int64_t max_facts, int32_t k)
+{
+    if (R < 1 || R > kMaxRequests || max_facts < 1 || max_facts > 0x7fffffff || k < 1 ||
+        k > KVI_MAX_K)
+        return 0;
+    return ws_layout(R, max_facts, k).total;
+}
+
+kvi_status kvi_trace_stages(const kvi_event_t *events, int32_t n_events)
+{
+    if (n_events == 0) {
+        t_trace_n = 0;
+        return KVI_OK;
+    }
+    if (n_events != 3 || !events || !events[0] || !events[1] || !events[2])
+        return fail(KVI_ERR_INVALID_ARG, "kvi_trace_stages wants 3 events or 0");
+    for (int i = 0; i < 3; ++i) t_trace[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+    t_trace_n = 3;
+    return KVI_OK;
+}
+
+kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, int32_t k,
+                             int32_t *d_ids, float *d_scores, void *d_ws, size_t ws_bytes,
+                             kvi_stream_t stream)
+{
+    kvi_status st = check_store(store, true, false);
+    if (st != KVI_OK) return st;
+    if (!d_query || !aligned(d_query, 16))
+        return fail(KVI_ERR_INVALID_ARG, "query must be a 16-byte aligned device pointer");
+    if (k < 1 || k > KVI_MAX_K || (int64_t)k > store->n_facts)
+        return fail(KVI_ERR_INVALID_ARG, "k=%d outside [1, min(%d, n_facts=%lld)]", k, KVI_MAX_K,
+                    (long long)store->n_facts);
+    if (!d_ids || !d_scores) return fail(KVI_ERR_INVALID_ARG, "ids or scores is NULL");
+    const WsLayout w = ws_layout(1, store->n_facts, k);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < w.total)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", w.total);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(d_ws);
+    KVI_CUDA(cudaMemsetAsync(ws, 0, ws_zero_bytes(w), s));
+
+    ScoreParams sp{};
+    sp.store.single = *store;
+    sp.store.many = nullptr;
+    sp.queries = d_query;
+    sp.g = store->g;
+    sp.R = 1;
+    sp.max_facts = store->n_facts;
+    sp.rows_per_cta = (kScoreThreads / 32) * kScoreRowsPerWarp;
+    sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
+    sp.key_stride = w.key_stride;
+    sp.hist = reinterpret_cast<uint32_t *>(ws + w.hist);
+    KVI_CUDA(launch_score(sp, s));
+
+    SelectParams lp{};
+    lp.store = sp.store;
+    lp.g = store->g;
+    lp.R = 1;
+    lp.k = k;
+    lp.max_facts = store->n_facts;
+    lp.key_stride = w.key_stride;
+    lp.keys = sp.keys;
+    lp.hist = sp.hist;
+    lp.ids = d_ids;
+    lp.scores = d_scores;
+    lp.place = 0;
+    KVI_CUDA(launch_select(lp, s));
+    return KVI_OK;
+}
+
+kvi_status kvi_place(const kvi_store_view *store, const int32_t *d_ids, int32_t n, int32_t start,
+                     int32_t *d_pos, int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_store(store, false, false);
+    if (st != KVI_OK) return st;
+    if (n < 1 || n > KVI_MAX_K) return fail(KVI_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, KVI_MAX_K);
+    if (!d_ids || !d_pos) return fail(KVI_ERR_INVALID_ARG, "ids or pos is NULL");
+    if (start < 0) return fail(KVI_ERR_INVALID_ARG, "start < 0");
+    PlaceParams pp{};
+    pp.store = *store;
+    pp.ids = d_ids;
+    pp.n = n;
+    pp.start = start;
+    pp.pos = d_pos;
+    pp.status = d_status;
+    KVI_CUDA(launch_place(pp, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_ids,
+                            const int32_t *d_start_pos, int32_t n, const int32_t *d_block_table,
+                            int32_t table_len, const kvi_paged_cache *cache, double rope_theta,
+                            int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_store(store, false, true);
+    if (st != KVI_OK) return st;
+    if (n < 1 || n > KVI_MAX_INJECT_FACTS)
+        return fail(KVI_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, KVI_MAX_INJECT_FACTS);
+    if (!d_fact_ids || !d_start_pos || !d_block_table)
+        return fail(KVI_ERR_INVALID_ARG, "fact ids, start positions or block table is NULL");
+    if (table_len < 1) return fail(KVI_ERR_INVALID_ARG, "table_len < 1");
+    st = check_cache(cache, store->g);
+    if (st != KVI_OK) return st;
+    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
+        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float4 *table;
+    int32_t positions;
+    st = rope_get(rope_theta, store->g.head_dim,
+                  clamp_rope((int64_t)table_len * cache->block_size), s, &table, &positions);
+    if (st != KVI_OK) return st;
+
+    InjectParams ip{};
+    ip.store.single = *store;
+    ip.store.many = nullptr;
+    ip.L = store->g.layers;
+    ip.H = store->g.kv_heads;
+    ip.D = store->g.head_dim;
+    ip.fused = 0;
+    ip.ids = d_fact_ids;
+    ip.pos = d_start_pos;
+    ip.n = n;
+    ip.block_tables = d_block_table;
+    ip.table_len = table_len;
+    ip.num_blocks = cache->num_blocks;
+    ip.block_size = cache->block_size;
+    ip.rope = table;
+    ip.rope_positions = positions;
+    ip.status = d_status;
+    for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
+    KVI_CUDA(launch_inject(ip, s));
+    return KVI_OK;
+}
+
+kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+                                   int64_t max_facts, const float *d_queries, int32_t k,
+                                   const int32_t *d_start_pos, const int32_t *d_block_tables,
+                                   const int32_t *d_table_lens, int32_t max_blocks,
+                                   const kvi_paged_cache *cache, double rope_theta, int32_t *d_ids,
+                                   float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
+                                   int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_geometry(g);
+    if (st != KVI_OK) return st;
+    if (R < 1 || R > kMaxRequests) return fail(KVI_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, kMaxRequests);
+    if (!d_stores || !aligned(d_stores, 8)) return fail(KVI_ERR_INVALID_ARG, "stores array is NULL or misaligned");
+    if (k < 1 || k > KVI_MAX_K) return fail(KVI_ERR_INVALID_ARG, "k=%d outside [1, %d]", k, KVI_MAX_K);
+    if (max_facts < k || max_facts > 0x7fffffff)
+        return fail(KVI_ERR_INVALID_ARG, "max_facts=%lld outside [k, 2^31)", (long long)max_facts);
+    if (!d_queries || !aligned(d_queries, 16) || (g->embed_dim * 4) % 16)
+        return fail(KVI_ERR_INVALID_ARG, "queries must be 16-byte aligned rows");
+    if (!d_start_pos || !d_block_tables || !d_table_lens)
+        return fail(KVI_ERR_INVALID_ARG, "start positions, block tables or table lengths is NULL");
+    if (max_blocks < 1) return fail(KVI_ERR_INVALID_ARG, "max_blocks < 1");
+    st = check_cache(cache, *g);
+    if (st != KVI_OK) return st;
+    if ((int64_t)max_blocks * cache->block_size > 0x7fffffff)
+        return fail(KVI_ERR_INVALID_ARG, "max_blocks * block_size must be < 2^31");
+    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
+        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    if (!d_ids || !d_scores || !d_pos) return fail(KVI_ERR_INVALID_ARG, "ids, scores or pos is NULL");
+    const WsLayout w = ws_layout(R, max_facts, k);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < w.total)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", w.total);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float4 *table;
+    int32_t positions;
+    st = rope_get(rope_theta, g->head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), s,
+                  &table, &positions);
+    if (st != KVI_OK) return st;
+
+    const bool trace = t_trace_n == 3;
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[0], s));
+    char *ws = static_cast<char *>(d_ws);
+    KVI_CUDA(cudaMemsetAsync(ws, 0, ws_zero_bytes(w), s));
+
+    ScoreParams sp{};
+    sp.store.many = d_stores;
+    sp.queries = d_queries;
+    sp.g = *g;
+    sp.R = R;
+    sp.max_facts = max_facts;
+    sp.rows_per_cta = (kScoreThreads / 32) * kScoreRowsPerWarp;
+    sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
+    sp.key_stride = w.key_stride;
+    sp.hist = reinterpret_cast<uint32_t *>(ws + w.hist);
+    KVI_CUDA(launch_score(sp, s));
+
+    SelectParams lp{};
+    lp.store = sp.store;
+    lp.g = *g;
+    lp.R = R;
+    lp.k = k;
+    lp.max_facts = max_facts;
+    lp.key_stride = w.key_stride;
+    lp.keys = sp.keys;
+    lp.hist = sp.hist;
+    lp.ids = d_ids;
+    lp.scores = d_scores;
+    lp.place = 1;
+    lp.start_pos = d_start_pos;
+    lp.table_lens = d_table_lens;
+    lp.max_blocks = max_blocks;
+    lp.block_size = cache->block_size;
+    lp.pos = d_pos;
+    lp.cum = reinterpret_cast<int32_t *>(ws + w.cum);
+    lp.tok = reinterpret_cast<int64_t *>(ws + w.tok);
+    lp.req_off = reinterpret_cast<int64_t *>(ws + w.req_off);
+    lp.counter = reinterpret_cast<uint32_t *>(ws + w.counter);
+    lp.status = d_status;
+    KVI_CUDA(launch_select(lp, s));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
+
+    InjectParams ip{};
+    ip.store.many = d_stores;
+    ip.L = g->layers;
+    ip.H = g->kv_heads;
+    ip.D = g->head_dim;
+    ip.fused = 1;
+    ip.ids = d_ids;
+    ip.pos = d_pos;
+    ip.R = R;
+    ip.k = k;
+    ip.cum = lp.cum;
+    ip.req_off = lp.req_off;
+    ip.block_tables = d_block_tables;
+    ip.table_lens = d_table_lens;
+    ip.max_blocks = max_blocks;
+    ip.num_blocks = cache->num_blocks;
+    ip.block_size = cache->block_size;
+    ip.rope = table;
+    ip.rope_positions = positions;
+    ip.status = d_status;
+    for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
+    KVI_CUDA(launch_inject(ip, s));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[2], s));
+    return KVI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+"""GPU parity at the full sizes of the serving workloads, in the launch
+configuration the benchmark times (one fused kvi_retrieve_and_inject call
+over all requests).
+
+At these sizes the oracle checks: every request's selected ids (bit-exact),
+scores and placements in full; a sample of injected tokens (all layers, K and
+V, including each request's first and last token) element by element; and,
+for the whole pool, that exactly the rows the oracle's placement maps tokens
+to were written in every layer and every other row kept its canary.
+
+Workloads ("InferScale: GPU-Native KV Injection for Personalized LLM
+Serving" serving setting, synthetic stand-ins for its LoCoMo stores):
+Llama-3-8B KV geometry with 10k facts (k = 5..50); 64 concurrent requests
+over their own 5k-fact stores; Mistral-7B geometry with 50k facts of 8-128
+tokens placed at random bases up to 32k (theta 1e6); Llama-3-70B geometry,
+256 requests, pool of about 150 GB.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from tests import kvi_check as kc
+from tests import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    kc.ensure_built()
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _run_and_check(b, k, samples):
+    f = kc.Fused(b, k)
+    f()
+    ids, scores, pos, status = f.results()
+    assert status == 0, f"device status {status}"
+    orc = kc.oracle_select(b, k)
+    kc.check_selection(ids, scores, pos, orc)
+    place = kc.placements_from_oracle(orc)
+    n = kc.check_pool_sampled(b, place, samples, seed=k)
+    kc.check_canaries_by_row(b, place)
+    return n
+
+
+def test_llama3_8b_10k_k_sweep():
+    b = synth.build_workload(synth.WORKLOADS["llama3_8b_10k"])
+    try:
+        for k in (5, 10, 20, 50):
+            synth.fill_canary(b.pool)
+            _run_and_check(b, k, 300)
+    finally:
+        del b
+        _free()
+
+
+def test_concurrent_64x5k():
+    b = synth.build_workload(synth.WORKLOADS["concurrent_64x5k"])
+    try:
+        for k in (5, 50):
+            synth.fill_canary(b.pool)
+            _run_and_check(b, k, 600)
+    finally:
+        del b
+        _free()
+
+
+def test_mistral_long_placement_50k():
+    b = synth.build_workload(synth.WORKLOADS["mistral_long_50k"])
+    try:
+        assert int(b.start_pos[0]) < 32768
+        _run_and_check(b, 50, 600)
+    finally:
+        del b
+        _free()
+
+
+def test_llama3_70b_capacity_256_requests():
+    w = synth.WORKLOADS["llama3_70b_capacity"]
+    b = synth.build_workload(w, with_pool=False)
+    try:
+        # block tables sized to each request's injected tokens, as an engine
+        # allocates them once it knows how many memory tokens it will receive
+        orc = kc.oracle_select(b)
+        synth.attach_pool(b, tokens_needed=[T for (_s, _sel, _p, T) in orc])
+        assert b.pool.numel() * 2 > 140e9
+        _run_and_check(b, 50, 800)
+    finally:
+        del b
+        _free()

@@ -296,6 +296,8 @@ def test_slot_mapping_hand_cases():
     assert oracle.slot(-1, bt, 2, 8) is None
     assert oracle.slot(0, np.array([8]), 2, 8) is None  # block id not in the pool
     assert oracle.slot(37, np.array([0, 1, 9]), 16, 10) == (9, 5)
+    blk, off = oracle.slots(np.array([0, 1, 2, 5, 6, -1]), bt, 2, 8)
+    assert blk.tolist() == [5, 5, 2, 7, -1, -1] and off.tolist() == [0, 1, 0, 1, -1, -1]
 
 
 # ----------------------------------------------------------- full expectation
