@@ -140,7 +140,9 @@ def check_k_v(gk, gv_bits, ek, ev_bits, where=""):
 def check_pool_full(b: synth.Built, placements):
     """placements: per request (ids[n], starts[n]) to expect.  Small pools:
     the whole pool is compared with the oracle's expected pool."""
-    assert b.kv_np is not None, "full pool check needs the store bits on the host"
+    kv_np = b.kv_np
+    if kv_np is None:  # drawn on the device: read the store bits back
+        kv_np = b.kv.view(torch.int16).cpu().numpy().view(np.uint16)
     bits, vals = _pool_arrays(b)
     L, _, NB, B, H, D = b.pool.shape
     written_all = np.zeros(bits.shape, np.uint8)
@@ -148,7 +150,7 @@ def check_pool_full(b: synth.Built, placements):
         st = b.stores[r]
         bt = b.block_tables[r, :b.table_lens[r]]
         rc, expect, written = oracle.inject_expected(
-            b.kv_np, st.start_np, st.len_np, ids, starts, bt, NB, B, b.w.rope_theta)
+            kv_np, st.start_np, st.len_np, ids, starts, bt, NB, B, b.w.rope_theta)
         assert rc == oracle.OK, f"oracle rejected request {r}: {rc}"
         m = written.astype(bool)
         assert not (written_all.astype(bool) & m).any(), "requests overlap"

@@ -174,8 +174,8 @@ def _split(b, k, ids_override=None, starts=None):
     kvi.kvi_place(view, ids, k, int(b.start_pos[0]), pos, status)
     inj_ids, inj_pos = ids, pos
     if ids_override is not None:
-        inj_ids = torch.from_numpy(np.asarray(ids_override, np.int32)).cuda()
-        inj_pos = torch.from_numpy(np.asarray(starts, np.int32)).cuda()
+        inj_ids = torch.from_numpy(np.ascontiguousarray(ids_override, np.int32)).cuda()
+        inj_pos = torch.from_numpy(np.ascontiguousarray(starts, np.int32)).cuda()
     tl = int(b.table_lens[0])
     bt = torch.from_numpy(b.block_tables[0, :tl].copy()).cuda()
     kvi.kvi_inject_paged(view, inj_ids, inj_pos, inj_ids.shape[0], bt, tl, cache, b.w.rope_theta,
@@ -211,7 +211,7 @@ def test_permuted_placement(mode):
     synth.attach_pool(b, tokens_needed=[need - 3 + 8], rng=rng)
     _ids, _s, _p, status = _split(b, 20, order, starts)
     assert status == 0
-    kc.check_pool_full(b, [(np.asarray(order, np.int32), np.asarray(starts, np.int64))])
+    kc.check_pool_full(b, [(np.ascontiguousarray(order, np.int32), np.asarray(starts, np.int64))])
 
 
 def test_position_zero_is_bit_identical_including_negative_zero():
