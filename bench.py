@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "injected KV GB/s (% of HBM peak) and inject latency/request at k=5..50"
 WORKLOAD = "llama3_8b_10k"
 N_QUERIES = 8          # distinct queries / block tables cycled through the steps
-FLUSH_BYTES = 256 << 20  # > 129 MB L2, written between timed steps
+FLUSH_BYTES = 256 << 20  # > 129 MB L2, written then read between timed steps
 SWEEP_KS = (5, 10, 20, 50)
 PROFILE = os.path.join(ROOT, "profiles", "inject_kernel_llama3_8b_10k.md")
 
@@ -55,6 +55,11 @@ def parse_args(argv=None):
     ap.add_argument("--k", type=int, default=50)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-trace", action="store_true")
+    # profiling case only (not a bench line): a smaller store with the same
+    # geometry, so that an ncu capture holds a few GB on the device
+    ap.add_argument("--facts", type=int, default=0)
     return ap.parse_args(argv)
 
 
@@ -194,7 +199,7 @@ class ClockSampler:
 class Bench:
     """The workload on this rank's GPU and everything one step needs."""
 
-    def __init__(self, rank: int, k: int):
+    def __init__(self, rank: int, k: int, facts: int = 0):
         import torch
 
         from tests import synth
@@ -205,9 +210,11 @@ class Bench:
         kvi.load_library()
         self.torch, self.kvi, self.synth = torch, kvi, synth
         w = synth.WORKLOADS[WORKLOAD]
+        import dataclasses
         if rank:
-            import dataclasses
             w = dataclasses.replace(w, seed=replica_seed(w.seed, rank))
+        if facts:
+            w = dataclasses.replace(w, n_facts=facts)
         self.w = w
         self.k = k
         b = synth.build_workload(w, k=max(SWEEP_KS + (k,)))
@@ -227,7 +234,8 @@ class Bench:
                                         dtype=torch.uint8).cuda()
         self.cache = kvi.paged_cache([b.pool[l] for l in range(w.layers)], w.block_size)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
         self.stream = torch.cuda.current_stream()
         kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, tl * w.block_size)
         self.bufs = {}
@@ -242,6 +250,13 @@ class Bench:
                 ws=t.empty(self.kvi.kvi_workspace_bytes(1, self.w.n_facts, k), dtype=t.uint8,
                            device="cuda"))
         return self.bufs[k]
+
+    def flush(self):
+        """Evict L2 between timed steps: write a buffer larger than L2, then
+        read another one, so that the dirty lines of the write are written
+        back here and not inside the next timed step."""
+        self.flush_w.zero_()
+        self.flush_r.sum()
 
     def step(self, i, k, query=None):
         bf = self.buffers(k)
@@ -268,7 +283,7 @@ class Bench:
         """Per-step device times (s) with an L2 flush between steps."""
         t = self.torch
         for i in range(warmup):
-            self.flush.zero_()
+            self.flush()
             self.step(i, k)
         t.cuda.synchronize()
         ev = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True),
@@ -280,7 +295,7 @@ class Bench:
             t.cuda.synchronize()
         times, stages = [], []
         for i in range(steps):
-            self.flush.zero_()
+            self.flush()
             if trace:
                 self.kvi.kvi_trace_stages(list(ev[i]))
                 self.step(i, k)
@@ -315,7 +330,7 @@ class Bench:
         h_status = t.empty(1, dtype=t.int32).pin_memory()
         times = []
         for i in range(warmup + steps):
-            self.flush.zero_()
+            self.flush()
             t.cuda.synchronize()
             t0 = time.perf_counter()
             j = i % N_QUERIES
@@ -380,7 +395,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dist = dist_init(world, "nccl")
     peak, peak_kind = load_peaks()
-    bench = Bench(rank, args.k)
+    bench = Bench(rank, args.k, args.facts)
     w, k = bench.w, args.k
     dev = torch.device("cuda", local)
 
@@ -414,7 +429,9 @@ def run_ours(args):
     hbm_frac = alg / my_time / 1e9 / peak
 
     # stage times (trace events) -> roofline of the inject kernel
-    _, stages = bench.timed(k, args.steps, args.warmup, trace=True)
+    stages = [(float("nan"), float("nan"))] * args.steps
+    if not args.no_trace:
+        _, stages = bench.timed(k, args.steps, args.warmup, trace=True)
     inj = [s[1] for s in stages]
     ret = [s[0] for s in stages]
     inj_alg = [2 * step_tokens[i] * w.token_bytes for i in range(args.steps)]
@@ -431,7 +448,8 @@ def run_ours(args):
                                f"embeddings, 1 request per step, k={k}, start 64, 16-token "
                                f"pages",
                    "requests_per_step": 1, "k": k, "parallelism": f"replicas x{world}",
-                   "l2": "256 MB write between steps, outside the timed events",
+                   "l2": "flushed between steps outside the timed events: 256 MB write, "
+                         "then 256 MB read (leaves L2 clean)",
                    "queries": f"{N_QUERIES} distinct queries and block tables cycled"},
         "hbm_frac_of_measured_peak": round(hbm_frac, 4),
         "peak_gbs": peak, "peak_kind": peak_kind,
@@ -453,11 +471,12 @@ def run_ours(args):
             ts, _ = bench.timed(kk, max(10, args.steps), args.warmup)
             lat[str(kk)] = round(statistics.median(ts) * 1e6, 2)
         out["latency_us_per_request"] = lat
-    e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
-    e_max = max_over_ranks(dist, sum(e_times), dev)
-    out["e2e"] = {"value": round(all_bytes / e_max / 1e9, 2), "unit": "GB/s",
-                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                  "latency_us_median": round(statistics.median(e_times) * 1e6, 2)}
+    if not args.no_e2e:
+        e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
+        e_max = max_over_ranks(dist, sum(e_times), dev)
+        out["e2e"] = {"value": round(all_bytes / e_max / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "latency_us_median": round(statistics.median(e_times) * 1e6, 2)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, secs, toks = cpu_baseline_sample(w, k, 6, w.seed + 99)
         out["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1,

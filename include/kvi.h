@@ -74,13 +74,15 @@ typedef enum {
     KVI_ERR_INVALID_ARG = 1,  /* bad pointer, size, geometry or limit */
     KVI_ERR_OUT_OF_RANGE = 2, /* fact id, store row, block id or position out of range */
     KVI_ERR_CAPACITY = 3,     /* the facts do not fit the request's block table */
-    KVI_ERR_CUDA = 4          /* a CUDA runtime call failed (see kvi_last_error) */
+    KVI_ERR_CUDA = 4,         /* a CUDA runtime call failed (see kvi_last_error) */
+    KVI_ERR_TIMEOUT = 5       /* a kernel's bounded wait for its own copies expired */
 } kvi_status;
 
 /* Limits of this build. */
 #define KVI_MAX_LAYERS 128        /* L */
 #define KVI_MAX_K 256             /* facts retrieved per request */
 #define KVI_MAX_INJECT_FACTS 4096 /* facts per kvi_inject_paged call */
+#define KVI_MAX_REQUESTS 4096     /* requests per kvi_retrieve_and_inject call */
 #define KVI_MAX_HEAD_DIM 512      /* D, a multiple of 16 */
 #define KVI_MAX_EMBED_DIM 8192    /* E, a multiple of 4 */
 

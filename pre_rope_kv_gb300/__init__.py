@@ -11,7 +11,8 @@ The compute is in ``libkvi.so`` (hand-written CUDA for sm_103a, C ABI in
 names.  Build the library with ``pre_rope_kv_gb300.build.build()``.
 """
 from ._binding import (  # noqa: F401
-    EXPORTED_SYMBOLS, ERR_CAPACITY, ERR_CUDA, ERR_INVALID_ARG, ERR_OUT_OF_RANGE, LIB_PATH,
+    EXPORTED_SYMBOLS, ERR_CAPACITY, ERR_CUDA, ERR_INVALID_ARG, ERR_OUT_OF_RANGE, ERR_TIMEOUT,
+    LIB_PATH, MAX_REQUESTS,
     MAX_INJECT_FACTS, MAX_K, MAX_LAYERS, OK, Geometry, KviError, PagedCache, StoreSizes,
     StoreView, geometry, kvi_inject_paged, kvi_last_error, kvi_place, kvi_prepare_rope,
     kvi_retrieve_and_inject, kvi_retrieve_topk, kvi_status_str, kvi_store_layout,

@@ -22,6 +22,8 @@ ERR_INVALID_ARG = 1
 ERR_OUT_OF_RANGE = 2
 ERR_CAPACITY = 3
 ERR_CUDA = 4
+ERR_TIMEOUT = 5
+MAX_REQUESTS = 4096
 
 MAX_LAYERS = 128
 MAX_K = 256

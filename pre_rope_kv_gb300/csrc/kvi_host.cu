@@ -20,10 +20,6 @@
 
 #include "kvi_internal.cuh"
 
-namespace kvi {
-cudaError_t inject_occupancy(int *ctas_per_sm);
-}
-
 using namespace kvi;
 
 namespace {
@@ -133,13 +129,19 @@ void fill_rope_rows(double theta, int32_t D, int32_t p0, int32_t p1, float4 *out
     const int32_t half = D / 2;
     std::vector<double> omega(half);
     for (int32_t i = 0; i < half; ++i) omega[i] = std::pow(theta, -2.0 * (double)i / (double)D);
+    // two adjacent frequencies per 32 bytes, the layout the kernels read as
+    // packed float32 pairs: {cos_hi[i], cos_hi[i+1], cos_lo[i], cos_lo[i+1]},
+    // {sin_hi[i], sin_hi[i+1], sin_lo[i], sin_lo[i+1]}, i even
     for (int32_t p = p0; p < p1; ++p) {
-        for (int32_t i = 0; i < half; ++i) {
-            const double a = (double)p * omega[i];
-            float4 e;
-            split16(std::cos(a), e.x, e.y);
-            split16(std::sin(a), e.z, e.w);
-            out[(size_t)p * half + i] = e;
+        for (int32_t i = 0; i < half; i += 2) {
+            float ch[2], cl[2], sh[2], sl[2];
+            for (int u = 0; u < 2; ++u) {
+                const double a = (double)p * omega[i + u];
+                split16(std::cos(a), ch[u], cl[u]);
+                split16(std::sin(a), sh[u], sl[u]);
+            }
+            out[(size_t)p * half + i] = make_float4(ch[0], ch[1], cl[0], cl[1]);
+            out[(size_t)p * half + i + 1] = make_float4(sh[0], sh[1], sl[0], sl[1]);
         }
     }
 }
@@ -216,32 +218,60 @@ cudaError_t device_info(DeviceInfo *out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1, DeviceInfo{0, 0});
+    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1, DeviceInfo{0});
     if (g_dev[dev].sms == 0) {
-        int sms = 0, occ = 0;
+        int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = inject_occupancy(&occ);
-        if (e != cudaSuccess) return e;
-        g_dev[dev] = DeviceInfo{sms, std::max(1, occ)};
+        g_dev[dev] = DeviceInfo{sms};
     }
     *out = g_dev[dev];
     return cudaSuccess;
+}
+
+cudaError_t smem_opt_in_raw(const void *kernel, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::vector<std::pair<int, const void *>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto &d : done)
+        if (d.first == dev && d.second == kernel) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.emplace_back(dev, kernel);
+    return e;
+}
+
+PieceGeom piece_geom(int32_t H, int32_t D, int32_t block_size)
+{
+    const int64_t token_bytes = (int64_t)H * D * 2;
+    PieceGeom g{1, H, 1};
+    if (token_bytes <= kPieceMax) {
+        const int64_t most = std::min<int64_t>(block_size, kPieceMax / token_bytes);
+        for (int32_t c = 1; c <= most; ++c)
+            if (block_size % c == 0) g.ct = c;
+    } else {
+        g.hg = 1;
+        for (int32_t h = 1; h <= H; ++h)
+            if (H % h == 0 && (int64_t)h * D * 2 <= kPieceMax) g.hg = h;
+        g.units = H / g.hg;
+    }
+    return g;
 }
 
 WsLayout ws_layout(int32_t R, int64_t max_facts, int32_t k)
 {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     WsLayout w{};
-    size_t at = 0;
-    w.hist = at;    at = up(at + (size_t)R * kHistBins * 4);
-    w.counter = at; at = up(at + 4);
-    w.keys = at;
     w.key_stride = (max_facts + 31) & ~(int64_t)31;
-    at = up(at + (size_t)R * (size_t)w.key_stride * 8);
-    w.cum = at;     at = up(at + (size_t)R * (size_t)(k + 1) * 4);
-    w.tok = at;     at = up(at + (size_t)R * 8);
-    w.req_off = at; at = up(at + (size_t)(R + 1) * 8);
+    size_t at = 0;
+    w.keys = at;     at = up(at + (size_t)R * (size_t)w.key_stride * 8);
+    w.lens = at;     at = up(at + (size_t)R * (size_t)w.key_stride * 4);
+    w.slot_len = at; at = up(at + (size_t)R * (size_t)k * 4);
+    w.pc = at;       at = up(at + (size_t)R * (size_t)(k + 1) * 4);
+    w.npc = at;      at = up(at + (size_t)R * 4);
     w.total = at;
     return w;
 }
@@ -260,6 +290,7 @@ const char *kvi_status_str(kvi_status s)
     case KVI_ERR_OUT_OF_RANGE: return "index out of range";
     case KVI_ERR_CAPACITY: return "facts do not fit the block table";
     case KVI_ERR_CUDA: return "CUDA error";
+    case KVI_ERR_TIMEOUT: return "a kernel wait timed out";
     }
     return "unknown status";
 }
@@ -339,7 +370,6 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
         return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", w.total);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(d_ws);
-    KVI_CUDA(cudaMemsetAsync(ws, 0, ws_zero_bytes(w), s));
 
     ScoreParams sp{};
     sp.store.single = *store;
@@ -347,11 +377,11 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
     sp.queries = d_query;
     sp.g = store->g;
     sp.R = 1;
+    sp.k = k;
     sp.max_facts = store->n_facts;
-    sp.rows_per_cta = (kScoreThreads / 32) * kScoreRowsPerWarp;
     sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
+    sp.lens = reinterpret_cast<int32_t *>(ws + w.lens);
     sp.key_stride = w.key_stride;
-    sp.hist = reinterpret_cast<uint32_t *>(ws + w.hist);
     KVI_CUDA(launch_score(sp, s));
 
     SelectParams lp{};
@@ -362,11 +392,11 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
     lp.max_facts = store->n_facts;
     lp.key_stride = w.key_stride;
     lp.keys = sp.keys;
-    lp.hist = sp.hist;
+    lp.lens = sp.lens;
     lp.ids = d_ids;
     lp.scores = d_scores;
     lp.place = 0;
-    KVI_CUDA(launch_select(lp, s));
+    KVI_CUDA(launch_select(lp, s, true));
     return KVI_OK;
 }
 
@@ -418,6 +448,7 @@ kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_i
     ip.L = store->g.layers;
     ip.H = store->g.kv_heads;
     ip.D = store->g.head_dim;
+    ip.pg = piece_geom(ip.H, ip.D, cache->block_size);
     ip.fused = 0;
     ip.ids = d_fact_ids;
     ip.pos = d_start_pos;
@@ -430,7 +461,7 @@ kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_i
     ip.rope_positions = positions;
     ip.status = d_status;
     for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
-    KVI_CUDA(launch_inject(ip, s));
+    KVI_CUDA(launch_inject(ip, s, false));
     return KVI_OK;
 }
 
@@ -474,18 +505,19 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     const bool trace = t_trace_n == 3;
     if (trace) KVI_CUDA(cudaEventRecord(t_trace[0], s));
     char *ws = static_cast<char *>(d_ws);
-    KVI_CUDA(cudaMemsetAsync(ws, 0, ws_zero_bytes(w), s));
+    const PieceGeom pg = piece_geom(g->kv_heads, g->head_dim, cache->block_size);
 
     ScoreParams sp{};
     sp.store.many = d_stores;
     sp.queries = d_queries;
     sp.g = *g;
     sp.R = R;
+    sp.k = k;
     sp.max_facts = max_facts;
-    sp.rows_per_cta = (kScoreThreads / 32) * kScoreRowsPerWarp;
     sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
+    sp.lens = reinterpret_cast<int32_t *>(ws + w.lens);
     sp.key_stride = w.key_stride;
-    sp.hist = reinterpret_cast<uint32_t *>(ws + w.hist);
+    sp.status = d_status;
     KVI_CUDA(launch_score(sp, s));
 
     SelectParams lp{};
@@ -496,7 +528,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     lp.max_facts = max_facts;
     lp.key_stride = w.key_stride;
     lp.keys = sp.keys;
-    lp.hist = sp.hist;
+    lp.lens = sp.lens;
     lp.ids = d_ids;
     lp.scores = d_scores;
     lp.place = 1;
@@ -504,13 +536,13 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     lp.table_lens = d_table_lens;
     lp.max_blocks = max_blocks;
     lp.block_size = cache->block_size;
+    lp.pg = pg;
     lp.pos = d_pos;
-    lp.cum = reinterpret_cast<int32_t *>(ws + w.cum);
-    lp.tok = reinterpret_cast<int64_t *>(ws + w.tok);
-    lp.req_off = reinterpret_cast<int64_t *>(ws + w.req_off);
-    lp.counter = reinterpret_cast<uint32_t *>(ws + w.counter);
+    lp.slot_len = reinterpret_cast<int32_t *>(ws + w.slot_len);
+    lp.pc = reinterpret_cast<int32_t *>(ws + w.pc);
+    lp.npc = reinterpret_cast<int32_t *>(ws + w.npc);
     lp.status = d_status;
-    KVI_CUDA(launch_select(lp, s));
+    KVI_CUDA(launch_select(lp, s, true));
     if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
 
     InjectParams ip{};
@@ -518,13 +550,15 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     ip.L = g->layers;
     ip.H = g->kv_heads;
     ip.D = g->head_dim;
+    ip.pg = pg;
     ip.fused = 1;
     ip.ids = d_ids;
     ip.pos = d_pos;
     ip.R = R;
     ip.k = k;
-    ip.cum = lp.cum;
-    ip.req_off = lp.req_off;
+    ip.slot_len = lp.slot_len;
+    ip.pc = lp.pc;
+    ip.npc = lp.npc;
     ip.block_tables = d_block_tables;
     ip.table_lens = d_table_lens;
     ip.max_blocks = max_blocks;
@@ -534,7 +568,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     ip.rope_positions = positions;
     ip.status = d_status;
     for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
-    KVI_CUDA(launch_inject(ip, s));
+    KVI_CUDA(launch_inject(ip, s, !trace));
     if (trace) KVI_CUDA(cudaEventRecord(t_trace[2], s));
     return KVI_OK;
 }

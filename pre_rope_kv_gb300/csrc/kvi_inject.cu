@@ -7,25 +7,39 @@
 // blocks before the forward pass, so only the query is prefilled.
 //
 // The kernel is a pure HBM stream: every injected byte is read once from the
-// store and written once to the pool.  It is persistent (one wave of CTAs,
-// grid-stride over work items) because the number of tokens is only known on
-// the device in the fused path.  A work item is one 2 x 16-byte vector pair
-// of one head row, for one token, K or V, over a group of kLayerGroup layers:
+// store and written once to the pool.  It is persistent (one CTA per SM,
+// since the number of tokens is only known on the device in the fused path)
+// and each CTA runs one deep bulk-copy pipeline:
 //
-//   - the two vectors of a pair are elements [8v, 8v+8) and [D/2+8v, D/2+8v+8)
-//     of a head, i.e. the rotate-half partners, so the rotation needs no
-//     data exchange between threads;
-//   - consecutive threads take consecutive pairs of the same row, so each
-//     warp reads and writes whole 128-byte lines of the store and the page;
-//   - the cos/sin entries of the token's position are loaded once per item
-//     and reused across its layers.
+//   - work is cut into pieces: up to `ct` consecutive tokens of one fact that
+//     fall in one page (ct divides the page size), for one layer and one of
+//     K/V, at most 8 KB; in the store and in the page a piece is one
+//     contiguous run of bytes.  A CTA takes a contiguous range of
+//     (piece, K|V, layer) items, layer innermost;
+//   - a producer warp resolves 32 items at a time (one per lane) and its
+//     lane 0 moves each piece into the next of 24 shared-memory stages with
+//     cp.async.bulk, completion tracked by the stage's "full" mbarrier, so up
+//     to 24 pieces (~170 KB) per SM are in flight whatever the registers;
+//   - twelve consumer warps take the stages round-robin: a V piece is copied
+//     out unchanged, a K piece is rotated (each lane takes rotate-half pairs
+//     of one (token, vector) group, elements [8v, 8v+8) and
+//     [D/2+8v, D/2+8v+8), for every head) and written with 16-byte stores;
+//     the warp then releases the stage through its "empty" mbarrier.  A
+//     consumer warp sees the same piece for several layers, so each lane
+//     loads its cos/sin entries once per piece.
 //
 // Rotation accuracy.  The table holds cos and sin of p * omega_i computed in
 // float64 on the host, split into a 16-significant-bit head and a float32
 // tail.  A bf16 key has 8 significant bits, so x * head is exact in float32,
-// and y = fma(x_i, c_hi, -x_j * s_hi) + (x_i * c_lo - x_j * s_lo) is within a
-// few float32 ulps of the exact rotation at any position; one rounding to
-// bf16 follows.  Position 0 is the identity and copies the key bits.
+// and y = (x_i c_hi - x_j s_hi) + (x_i c_lo - x_j s_lo), whose first
+// difference of exact products is rounded once, is within a few float32 ulps
+// of the exact rotation at any position; one rounding to bf16 follows.
+// Position 0 is the identity and copies the key bits.  The arithmetic runs
+// on packed float32 pairs (two frequencies per instruction).
+//
+// Every wait is bounded (one second of globaltimer); a warp that times out
+// records KVI_ERR_TIMEOUT and stops, and the warps waiting on it stop after
+// their own bounded waits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -34,29 +48,104 @@
 namespace kvi {
 namespace {
 
-__device__ __forceinline__ void record(int32_t *status, int code)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+struct PieceDesc {
+    uint8_t *dst;
+    uint32_t bytes;  // 0: nothing to do
+    int32_t pos0;
+    int32_t ntok;
+    int32_t kv;
+};
+
+struct __align__(128) InjSmem {
+    uint8_t stage[kInjRing][kPieceMax];
+    uint64_t full[kInjRing];
+    uint64_t empty[kInjRing];
+    PieceDesc desc[kInjRing];
+    int32_t prefix[kMaxPrefix + 1];
+    int32_t part[kInjThreads];
+};
+
+// ------------------------------------------------------ async-copy helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
-    if (status) atomicCAS(status, 0, code);
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; false after the
+// time limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_u4(void *p, const uint4 &v)
 {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
-                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
                  : "memory");
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+// --------------------------------------------------------------- rotation
+
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 {
@@ -64,229 +153,385 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Rotate 8 rotate-half pairs: lo holds x_i, hi holds x_{i+D/2}.
+// Packed float32 pairs (Blackwell .f32x2 arithmetic): two adjacent
+// frequencies are rotated by one instruction.  Each op rounds each half to
+// nearest, exactly as the scalar op would.
+__device__ __forceinline__ uint64_t f2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16x2 (low half = first element) -> float32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t u)
+{
+    return f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// float32 pair -> bf16x2, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return pack_bf16(lo, hi);
+}
+
+// Rotate 8 rotate-half pairs: lo holds x_i, hi holds x_{i+D/2}, for
+// i = 8v .. 8v+7.  cs holds the table entries of those pairs, two pairs per
+// 32 bytes: {cos_hi[i], cos_hi[i+1], cos_lo[i], cos_lo[i+1]},
+// {sin_hi[i], sin_hi[i+1], sin_lo[i], sin_lo[i+1]}.  x * hi products are exact
+// (8 x 16 significant bits), so y0 = x0 c - x1 s and y1 = x1 c + x0 s get one
+// rounding of their main part plus a float32 tail correction.
 __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float4 *cs)
 {
     uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
     uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        float y0[2], y1[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float x0 = h ? bf_hi(pl[w]) : bf_lo(pl[w]);
-            const float x1 = h ? bf_hi(ph[w]) : bf_lo(ph[w]);
-            const float4 t = cs[2 * w + h];  // {cos_hi, cos_lo, sin_hi, sin_lo}
-            y0[h] = __fadd_rn(__fmaf_rn(x0, t.x, -__fmul_rn(x1, t.z)),
-                              __fsub_rn(__fmul_rn(x0, t.y), __fmul_rn(x1, t.w)));
-            y1[h] = __fadd_rn(__fmaf_rn(x1, t.x, __fmul_rn(x0, t.z)),
-                              __fadd_rn(__fmul_rn(x1, t.y), __fmul_rn(x0, t.w)));
-        }
-        pl[w] = pack_bf16(y0[0], y0[1]);
-        ph[w] = pack_bf16(y1[0], y1[1]);
+        const uint64_t x0 = bf2_to_f2(pl[w]);
+        const uint64_t x1 = bf2_to_f2(ph[w]);
+        const float4 c = cs[2 * w], sn = cs[2 * w + 1];
+        const uint64_t chi = f2(c.x, c.y), clo = f2(c.z, c.w);
+        const uint64_t shi = f2(sn.x, sn.y), slo = f2(sn.z, sn.w);
+        const uint64_t y0 = add2(sub2(mul2(x0, chi), mul2(x1, shi)), sub2(mul2(x0, clo), mul2(x1, slo)));
+        const uint64_t y1 = add2(add2(mul2(x1, chi), mul2(x0, shi)), add2(mul2(x1, clo), mul2(x0, slo)));
+        pl[w] = f2_to_bf2(y0);
+        ph[w] = f2_to_bf2(y1);
     }
 }
+
+// cos/sin entries of one (position, vector) pair group, kept in registers
+// across the layers of a piece.
+struct TableCache {
+    int32_t p, v;
+    float4 cs[8];
+};
+
+// Rotate a staged K piece ([ntok][hg][D] bf16) and write it to dst.  Lane
+// c takes the (token, vector) group t = c / vph, v = c % vph, loads its 8
+// cos/sin entries (cached across the layers of the piece) and walks the
+// piece's heads.  Eight lanes of one token cover 128 contiguous bytes of a
+// head, in shared memory and in the page.
+__device__ __forceinline__ void rotate_piece(const InjectParams &p, const uint8_t *stg, uint8_t *dst,
+                                             int ntok, int32_t pos0, int lane, TableCache &tc)
+{
+    const int D = p.D, HG = p.pg.hg, vph = D >> 4, half = D >> 1;
+    const int groups = ntok * vph;
+    for (int c = lane; c < groups; c += 32) {
+        const int t = c / vph;
+        const int v = c - t * vph;
+        const int32_t pp = pos0 + t;
+        if (pp != 0 && (pp != tc.p || v != tc.v)) {
+            const float4 *tp = p.rope + (int64_t)pp * half + 8 * v;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc.cs[e] = __ldg(tp + e);
+            tc.p = pp;
+            tc.v = v;
+        }
+#pragma unroll 2
+        for (int h = 0; h < HG; ++h) {
+            const int off = ((t * HG + h) * D + 8 * v) * 2;
+            uint4 lo = *reinterpret_cast<const uint4 *>(stg + off);
+            uint4 hi = *reinterpret_cast<const uint4 *>(stg + off + D);
+            if (pp != 0) rotate8(lo, hi, tc.cs);
+            st_u4(dst + off, lo);
+            st_u4(dst + off + D, hi);
+        }
+    }
+}
+
+// Copy a staged V piece to dst, 16 bytes per lane per step.
+__device__ __forceinline__ void copy_piece(const uint8_t *stg, uint8_t *dst, uint32_t bytes, int lane)
+{
+#pragma unroll 4
+    for (uint32_t o = 16u * lane; o < bytes; o += 512u)
+        st_u4(dst + o, *reinterpret_cast<const uint4 *>(stg + o));
+}
+
+// ----------------------------------------------------------------- pieces
 
 // Largest j in [0, n) with a[j] <= x, for non-decreasing a[0..n] and
 // a[0] <= x < a[n].
 template <typename T, typename U>
 __device__ __forceinline__ int search_le(const T *a, int n, U x)
 {
-    int lo = 0, hi = n;  // invariant: a[lo] <= x < a[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if ((U)a[mid] <= x) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-template <typename T, typename U>
-__device__ __forceinline__ int search_le_cg(const T *a, int n, U x)
-{
     int lo = 0, hi = n;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((U)__ldcg(a + mid) <= x) lo = mid; else hi = mid;
+        if ((U)a[mid] <= x) lo = mid;
+        else hi = mid;
     }
     return lo;
 }
 
-__global__ void __launch_bounds__(kInjectThreads)
+struct Piece {
+    const uint8_t *src;
+    uint8_t *dst;
+    uint32_t bytes;  // 0: nothing to do
+    int32_t pos0;
+    int32_t ntok;
+    int32_t kv;
+};
+
+__device__ Piece resolve_piece(const InjectParams &p, const int32_t *prefix, int64_t it)
+{
+    Piece x{nullptr, nullptr, 0u, 0, 0, 0};
+    const int L2 = 2 * p.L;
+    const int64_t piece = it / L2;
+    const int kl = (int)(it - piece * L2);
+    const int kv = kl >= p.L ? 1 : 0;
+    const int l = kl - kv * p.L;
+    int32_t f, m, len;
+    int64_t pos;
+    const int32_t *bt;
+    int32_t tlen;
+    const kvi_store_view *sv;
+    if (!p.fused) {
+        const int j = search_le(prefix, p.n, (int32_t)piece);
+        m = (int32_t)piece - prefix[j];
+        f = p.ids[j];
+        pos = p.pos[j];
+        sv = &p.store.single;
+        len = sv->fact_len[f];
+        bt = p.block_tables;
+        tlen = p.table_len;
+    } else {
+        const int r = search_le(prefix, p.R, (int32_t)piece);
+        const int32_t local = (int32_t)piece - prefix[r];
+        const int32_t *pcr = p.pc + (int64_t)r * (p.k + 1);
+        const int j = search_le(pcr, p.k, local);
+        m = local - pcr[j];
+        f = p.ids[(int64_t)r * p.k + j];
+        pos = p.pos[(int64_t)r * p.k + j];
+        len = p.slot_len[(int64_t)r * p.k + j];
+        sv = p.store.many + r;
+        bt = p.block_tables + (int64_t)r * p.max_blocks;
+        tlen = p.table_lens[r];
+    }
+    const int32_t mt = m / p.pg.units;
+    const int32_t hg = m - mt * p.pg.units;
+    const int64_t first = pos / p.pg.ct;
+    const int64_t a = max(pos, (first + mt) * p.pg.ct);
+    const int64_t b = min(pos + len, (first + mt + 1) * p.pg.ct);
+    const int B = p.block_size;
+    if (a < 0 || b <= a || b > (int64_t)tlen * B || b > p.rope_positions) {
+        record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+        return x;
+    }
+    const int32_t blk = bt[a / B];
+    if (blk < 0 || blk >= p.num_blocks) {
+        record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+        return x;
+    }
+    const int64_t HD = (int64_t)p.H * p.D;
+    const int64_t hoff = (int64_t)hg * p.pg.hg * p.D;
+    const int64_t row = sv->fact_start[f] + (a - pos);
+    x.src = reinterpret_cast<const uint8_t *>(sv->kv) +
+            ((((int64_t)l * 2 + kv) * sv->n_tokens + row) * HD + hoff) * 2;
+    x.dst = reinterpret_cast<uint8_t *>(p.layer_base[l]) +
+            ((((int64_t)kv * p.num_blocks + blk) * B + (a % B)) * HD + hoff) * 2;
+    x.ntok = (int32_t)(b - a);
+    x.bytes = (uint32_t)(x.ntok * p.pg.hg * p.D * 2);
+    x.pos0 = (int32_t)a;
+    x.kv = kv;
+    return x;
+}
+
+__device__ __forceinline__ Piece shfl_piece(const Piece &x, int src)
+{
+    Piece y;
+    y.src = reinterpret_cast<const uint8_t *>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(x.src), src));
+    y.dst = reinterpret_cast<uint8_t *>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(x.dst), src));
+    y.bytes = __shfl_sync(0xffffffffu, x.bytes, src);
+    y.pos0 = __shfl_sync(0xffffffffu, x.pos0, src);
+    y.ntok = __shfl_sync(0xffffffffu, x.ntok, src);
+    y.kv = __shfl_sync(0xffffffffu, x.kv, src);
+    return y;
+}
+
+// counts in a[1..n] -> exclusive prefix a[0..n] (a[0] = 0), whole CTA.
+__device__ void cta_prefix(int32_t *a, int n, int32_t *part)
+{
+    const int tid = threadIdx.x;
+    const int per = (n + kInjThreads - 1) / kInjThreads;
+    const int j0 = tid * per;
+    int32_t run = 0;
+    for (int j = j0; j < j0 + per && j < n; ++j) run += a[j + 1];
+    part[tid] = run;
+    __syncthreads();
+    if (tid < 32) {
+        int32_t carry = 0;
+        for (int base = 0; base < kInjThreads; base += 32) {
+            const int32_t v = part[base + tid];
+            int32_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += t;
+            }
+            part[base + tid] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    __syncthreads();
+    int32_t acc = part[tid];
+    if (tid == 0) a[0] = 0;
+    for (int j = j0; j < j0 + per && j < n; ++j) {
+        acc += a[j + 1];
+        a[j + 1] = acc;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kInjThreads, 1)
 inject_kernel(const __grid_constant__ InjectParams p)
 {
-    __shared__ int32_t s_cum[KVI_MAX_INJECT_FACTS + 1];
-    __shared__ int32_t s_part[kInjectThreads];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    InjSmem &sm = *reinterpret_cast<InjSmem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kInjRing; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        fence_async_smem();
+    }
 
-    int64_t T;
-    if (!p.fused) {
-        // token prefix of the n facts (invalid ids or extents count as 0)
+    pdl_wait();  // selection and placement of the previous kernel
+    int count;
+    if (p.fused) {
+        count = p.R;
+        for (int r = tid; r < p.R; r += kInjThreads) sm.prefix[r + 1] = p.npc[r];
+    } else {
+        count = p.n;
         const kvi_store_view &st = p.store.single;
-        constexpr int per = (KVI_MAX_INJECT_FACTS + kInjectThreads - 1) / kInjectThreads;
-        const int j0 = threadIdx.x * per;
-        int32_t run = 0;
-        for (int j = j0; j < j0 + per && j < p.n; ++j) {
+        for (int j = tid; j < p.n; j += kInjThreads) {
             const int32_t f = p.ids[j];
-            int32_t len = 0;
+            const int64_t pos = p.pos[j];
+            int32_t pieces = 0;
             if (f >= 0 && (int64_t)f < st.n_facts) {
                 const int64_t s0 = st.fact_start[f];
                 const int32_t l0 = st.fact_len[f];
-                if (l0 >= 0 && s0 >= 0 && s0 + l0 <= st.n_tokens) len = l0;
-                else if (blockIdx.x == 0) record(p.status, KVI_ERR_OUT_OF_RANGE);
-            } else if (blockIdx.x == 0) {
-                record(p.status, KVI_ERR_OUT_OF_RANGE);
+                if (l0 >= 0 && s0 >= 0 && s0 + l0 <= st.n_tokens && pos >= 0) {
+                    if (l0 > 0)
+                        pieces = (int32_t)(((pos + l0 - 1) / p.pg.ct - pos / p.pg.ct + 1) * p.pg.units);
+                } else {
+                    record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+                }
+            } else {
+                record_status(p.status, KVI_ERR_OUT_OF_RANGE);
             }
-            s_cum[j + 1] = len;  // length for now, prefix below
-            run += len;
+            sm.prefix[j + 1] = pieces;
         }
-        s_part[threadIdx.x] = run;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int32_t acc = 0;
-            for (int t = 0; t < kInjectThreads; ++t) {
-                const int32_t v = s_part[t];
-                s_part[t] = acc;
-                acc += v;
-            }
-        }
-        __syncthreads();
-        int32_t acc = s_part[threadIdx.x];
-        if (threadIdx.x == 0) s_cum[0] = 0;
-        for (int j = j0; j < j0 + per && j < p.n; ++j) {
-            acc += s_cum[j + 1];
-            s_cum[j + 1] = acc;
-        }
-        __syncthreads();
-        T = s_cum[p.n];
-    } else {
-        T = __ldcg(p.req_off + p.R);
     }
+    __syncthreads();
+    cta_prefix(sm.prefix, count, sm.part);
+    const int64_t total = (int64_t)sm.prefix[count] * 2 * p.L;
+    // this CTA's contiguous range of items
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t it0 = (int64_t)blockIdx.x * per;
+    const int64_t n_items = total > it0 ? min(per, total - it0) : 0;
 
-    const int D = p.D, H = p.H, L = p.L, B = p.block_size;
-    const int half = D >> 1;
-    const int vph = D >> 4;  // vector pairs per head
-    const int VP = H * vph;  // vector pairs per token row
-    const int NG = (L + kLayerGroup - 1) / kLayerGroup;
-    const int64_t HD = (int64_t)H * D;
-    const int64_t W = T * 2 * NG * VP;
-
-    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < W;
-         w += (int64_t)gridDim.x * blockDim.x) {
-        int64_t rest = w / VP;
-        const int qq = (int)(w - rest * VP);
-        const int kvsel = (int)(rest & 1);
-        rest >>= 1;
-        const int64_t tok = rest / NG;
-        const int g = (int)(rest - tok * NG);
-
-        // which fact and which of its tokens
-        int32_t f;
-        int64_t pos;
-        const int32_t *bt;
-        int32_t tlen;
-        int64_t row;
-        const void *kvbase;
-        int64_t n_tokens;
-        if (!p.fused) {
-            const int j = search_le(s_cum, p.n, (int32_t)tok);
-            const int32_t t = (int32_t)tok - s_cum[j];
-            f = p.ids[j];
-            pos = (int64_t)p.pos[j] + t;
-            bt = p.block_tables;
-            tlen = p.table_len;
-            row = p.store.single.fact_start[f] + t;
-            kvbase = p.store.single.kv;
-            n_tokens = p.store.single.n_tokens;
-        } else {
-            const int r = search_le_cg(p.req_off, p.R, tok);
-            const int32_t local = (int32_t)(tok - __ldcg(p.req_off + r));
-            const int32_t *cumr = p.cum + (int64_t)r * (p.k + 1);
-            const int j = search_le_cg(cumr, p.k, local);
-            const int32_t t = local - __ldcg(cumr + j);
-            f = __ldcg(p.ids + (int64_t)r * p.k + j);
-            pos = (int64_t)__ldcg(p.pos + (int64_t)r * p.k + j) + t;
-            bt = p.block_tables + (int64_t)r * p.max_blocks;
-            tlen = p.table_lens[r];
-            const kvi_store_view *sv = p.store.many + r;
-            row = sv->fact_start[f] + t;
-            kvbase = sv->kv;
-            n_tokens = sv->n_tokens;
-        }
-
-        // where it goes
-        if (pos < 0 || pos >= (int64_t)tlen * B || pos >= p.rope_positions) {
-            record(p.status, KVI_ERR_OUT_OF_RANGE);
-            continue;
-        }
-        const int32_t blk = bt[pos / B];
-        const int32_t off = (int32_t)(pos % B);
-        if (blk < 0 || blk >= p.num_blocks) {
-            record(p.status, KVI_ERR_OUT_OF_RANGE);
-            continue;
-        }
-
-        const int h = qq / vph;
-        const int v = qq - h * vph;
-        const int64_t e_lo = (int64_t)h * D + 8 * v;
-        const int64_t e_hi = e_lo + half;
-        const bool rot = (kvsel == 0) && (pos != 0);
-
-        float4 cs[8];
-        if (rot) {
-            const float4 *tp = p.rope + pos * half + 8 * v;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) cs[e] = __ldg(tp + e);
-        }
-
-        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(kvbase) +
-                                   ((int64_t)kvsel * n_tokens + row) * HD;
-        const int64_t lstride = 2 * n_tokens * HD;  // elements between layers
-        const int64_t dst_off = (((int64_t)kvsel * p.num_blocks + blk) * B + off) * HD;
-        const int l0 = g * kLayerGroup;
-        const int l1 = min(L, l0 + kLayerGroup);
-        int l = l0;
-        for (; l + 4 <= l1; l += 4) {
-            uint4 a[4], b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const __nv_bfloat16 *s = src + (int64_t)(l + u) * lstride;
-                a[u] = ld_stream_u4(s + e_lo);
-                b[u] = ld_stream_u4(s + e_hi);
+    if (warp == kInjConsumers) {
+        // producer
+        for (int64_t base = 0; base < n_items; base += 32) {
+            Piece mine{nullptr, nullptr, 0u, 0, 0, 0};
+            if (base + lane < n_items) mine = resolve_piece(p, sm.prefix, it0 + base + lane);
+            const int nb = (int)min((int64_t)32, n_items - base);
+            bool ok = true;
+            for (int i = 0; i < nb; ++i) {
+                const Piece x = shfl_piece(mine, i);
+                if (lane == 0) {
+                    const int64_t j = base + i;
+                    const int s = (int)(j % kInjRing);
+                    const int64_t round = j / kInjRing;
+                    if (round > 0 && !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1),
+                                                kWaitLimitNs)) {
+                        record_status(p.status, KVI_ERR_TIMEOUT);
+                        ok = false;
+                    } else {
+                        sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, x.kv};
+                        const uint32_t fb = smem_u32(&sm.full[s]);
+                        if (x.bytes) {
+                            fence_async_smem();
+                            mbar_expect_tx(fb, x.bytes);
+                            bulk_load(smem_u32(sm.stage[s]), x.src, x.bytes, fb);
+                        } else {
+                            mbar_arrive(fb);
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (rot) rotate8(a[u], b[u], cs);
-                __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(p.layer_base[l + u]) + dst_off;
-                st_u4(d + e_lo, a[u]);
-                st_u4(d + e_hi, b[u]);
-            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         }
-        for (; l < l1; ++l) {
-            const __nv_bfloat16 *s = src + (int64_t)l * lstride;
-            uint4 a = ld_stream_u4(s + e_lo);
-            uint4 b = ld_stream_u4(s + e_hi);
-            if (rot) rotate8(a, b, cs);
-            __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(p.layer_base[l]) + dst_off;
-            st_u4(d + e_lo, a);
-            st_u4(d + e_hi, b);
+    } else {
+        // consumers
+        TableCache tc;
+        tc.p = -1;
+        tc.v = -1;
+        for (int64_t j = warp; j < n_items; j += kInjConsumers) {
+            const int s = (int)(j % kInjRing);
+            const uint32_t parity = (uint32_t)((j / kInjRing) & 1);
+            const bool ok = mbar_wait(smem_u32(&sm.full[s]), parity, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
+                break;
+            }
+            const PieceDesc d = sm.desc[s];
+            const uint8_t *stg = sm.stage[s];
+            if (d.bytes) {
+                if (d.kv) copy_piece(stg, d.dst, d.bytes, lane);
+                else rotate_piece(p, stg, d.dst, d.ntok, d.pos0, lane, tc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
         }
     }
 }
 
 }  // namespace
 
-cudaError_t launch_inject(const InjectParams &p, cudaStream_t s)
+cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl)
 {
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(di.sms * di.inject_ctas_per_sm);
-    inject_kernel<<<grid, kInjectThreads, 0, s>>>(p);
+    const int smem = (int)sizeof(InjSmem);
+    e = smem_opt_in(inject_kernel, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)di.sms);
+    cfg.blockDim = dim3(kInjThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, inject_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
-}
-
-cudaError_t inject_occupancy(int *ctas_per_sm)
-{
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, inject_kernel, kInjectThreads, 0);
 }
 
 }  // namespace kvi

@@ -13,12 +13,16 @@ namespace kvi {
 // ---------------------------------------------------------------- constants
 constexpr int kHistBins = 4096;     // first-level score buckets per request
 constexpr int kScoreThreads = 256;  // 8 warps, one fact row per warp at a time
-constexpr int kScoreRowsPerWarp = 4;
 constexpr int kSelectThreads = 1024;
+constexpr int kKeysPerThread = 12;  // keys a select thread keeps in registers
 constexpr int kCandCap = 1024;      // candidates ranked directly in shared memory
-constexpr int kInjectThreads = 256;
-constexpr int kLayerGroup = 8;      // layers handled by one inject work item
-constexpr int kMaxRequests = 1 << 16;
+constexpr int kInjConsumers = 12;   // inject warps that rotate / write pieces
+constexpr int kInjThreads = (kInjConsumers + 1) * 32;  // + one producer warp
+constexpr int kInjRing = 24;        // shared-memory stages per inject CTA
+constexpr int kPieceMax = 8192;     // bytes of one staged piece
+constexpr int kMaxPrefix = 4096;    // requests (fused) or facts (split) per inject call
+constexpr int kMaxRequests = KVI_MAX_REQUESTS;
+static_assert(KVI_MAX_REQUESTS <= kMaxPrefix && KVI_MAX_INJECT_FACTS <= kMaxPrefix, "prefix");
 
 // A store is either one host-provided view (single-request calls) or a device
 // array of views indexed by request (fused batched call).
@@ -28,30 +32,38 @@ struct StoreRef {
 };
 
 // Workspace regions (byte offsets from the workspace base, 256-aligned).
+// Nothing in it needs initialising: every region is written before it is read
+// within one call.
 struct WsLayout {
-    size_t hist;     // uint32 [R][kHistBins]
-    size_t counter;  // uint32 [1] CTAs of the select kernel that finished
-    size_t keys;     // uint64 [R][key_stride] order-preserving score keys
-    size_t cum;      // int32  [R][k + 1] token prefix of the selected facts
-    size_t tok;      // int64  [R] tokens injected per request
-    size_t req_off;  // int64  [R + 1] token offset of each request
+    size_t keys;      // uint64 [R][key_stride] order-preserving score keys
+    size_t lens;      // int32  [R][key_stride] validated fact length, -1 = bad extent
+    size_t slot_len;  // int32  [R][k] length of each selected fact
+    size_t pc;        // int32  [R][k + 1] piece prefix of the selected facts
+    size_t npc;       // int32  [R] pieces of each request (0: nothing to inject)
     size_t total;
     int64_t key_stride;
 };
 WsLayout ws_layout(int32_t R, int64_t max_facts, int32_t k);
-// Bytes at the start of the workspace that must be zero before each call.
-inline size_t ws_zero_bytes(const WsLayout &w) { return w.keys; }
+
+// How the inject kernel cuts facts into pieces that fit one shared-memory
+// stage: `ct` tokens (a divisor of the page size, so a piece never crosses a
+// page) of `hg` heads; a token splits into `units` = H / hg head groups when
+// one token row is larger than a stage.
+struct PieceGeom {
+    int32_t ct, hg, units;
+};
+PieceGeom piece_geom(int32_t H, int32_t D, int32_t block_size);
 
 struct ScoreParams {
     StoreRef store;
     const float *queries;  // [R][E]
     kvi_geometry g;
-    int32_t R;
+    int32_t R, k;
     int64_t max_facts;
-    int32_t rows_per_cta;
     uint64_t *keys;
+    int32_t *lens;
     int64_t key_stride;
-    uint32_t *hist;
+    int32_t *status;  // may be null (kvi_retrieve_topk has no status word)
 };
 
 struct SelectParams {
@@ -61,7 +73,7 @@ struct SelectParams {
     int64_t max_facts;
     int64_t key_stride;
     const uint64_t *keys;
-    const uint32_t *hist;
+    const int32_t *lens;
     int32_t *ids;     // [R][k]
     float *scores;    // [R][k]
     // placement (fused path only; place == 0 skips it)
@@ -70,11 +82,11 @@ struct SelectParams {
     const int32_t *table_lens;  // [R]
     int32_t max_blocks;
     int32_t block_size;
+    PieceGeom pg;
     int32_t *pos;               // [R][k]
-    int32_t *cum;               // [R][k + 1]
-    int64_t *tok;               // [R]
-    int64_t *req_off;           // [R + 1]
-    uint32_t *counter;
+    int32_t *slot_len;          // [R][k]
+    int32_t *pc;                // [R][k + 1]
+    int32_t *npc;               // [R]
     int32_t *status;
 };
 
@@ -90,35 +102,64 @@ struct PlaceParams {
 struct InjectParams {
     StoreRef store;
     int32_t L, H, D;
+    PieceGeom pg;
     int32_t fused;             // 0: n explicit facts; 1: R requests of k facts
     const int32_t *ids;        // split [n], fused [R][k]
     const int32_t *pos;        // split [n] start positions, fused [R][k]
     int32_t n;                 // split
     int32_t R, k;              // fused
-    const int32_t *cum;        // fused [R][k + 1]
-    const int64_t *req_off;    // fused [R + 1]
+    const int32_t *slot_len;   // fused [R][k]
+    const int32_t *pc;         // fused [R][k + 1]
+    const int32_t *npc;        // fused [R]
     const int32_t *block_tables;  // split [table_len], fused [R][max_blocks]
     const int32_t *table_lens;    // fused [R]
     int32_t table_len;            // split
     int32_t max_blocks;           // fused row stride
     int32_t num_blocks, block_size;
-    const float4 *rope;        // [rope_positions][D/2] {cos_hi, cos_lo, sin_hi, sin_lo}
+    const float4 *rope;        // [rope_positions][D/2]: pairs of frequencies, see kvi_host.cu
     int32_t rope_positions;
     int32_t *status;
     void *layer_base[KVI_MAX_LAYERS];
 };
 
-// Launchers (return the CUDA error of the launch).
+// Launchers (return the CUDA error of the launch).  `pdl` launches the kernel
+// with programmatic stream serialization so that it can start while the
+// previous kernel of the stream drains; the kernel waits for that kernel's
+// results before reading them.
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
-cudaError_t launch_select(const SelectParams &p, cudaStream_t s);
+cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl);
 cudaError_t launch_place(const PlaceParams &p, cudaStream_t s);
-cudaError_t launch_inject(const InjectParams &p, cudaStream_t s);
+cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl);
 
-// Device facts cached per device (SM count, resident inject CTAs per SM).
+// Device facts cached per device (SM count).
 struct DeviceInfo {
     int sms;
-    int inject_ctas_per_sm;
 };
 cudaError_t device_info(DeviceInfo *out);
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
+// and kernel (later calls only look the pair up).
+cudaError_t smem_opt_in_raw(const void *kernel, int bytes);
+template <typename K>
+inline cudaError_t smem_opt_in(K kernel, int bytes)
+{
+    return smem_opt_in_raw(reinterpret_cast<const void *>(kernel), bytes);
+}
+
+// Device-side helpers shared by the kernels.
+#ifdef __CUDACC__
+__device__ __forceinline__ void record_status(int32_t *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+// Programmatic dependent launch: wait for the previous kernel's memory, and
+// let the next kernel of the stream begin launching.  Both are no-ops when
+// the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 }  // namespace kvi

@@ -8,22 +8,24 @@
 // embedding row is read once per query), so the kernels here are shaped for
 // bandwidth, not for tensor cores:
 //
-//   score_kernel   one warp per fact row, 16-byte streaming loads, query held
-//                  in registers; the dot product is accumulated with Dot2
-//                  (Ogita, Rump & Oishi, "Accurate Sum and Dot Product", SIAM
-//                  J. Sci. Comput. 26(6), 2005: error-free TwoProduct by FMA
-//                  and TwoSum, carried as a float32 pair) and the pair is
-//                  turned into a float64 selection key.  Each key also bumps a
-//                  4096-bucket histogram of its float32 rounding, a monotone
-//                  map, so the selector knows which bucket holds the k-th key.
-//   select_kernel  one CTA per request: buckets above the k-th one are taken
-//                  whole; the k-th bucket's keys are ranked exactly (or, when
-//                  it is crowded, refined by an 8-bit radix select on the full
-//                  64-bit key, down to ties, which go to the lower fact id).
+//   score_kernel   each warp streams a contiguous range of fact rows with the
+//                  next row's 16-byte loads in flight while it reduces the
+//                  current one; the query is re-read from L1.  The dot product
+//                  is accumulated with Dot2 (Ogita, Rump & Oishi, "Accurate
+//                  Sum and Dot Product", SIAM J. Sci. Comput. 26(6), 2005:
+//                  error-free TwoProduct by FMA and TwoSum, carried as a
+//                  float32 pair) and the pair becomes an exact 64-bit
+//                  selection key with integer ordering only (no float64).
+//                  The same warp validates the fact's extent in the store.
+//   select_kernel  one CTA per request: a shared-memory histogram of the keys'
+//                  float32 parts (a monotone map) finds the bucket that
+//                  holds the k-th key; buckets above it are taken whole, the
+//                  k-th bucket's keys are ranked exactly (or, when it is
+//                  crowded, refined by an 8-bit radix select on the full
+//                  64-bit key down to ties, which go to the lower fact id).
 //                  In the fused path it also places the facts (rank order,
-//                  back to back from the request's start) and publishes the
-//                  request's token count; the last CTA to finish turns those
-//                  counts into request offsets for the inject kernel.
+//                  back to back from the request's start) and cuts them into
+//                  the inject kernel's pieces.
 //   place_kernel   placement alone, for the split API.
 #include <cuda_runtime.h>
 
@@ -32,20 +34,23 @@
 namespace kvi {
 namespace {
 
-__device__ __forceinline__ void record(int32_t *status, int code)
-{
-    if (status) atomicCAS(status, 0, code);
-}
-
 // 16-byte load that bypasses L1 allocation: each embedding row is read once.
 __device__ __forceinline__ float4 ld_stream_f4(const float4 *p)
 {
     float4 v;
     asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
     return v;
 }
+
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+constexpr int64_t kPrefetchRows = 8;
 
 // TwoSum (Knuth): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
@@ -74,6 +79,35 @@ __device__ __forceinline__ void dot2_f4(const float4 &q, const float4 &e, float 
     dot2_step(q.w, e.w, s, c);
 }
 
+// Four independent Dot2 accumulations, one per float4 component, so that
+// consecutive steps do not wait on each other; combined in a fixed order.
+struct Dot2x4 {
+    float s[4], c[4];
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) s[u] = c[u] = 0.f;
+    }
+    __device__ __forceinline__ void add(const float4 &q, const float4 &e)
+    {
+        dot2_step(q.x, e.x, s[0], c[0]);
+        dot2_step(q.y, e.y, s[1], c[1]);
+        dot2_step(q.z, e.z, s[2], c[2]);
+        dot2_step(q.w, e.w, s[3], c[3]);
+    }
+    __device__ __forceinline__ void combine(float &so, float &co) const
+    {
+        float a, ea, b, eb;
+        two_sum(s[0], s[1], a, ea);
+        two_sum(s[2], s[3], b, eb);
+        float t, et;
+        two_sum(a, b, t, et);
+        so = t;
+        co = __fadd_rn(__fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3])),
+                       __fadd_rn(__fadd_rn(ea, eb), et));
+    }
+};
+
 // Butterfly reduction of (s, c) pairs across the warp, compensated.
 __device__ __forceinline__ void warp_reduce_pair(float &s, float &c)
 {
@@ -88,30 +122,48 @@ __device__ __forceinline__ void warp_reduce_pair(float &s, float &c)
     }
 }
 
-// Order-preserving map double -> uint64 (larger key = larger score).  -0 is
-// folded onto +0 first so that the two compare equal, as they do as doubles.
-__device__ __forceinline__ uint64_t order_key(double s)
+// Selection key of a compensated score (s, c) without float64 arithmetic.
+// TwoSum normalises the pair so that s' = fl(s' + c') and c' is the exact
+// remainder.  Rounding to nearest is monotone, so for two scores the order of
+// the exact values s' + c' is the lexicographic order of (s', c'); the key is
+// the order-preserving images of s' (high word) and c' (low word).  -0 is
+// folded onto +0 first.
+__device__ __forceinline__ uint32_t order32(float x)
 {
-    s = __dadd_rn(s, 0.0);
-    const uint64_t u = (uint64_t)__double_as_longlong(s);
-    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
+    return (u >> 31) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ double unorder_key(uint64_t u)
+__device__ __forceinline__ float unorder32(uint32_t o)
 {
-    const uint64_t v = (u >> 63) ? (u & 0x7fffffffffffffffull) : ~u;
-    return __longlong_as_double((long long)v);
+    return __uint_as_float((o >> 31) ? (o & 0x7fffffffu) : ~o);
 }
 
-// First-level bucket: top 12 bits of the order-preserving image of the key
-// rounded to float32.  Rounding is monotone, so key_a > key_b implies
-// bucket_a >= bucket_b.
-__device__ __forceinline__ uint32_t bucket_of(uint64_t okey)
+__device__ __forceinline__ uint64_t score_key(float s, float c)
 {
-    const float f = __fadd_rn(__double2float_rn(unorder_key(okey)), 0.0f);
-    uint32_t u = __float_as_uint(f);
-    u = (u >> 31) ? ~u : (u | 0x80000000u);
-    return u >> 20;
+    float hi, lo;
+    two_sum(s, c, hi, lo);
+    return ((uint64_t)order32(hi) << 32) | order32(lo);
+}
+
+// The similarity reported for a key: s' = the score rounded to float32.
+__device__ __forceinline__ float key_score(uint64_t key) { return unorder32((uint32_t)(key >> 32)); }
+
+// First-level bucket (12 bits) of a key, from integer bit fields of s': its
+// sign, its exponent clamped to [-48, 15] (6 bits) and the top 5 bits of its
+// mantissa, i.e. 1/32-octave buckets for magnitudes 2^-48 .. 2^16 (coarser
+// outside, where the clamp merges octaves).  Truncation and clamping never
+// reverse an order, so key_a > key_b implies bucket_a >= bucket_b.
+__device__ __forceinline__ uint32_t bucket_of(uint64_t key)
+{
+    const uint32_t o = (uint32_t)(key >> 32);
+    const uint32_t u = (o >> 31) ? (o & 0x7fffffffu) : ~o;  // float bits of s'
+    const int32_t e = (int32_t)((u >> 23) & 0xff) - 127 + 48;
+    uint32_t mag;
+    if (e < 0) mag = 0;
+    else if (e > 63) mag = 2047;
+    else mag = ((uint32_t)e << 5) | ((u >> 18) & 31u);
+    return (u >> 31) ? 2047u - mag : 2048u + mag;
 }
 
 __device__ __forceinline__ bool better(uint64_t ka, int32_t ia, uint64_t kb, int32_t ib)
@@ -137,46 +189,347 @@ __device__ __forceinline__ kvi_store_view load_store(const StoreRef &s, int r)
 
 // ------------------------------------------------------------------ scoring
 
+// Which request and fact a flat row index is, where its embedding starts
+// (null when it is not a fact of a valid store), and its extent in the store
+// (loaded with the row so that validating it costs no extra round trip).
+struct RowRef {
+    int32_t r;
+    int64_t i;
+    const float4 *e4;
+    int64_t n_tokens;
+    int64_t s0;
+    int32_t l0;
+};
+
+struct ReqCache {
+    int32_t r;
+    bool ok;
+    kvi_store_view st;
+};
+
+__device__ __forceinline__ RowRef resolve_row(const ScoreParams &p, int64_t g, ReqCache &rc,
+                                              int lane)
+{
+    RowRef rr;
+    rr.r = (int32_t)(g / p.max_facts);
+    rr.i = g - (int64_t)rr.r * p.max_facts;
+    if (rr.r != rc.r) {
+        rc.r = rr.r;
+        rc.st = load_store(p.store, rr.r);
+        rc.ok = !p.store.many || store_ok(rc.st, p.g, p.max_facts, p.k);
+    }
+    const bool live = rc.ok && rr.i < rc.st.n_facts;
+    rr.e4 = live ? reinterpret_cast<const float4 *>(rc.st.emb + rr.i * p.g.embed_dim) : nullptr;
+    rr.n_tokens = rc.st.n_tokens;
+    rr.s0 = 0;
+    rr.l0 = -1;
+    if (live && lane == 1) {
+        rr.s0 = __ldg(rc.st.fact_start + rr.i);
+        rr.l0 = __ldg(rc.st.fact_len + rr.i);
+    }
+    return rr;
+}
+
+// Key (lane 0) and validated length (lane 1) of one scored row.
+__device__ __forceinline__ void finish_row(const ScoreParams &p, const RowRef &rr, float s,
+                                           float c, int lane)
+{
+    warp_reduce_pair(s, c);
+    const int64_t at = (int64_t)rr.r * p.key_stride + rr.i;
+    if (lane == 0) p.keys[at] = score_key(s, c);
+    if (lane == 1)
+        p.lens[at] = (rr.l0 >= 0 && rr.s0 >= 0 && rr.s0 + rr.l0 <= rr.n_tokens) ? rr.l0 : -1;
+}
+
 template <int NV>  // float4 per lane per row (E = 128 * NV); 0 = any E % 4 == 0
-__global__ void __launch_bounds__(kScoreThreads)
+__global__ void __launch_bounds__(kScoreThreads, 2)
 score_kernel(const __grid_constant__ ScoreParams p)
 {
-    const int r = blockIdx.y;
-    const kvi_store_view st = load_store(p.store, r);
-    if (p.store.many && !store_ok(st, p.g, p.max_facts, 1)) return;  // reported by select
-    const int64_t N = st.n_facts;
-    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
-    if (row0 >= N) return;
-    const int64_t row1 = min(N, row0 + (int64_t)p.rows_per_cta);
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    const int64_t G = (int64_t)gridDim.x * (kScoreThreads / 32);
+    const int64_t gw = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
+    const int64_t total = (int64_t)p.R * p.max_facts;
+    const int64_t per = (total + G - 1) / G;
+    const int64_t g0 = gw * per;
+    const int64_t g1 = min(total, g0 + per);
+    if (g0 >= g1) return;
     const int E = p.g.embed_dim;
-    const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)r * E);
-    uint64_t *keys = p.keys + (int64_t)r * p.key_stride;
-    uint32_t *hist = p.hist + (int64_t)r * kHistBins;
 
-    float4 qv[NV > 0 ? NV : 1];
-    if constexpr (NV > 0) {
-#pragma unroll
-        for (int m = 0; m < NV; ++m) qv[m] = __ldg(q4 + lane + 32 * m);
-    }
-    for (int64_t i = row0 + warp; i < row1; i += kScoreThreads / 32) {
-        const float4 *e4 = reinterpret_cast<const float4 *>(st.emb + i * E);
-        float s = 0.f, c = 0.f;
-        if constexpr (NV > 0) {
-            float4 ev[NV];
-#pragma unroll
-            for (int m = 0; m < NV; ++m) ev[m] = ld_stream_f4(e4 + lane + 32 * m);
-#pragma unroll
-            for (int m = 0; m < NV; ++m) dot2_f4(qv[m], ev[m], s, c);
-        } else {
-            for (int v = lane; v < E / 4; v += 32) dot2_f4(__ldg(q4 + v), ld_stream_f4(e4 + v), s, c);
+    ReqCache rc;
+    rc.r = -1;
+    rc.ok = false;
+    // keep the next kPrefetchRows rows of this warp's range on their way into
+    // L2 (bulk prefetch, no registers), so that each row's loads hit L2; rows
+    // of another request than the cached one are left to the plain loads
+    const int64_t row_bytes = (int64_t)E * 4;
+    int64_t pf = g0;
+    auto prefetch_to = [&](int64_t upto) {
+        upto = min(upto, g1);
+        while (pf < upto) {
+            const int32_t r = (int32_t)(pf / p.max_facts);
+            const int64_t i = pf - (int64_t)r * p.max_facts;
+            const int64_t seg = min(upto, (int64_t)(r + 1) * p.max_facts) - pf;
+            if (lane == 0 && r == rc.r && rc.ok) {
+                const int64_t n = min(seg, rc.st.n_facts - i);
+                if (n > 0) bulk_prefetch_l2(rc.st.emb + i * E, (uint32_t)(n * row_bytes));
+            }
+            pf += seg;
         }
-        warp_reduce_pair(s, c);
-        if (lane == 0) {
-            const uint64_t ok = order_key(__dadd_rn((double)s, (double)c));
-            keys[i] = ok;
-            atomicAdd(hist + bucket_of(ok), 1u);
+    };
+    if constexpr (NV > 0) {
+        // double-buffered rows where registers allow it (E <= 1024)
+        // the query is read per row from L1 (it stays resident there)
+        constexpr bool kDB = NV <= 8;
+        float4 cur[NV], nxt[kDB ? NV : 1];
+        RowRef a = resolve_row(p, g0, rc, lane);
+        prefetch_to(g0 + 1 + kPrefetchRows);
+        if (a.e4) {
+#pragma unroll
+            for (int m = 0; m < NV; ++m) cur[m] = ld_stream_f4(a.e4 + lane + 32 * m);
+        }
+        for (int64_t g = g0; g < g1; ++g) {
+            prefetch_to(g + 1 + kPrefetchRows);
+            RowRef b{0, 0, nullptr, 0, 0, -1};
+            if (kDB && g + 1 < g1) {
+                b = resolve_row(p, g + 1, rc, lane);
+                if (b.e4) {
+#pragma unroll
+                    for (int m = 0; m < (kDB ? NV : 1); ++m) nxt[m] = ld_stream_f4(b.e4 + lane + 32 * m);
+                }
+            }
+            if (a.e4) {
+                const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)a.r * E);
+                float s = 0.f, c = 0.f;
+#pragma unroll
+                for (int m = 0; m < NV; ++m) dot2_f4(__ldg(q4 + lane + 32 * m), cur[m], s, c);
+                finish_row(p, a, s, c, lane);
+            }
+            if constexpr (kDB) {
+                a = b;
+#pragma unroll
+                for (int m = 0; m < NV; ++m) cur[m] = nxt[m];
+            } else if (g + 1 < g1) {
+                a = resolve_row(p, g + 1, rc, lane);
+                if (a.e4) {
+#pragma unroll
+                    for (int m = 0; m < NV; ++m) cur[m] = ld_stream_f4(a.e4 + lane + 32 * m);
+                }
+            }
+        }
+    } else {
+        for (int64_t g = g0; g < g1; ++g) {
+            const RowRef a = resolve_row(p, g, rc, lane);
+            prefetch_to(g + 1 + kPrefetchRows);
+            if (!a.e4) continue;
+            const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)a.r * E);
+            float s = 0.f, c = 0.f;
+            for (int v = lane; v < E / 4; v += 32) dot2_f4(__ldg(q4 + v), ld_stream_f4(a.e4 + v), s, c);
+            finish_row(p, a, s, c, lane);
+        }
+    }
+}
+
+// Ring variant (rows of at most 8 KB, i.e. E <= 2048): one CTA per SM; a
+// producer lane streams the CTA's contiguous range of fact rows into a ring
+// of shared-memory stages (one row per stage, 192 KB in all) with
+// cp.async.bulk, and twelve consumer warps take the rows round-robin, each
+// lane reading its float4 slots from shared memory and keeping four
+// independent Dot2 accumulators.  The extents of a warp's next 32 rows are
+// fetched together (one per lane), so validating them costs one round trip
+// per 32 rows.  The code is kept short: it is fetched cold on every launch.
+
+constexpr int kRingConsumers = 12;
+constexpr int kRingThreads = (kRingConsumers + 1) * 32;
+constexpr int kRingBytes = 192 * 1024;
+constexpr int kRingMaxStages = 96;
+constexpr uint64_t kRingWaitNs = 1000000000ull;
+
+struct ScoreRingSmem {
+    uint8_t ring[kRingBytes];
+    uint64_t full[kRingMaxStages];
+    uint64_t empty[kRingMaxStages];
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __noinline__ bool ring_wait(uint32_t bar, uint32_t parity)
+{
+    uint64_t t0 = 0;
+    for (int it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (it == 0) t0 = t;
+        else if (t - t0 > kRingWaitNs) return false;
+    }
+}
+
+// Flat row g of the R x max_facts row space, advanced without divisions.
+struct RowCursor {
+    int32_t r;
+    int64_t i;
+    __device__ void init(int64_t g, int64_t max_facts)
+    {
+        r = (int32_t)(g / max_facts);
+        i = g - (int64_t)r * max_facts;
+    }
+    __device__ void advance(int64_t by, int64_t max_facts)
+    {
+        i += by;
+        while (i >= max_facts) {
+            i -= max_facts;
+            ++r;
+        }
+    }
+};
+
+struct StoreCache {
+    int32_t r;
+    bool ok;
+    kvi_store_view st;
+    __device__ void get(const ScoreParams &p, int32_t rr)
+    {
+        if (rr == r) return;
+        r = rr;
+        st = load_store(p.store, rr);
+        ok = !p.store.many || store_ok(st, p.g, p.max_facts, p.k);
+    }
+    __device__ bool live(int64_t i) const { return ok && i < st.n_facts; }
+};
+
+__global__ void __launch_bounds__(kRingThreads, 1)
+score_ring_kernel(const __grid_constant__ ScoreParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    ScoreRingSmem &sm = *reinterpret_cast<ScoreRingSmem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.g.embed_dim;
+    const uint32_t row_bytes = (uint32_t)E * 4u;
+    const int S = min(kRingMaxStages, (int)(kRingBytes / row_bytes));
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[s])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.empty[s])) : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const int64_t total = (int64_t)p.R * p.max_facts;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t g0 = (int64_t)blockIdx.x * per;
+    const int64_t n = total > g0 ? min(per, total - g0) : 0;  // rows of this CTA
+    StoreCache sc;
+    sc.r = -1;
+    sc.ok = false;
+
+    if (warp == kRingConsumers) {
+        // producer: one row per stage, stage index and phase kept incrementally
+        if (lane != 0) return;
+        RowCursor cur;
+        cur.init(g0, p.max_facts);
+        int s = 0;
+        uint32_t round = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            if (round > 0 && !ring_wait(smem_addr(&sm.empty[s]), (round - 1) & 1u)) {
+                record_status(p.status, KVI_ERR_TIMEOUT);
+                return;
+            }
+            sc.get(p, cur.r);
+            const uint32_t fb = smem_addr(&sm.full[s]);
+            if (sc.live(cur.i)) {
+                if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                             "r"(row_bytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+                    "[%3];" ::"r"(smem_addr(sm.ring + (size_t)s * row_bytes)),
+                    "l"(sc.st.emb + cur.i * E), "r"(row_bytes), "r"(fb)
+                    : "memory");
+            } else {
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
+            }
+            cur.advance(1, p.max_facts);
+            if (++s == S) {
+                s = 0;
+                ++round;
+            }
+        }
+        return;
+    }
+
+    // consumers: rows warp, warp + 12, ...  The extents of the next 32 of a
+    // warp's rows are loaded together, one per lane, and handed to the row's
+    // finishing lanes with shuffles, so their latency is paid once per 32 rows.
+    RowCursor cur;
+    cur.init(g0 + warp, p.max_facts);
+    int s = warp % S;
+    uint32_t round = (uint32_t)(warp / S);
+    int64_t bs0 = 0;
+    int32_t bl0 = -1;
+#pragma unroll 1
+    for (int64_t j = warp, m = 0; j < n; j += kRingConsumers, ++m) {
+        if ((m & 31) == 0) {
+            // lane l: extent of this warp's row j + 12 l
+            RowCursor c = cur;
+            c.advance((int64_t)lane * kRingConsumers, p.max_facts);
+            bs0 = 0;
+            bl0 = -1;
+            if (j + (int64_t)lane * kRingConsumers < n) {
+                sc.get(p, c.r);
+                if (sc.live(c.i)) {
+                    bs0 = __ldg(sc.st.fact_start + c.i);
+                    bl0 = __ldg(sc.st.fact_len + c.i);
+                }
+            }
+        }
+        const int64_t s0 = __shfl_sync(0xffffffffu, bs0, (int)(m & 31));
+        const int32_t l0 = __shfl_sync(0xffffffffu, bl0, (int)(m & 31));
+        const bool ok = ring_wait(smem_addr(&sm.full[s]), round & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
+            return;
+        }
+        sc.get(p, cur.r);
+        if (sc.live(cur.i)) {
+            const float4 *row = reinterpret_cast<const float4 *>(sm.ring + (size_t)s * row_bytes);
+            const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)cur.r * E);
+            Dot2x4 acc;
+            acc.zero();
+#pragma unroll 4
+            for (int v = lane; v < E / 4; v += 32) acc.add(__ldg(q4 + v), row[v]);
+            float sacc, cacc;
+            acc.combine(sacc, cacc);
+            RowRef rr;
+            rr.r = cur.r;
+            rr.i = cur.i;
+            rr.e4 = nullptr;
+            rr.n_tokens = sc.st.n_tokens;
+            rr.s0 = s0;
+            rr.l0 = l0;
+            finish_row(p, rr, sacc, cacc, lane);
+        }
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm.empty[s])) : "memory");
+        cur.advance(kRingConsumers, p.max_facts);
+        s += kRingConsumers;
+        while (s >= S) {
+            s -= S;
+            ++round;
         }
     }
 }
@@ -184,54 +537,29 @@ score_kernel(const __grid_constant__ ScoreParams p)
 // ---------------------------------------------------------------- selection
 
 // Inclusive scan of one value per thread over a 1024-thread block.
-__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_tot)
+template <typename T>
+__device__ __forceinline__ T block_incl_scan(T v, T *warp_tot)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        const T t = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += t;
     }
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = warp_tot[lane];
+        T w = warp_tot[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, w, o);
+            const T t = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += t;
         }
         warp_tot[lane] = w;
     }
     __syncthreads();
-    const uint32_t before = warp ? warp_tot[warp - 1] : 0u;
+    const T before = warp ? warp_tot[warp - 1] : T(0);
     __syncthreads();  // warp_tot is reused by the next call
-    return v + before;
-}
-
-// Same for 64-bit values (request token offsets).
-__device__ __forceinline__ uint64_t block_incl_scan64(uint64_t v, uint64_t *warp_tot)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        uint64_t w = warp_tot[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t t = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += t;
-        }
-        warp_tot[lane] = w;
-    }
-    __syncthreads();
-    const uint64_t before = warp ? warp_tot[warp - 1] : 0ull;
-    __syncthreads();
     return v + before;
 }
 
@@ -239,16 +567,16 @@ struct SelectSmem {
     uint32_t hist[kHistBins];
     uint64_t cand_key[kCandCap];
     int32_t cand_id[kCandCap];
+    int32_t cand_len[kCandCap];
     uint64_t sure_key[KVI_MAX_K];
     int32_t sure_id[KVI_MAX_K];
+    int32_t sure_len[KVI_MAX_K];
     uint64_t out_key[KVI_MAX_K];
     int32_t out_id[KVI_MAX_K];
     int32_t out_len[KVI_MAX_K];
+    int32_t out_pc[KVI_MAX_K];
     uint32_t warp_tot[32];
-    uint64_t warp_tot64[32];
-    uint32_t n_sure, n_cand, bucket, above, digit, above2;
-    int32_t last;
-    int32_t fit;
+    uint32_t n_sure, n_cand, bucket, above, digit, above2, pop;
 };
 
 // Rank the n_cand candidates in shared memory and move the best `need` of
@@ -263,37 +591,262 @@ __device__ void take_best_candidates(SelectSmem &sm, uint32_t n_cand, uint32_t n
         if (rank < need && base + rank < (uint32_t)KVI_MAX_K) {
             sm.sure_key[base + rank] = kc;
             sm.sure_id[base + rank] = ic;
+            sm.sure_len[base + rank] = sm.cand_len[c];
         }
+    }
+}
+
+__device__ __forceinline__ void add_sure(SelectSmem &sm, uint64_t key, int32_t id, int32_t len)
+{
+    const uint32_t at = atomicAdd(&sm.n_sure, 1u);
+    if (at < (uint32_t)KVI_MAX_K) {
+        sm.sure_key[at] = key;
+        sm.sure_id[at] = id;
+        sm.sure_len[at] = len;
+    }
+}
+
+__device__ __forceinline__ void add_cand(SelectSmem &sm, uint64_t key, int32_t id, int32_t len)
+{
+    const uint32_t at = atomicAdd(&sm.n_cand, 1u);
+    if (at < (uint32_t)kCandCap) {
+        sm.cand_key[at] = key;
+        sm.cand_id[at] = id;
+        sm.cand_len[at] = len;
+    }
+}
+
+// Radix refinement of a crowded first-level bucket b0 on the full 64-bit
+// keys (read from global memory), down to ties broken by the lower id.  Kept
+// out of line: it is rarely taken and its code need not be fetched otherwise.
+__device__ __noinline__ void select_crowded(SelectSmem &sm, const uint64_t *keys, const int32_t *lens,
+                               int64_t N, uint32_t b0, uint32_t need)
+{
+    const int tid = threadIdx.x;
+    uint64_t prefix = 0;
+    uint32_t need_r = need;
+    bool done = false;
+    for (int shift = 56; shift >= 0 && !done; shift -= 8) {
+        for (int b = tid; b < 256; b += kSelectThreads) sm.hist[b] = 0;
+        __syncthreads();
+        for (int64_t i = tid; i < N; i += kSelectThreads) {
+            const uint64_t key = __ldcg(keys + i);
+            if (bucket_of(key) != b0) continue;
+            if (shift < 56 && (key >> (shift + 8)) != prefix) continue;
+            atomicAdd(&sm.hist[(key >> shift) & 0xff], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t run = 0;
+            for (int d = 255; d >= 0; --d) {
+                if (run + sm.hist[d] >= need_r) { sm.digit = (uint32_t)d; sm.above2 = run; break; }
+                run += sm.hist[d];
+            }
+        }
+        __syncthreads();
+        const uint32_t dd = sm.digit;
+        const uint32_t above2 = sm.above2;
+        const uint32_t M2 = sm.hist[dd];
+        for (int64_t i = tid; i < N; i += kSelectThreads) {
+            const uint64_t key = __ldcg(keys + i);
+            if (bucket_of(key) != b0) continue;
+            if (shift < 56 && (key >> (shift + 8)) != prefix) continue;
+            if (((key >> shift) & 0xff) > dd) add_sure(sm, key, (int32_t)i, __ldcg(lens + i));
+        }
+        need_r -= above2;
+        prefix = (prefix << 8) | dd;
+        if (tid == 0) sm.n_cand = 0;
+        __syncthreads();
+        if (M2 <= (uint32_t)kCandCap) {
+            for (int64_t i = tid; i < N; i += kSelectThreads) {
+                const uint64_t key = __ldcg(keys + i);
+                if (bucket_of(key) == b0 && (key >> shift) == prefix)
+                    add_cand(sm, key, (int32_t)i, __ldcg(lens + i));
+            }
+            __syncthreads();
+            take_best_candidates(sm, M2, need_r, sm.n_sure);
+            done = true;
+        }
+        __syncthreads();
+    }
+    if (!done) {
+        // every remaining key equals `prefix`: the lowest ids win.
+        const uint32_t base = sm.n_sure;
+        uint32_t taken = 0;
+        for (int64_t i0 = 0; i0 < N && taken < need_r; i0 += kSelectThreads) {
+            const int64_t i = i0 + tid;
+            uint32_t flag = 0;
+            uint64_t key = 0;
+            if (i < N) {
+                key = __ldcg(keys + i);
+                flag = (bucket_of(key) == b0 && key == prefix) ? 1u : 0u;
+            }
+            const uint32_t incl = block_incl_scan<uint32_t>(flag, sm.warp_tot);
+            const uint32_t at = taken + incl - flag;
+            if (flag && at < need_r && base + at < (uint32_t)KVI_MAX_K) {
+                sm.sure_key[base + at] = key;
+                sm.sure_id[base + at] = (int32_t)i;
+                sm.sure_len[base + at] = __ldcg(lens + i);
+            }
+            taken += sm.warp_tot[31];  // block total of the flags
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+}
+
+// Placement of one request by warp 0: rank order, back to back from the
+// request's start; each fact is cut into the inject kernel's pieces.
+__device__ __forceinline__ void place_request(const SelectParams &p, SelectSmem &sm, int r, bool ok,
+                              const kvi_store_view &st, int64_t start, int32_t tl)
+{
+    const int lane = threadIdx.x;
+    const int32_t k = p.k;
+    if (!ok && lane == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+    constexpr int kPer = (KVI_MAX_K + 31) / 32;
+    const int per = (k + 31) / 32;
+    const int j0 = lane * per;
+    int64_t len_run = 0;
+    int32_t lens_l[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+        const int j = j0 + m;
+        int32_t len = 0;
+        if (m < per && j < k && ok) {
+            const int32_t f = sm.out_id[j];
+            len = sm.out_len[j];
+            if (f < 0 || (int64_t)f >= st.n_facts || len < 0) {
+                record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+                len = 0;
+            }
+        }
+        lens_l[m] = len;
+        len_run += len;
+    }
+    int64_t incl = len_run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+    int fit = ok ? 1 : 0;
+    if (tl < 0 || tl > p.max_blocks) {
+        if (lane == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+        fit = 0;
+    } else if (start < 0 || start + total > (int64_t)tl * p.block_size) {
+        if (lane == 0 && ok) record_status(p.status, KVI_ERR_CAPACITY);
+        fit = 0;
+    }
+    int64_t run = start + incl - len_run;
+    int64_t pieces = 0;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+        const int j = j0 + m;
+        if (m >= per || j >= k) break;
+        const int32_t len = lens_l[m];
+        int32_t pc = 0;
+        if (fit && len > 0) {  // positions fit 31 bits once the request fits its table
+            const uint32_t ct = (uint32_t)p.pg.ct;
+            const uint32_t first = (uint32_t)run / ct, last = (uint32_t)(run + len - 1) / ct;
+            pc = (int32_t)((last - first + 1) * (uint32_t)p.pg.units);
+        }
+        p.pos[(int64_t)r * k + j] = (int32_t)run;
+        p.slot_len[(int64_t)r * k + j] = len;
+        sm.out_pc[j] = pc;
+        pieces += pc;
+        run += len;
+    }
+    int64_t pincl = pieces;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, pincl, o);
+        if (lane >= o) pincl += t;
+    }
+    int64_t prun = pincl - pieces;
+    for (int m = 0; m < per; ++m) {
+        const int j = j0 + m;
+        if (j >= k) break;
+        p.pc[(int64_t)r * (k + 1) + j] = (int32_t)prun;
+        prun += sm.out_pc[j];
+    }
+    if (lane == 31) {
+        p.pc[(int64_t)r * (k + 1) + k] = (int32_t)pincl;
+        p.npc[r] = (int32_t)pincl;
     }
 }
 
 __global__ void __launch_bounds__(kSelectThreads, 1)
 select_kernel(const __grid_constant__ SelectParams p)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     SelectSmem &sm = *reinterpret_cast<SelectSmem *>(smem_raw);
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
     const int32_t k = p.k;
+
+    for (int b = tid; b < kHistBins; b += kSelectThreads) sm.hist[b] = 0;
+    for (int e = tid; e < KVI_MAX_K; e += kSelectThreads) {
+        sm.sure_key[e] = 0;
+        sm.sure_id[e] = -1;
+        sm.sure_len[e] = -1;
+        sm.out_key[e] = 0;
+        sm.out_id[e] = -1;
+        sm.out_len[e] = -1;
+    }
+    if (tid == 0) {
+        sm.n_sure = 0;
+        sm.n_cand = 0;
+    }
+
+    // the request's own inputs can be read before the scoring kernel ends
+    const int64_t start = (p.place && tid < 32) ? (int64_t)p.start_pos[r] : 0;
+    const int32_t tl = (p.place && tid < 32) ? p.table_lens[r] : 0;
+    pdl_wait();  // keys and lengths of the scoring kernel
+    pdl_launch_dependents();
     const kvi_store_view st = load_store(p.store, r);
     const bool ok = !p.store.many || store_ok(st, p.g, p.max_facts, k);
-    const int64_t N = st.n_facts;
+    const int64_t N = ok ? st.n_facts : 0;
     const uint64_t *keys = p.keys + (int64_t)r * p.key_stride;
+    const int32_t *lens = p.lens + (int64_t)r * p.key_stride;
+    // up to kSelectThreads * kKeysPerThread keys (and their lengths) are read
+    // once, in one round trip, and kept in registers; larger stores stream
+    // them from L2 twice
+    const bool in_regs = N <= (int64_t)kSelectThreads * kKeysPerThread;
+    uint64_t kr[kKeysPerThread];
+    int32_t lr[kKeysPerThread];
+    uint32_t br[kKeysPerThread];
+    if (in_regs) {
+#pragma unroll
+        for (int m = 0; m < kKeysPerThread; ++m) {
+            const int64_t i = tid + (int64_t)m * kSelectThreads;
+            kr[m] = i < N ? __ldcg(keys + i) : 0;
+            lr[m] = i < N ? __ldcg(lens + i) : -1;
+        }
+    }
+    __syncthreads();
 
     if (ok) {
-        // 1. the bucket holding the k-th key, from the histogram (bucket
-        //    4095 is the best); thread t owns buckets 4095-4t .. 4092-4t.
-        const uint32_t *gh = p.hist + (int64_t)r * kHistBins;
-        const int top = kHistBins - 1 - 4 * tid;
-        const uint32_t c0 = __ldcg(gh + top), c1 = __ldcg(gh + top - 1);
-        const uint32_t c2 = __ldcg(gh + top - 2), c3 = __ldcg(gh + top - 3);
-        const uint32_t incl = block_incl_scan(c0 + c1 + c2 + c3, sm.warp_tot);
-        const uint32_t excl = incl - (c0 + c1 + c2 + c3);
-        if (tid == 0) { sm.n_sure = 0; sm.n_cand = 0; }
-        for (int e = tid; e < KVI_MAX_K; e += kSelectThreads) {
-            sm.sure_key[e] = 0;
-            sm.sure_id[e] = -1;
+        // 1. histogram of the first-level buckets
+        if (in_regs) {
+#pragma unroll
+            for (int m = 0; m < kKeysPerThread; ++m) {
+                br[m] = bucket_of(kr[m]);
+                if (tid + (int64_t)m * kSelectThreads < N) atomicAdd(&sm.hist[br[m]], 1u);
+            }
+        } else {
+#pragma unroll 4
+            for (int64_t i = tid; i < N; i += kSelectThreads)
+                atomicAdd(&sm.hist[bucket_of(__ldcg(keys + i))], 1u);
         }
+        __syncthreads();
+        // 2. the bucket holding the k-th key (bucket 4095 is the best);
+        //    thread t owns buckets 4095-4t .. 4092-4t.
+        const int top = kHistBins - 1 - 4 * tid;
+        const uint32_t c0 = sm.hist[top], c1 = sm.hist[top - 1];
+        const uint32_t c2 = sm.hist[top - 2], c3 = sm.hist[top - 3];
+        const uint32_t incl = block_incl_scan<uint32_t>(c0 + c1 + c2 + c3, sm.warp_tot);
+        const uint32_t excl = incl - (c0 + c1 + c2 + c3);
         if (excl < (uint32_t)k && incl >= (uint32_t)k) {
             const uint32_t cs[4] = {c0, c1, c2, c3};
             uint32_t run = excl;
@@ -301,7 +854,7 @@ select_kernel(const __grid_constant__ SelectParams p)
                 if (run + cs[j] >= (uint32_t)k) {
                     sm.bucket = (uint32_t)(top - j);
                     sm.above = run;
-                    sm.hist[0] = cs[j];  // population of the k-th bucket
+                    sm.pop = cs[j];
                     break;
                 }
                 run += cs[j];
@@ -310,203 +863,96 @@ select_kernel(const __grid_constant__ SelectParams p)
         __syncthreads();
         const uint32_t b0 = sm.bucket;
         const uint32_t above = sm.above;
-        const uint32_t M = sm.hist[0];
+        const uint32_t M = sm.pop;
         const uint32_t need = (uint32_t)k - above;
 
-        // 2. keys above the bucket are in; keys in it are candidates.
-        for (int64_t i = tid; i < N; i += kSelectThreads) {
-            const uint64_t key = __ldcg(keys + i);
-            const uint32_t b = bucket_of(key);
-            if (b > b0) {
-                const uint32_t at = atomicAdd(&sm.n_sure, 1u);
-                if (at < (uint32_t)KVI_MAX_K) { sm.sure_key[at] = key; sm.sure_id[at] = (int32_t)i; }
-            } else if (b == b0 && M <= (uint32_t)kCandCap) {
-                const uint32_t at = atomicAdd(&sm.n_cand, 1u);
-                if (at < (uint32_t)kCandCap) { sm.cand_key[at] = key; sm.cand_id[at] = (int32_t)i; }
+        // 3. keys above the bucket are in; keys in it are candidates.
+        const bool direct = M <= (uint32_t)kCandCap;
+        if (in_regs) {
+#pragma unroll
+            for (int m = 0; m < kKeysPerThread; ++m) {
+                const int64_t i = tid + (int64_t)m * kSelectThreads;
+                if (i >= N) continue;
+                const uint32_t b = br[m];
+                if (b > b0) add_sure(sm, kr[m], (int32_t)i, lr[m]);
+                else if (b == b0 && direct) add_cand(sm, kr[m], (int32_t)i, lr[m]);
             }
-        }
-        __syncthreads();
-
-        if (M <= (uint32_t)kCandCap) {
-            take_best_candidates(sm, M, need, above);
         } else {
-            // 3. crowded bucket: radix select on the 64-bit key, 8 bits at a
-            //    time, restricted to bucket b0.
-            uint64_t prefix = 0;
-            uint32_t need_r = need;
-            bool done = false;
-            for (int shift = 56; shift >= 0 && !done; shift -= 8) {
-                for (int b = tid; b < 256; b += kSelectThreads) sm.hist[b] = 0;
-                __syncthreads();
-                for (int64_t i = tid; i < N; i += kSelectThreads) {
-                    const uint64_t key = __ldcg(keys + i);
-                    if (bucket_of(key) != b0) continue;
-                    if (shift < 56 && (key >> (shift + 8)) != prefix) continue;
-                    atomicAdd(&sm.hist[(key >> shift) & 0xff], 1u);
-                }
-                __syncthreads();
-                if (tid == 0) {
-                    uint32_t run = 0;
-                    for (int d = 255; d >= 0; --d) {
-                        if (run + sm.hist[d] >= need_r) { sm.digit = (uint32_t)d; sm.above2 = run; break; }
-                        run += sm.hist[d];
-                    }
-                }
-                __syncthreads();
-                const uint32_t dd = sm.digit;
-                const uint32_t above2 = sm.above2;
-                const uint32_t M2 = sm.hist[dd];
-                // keys of the current prefix with a larger digit are in
-                for (int64_t i = tid; i < N; i += kSelectThreads) {
-                    const uint64_t key = __ldcg(keys + i);
-                    if (bucket_of(key) != b0) continue;
-                    if (shift < 56 && (key >> (shift + 8)) != prefix) continue;
-                    if (((key >> shift) & 0xff) > dd) {
-                        const uint32_t at = atomicAdd(&sm.n_sure, 1u);
-                        if (at < (uint32_t)KVI_MAX_K) { sm.sure_key[at] = key; sm.sure_id[at] = (int32_t)i; }
-                    }
-                }
-                need_r -= above2;
-                prefix = (prefix << 8) | dd;
-                if (tid == 0) sm.n_cand = 0;
-                __syncthreads();
-                if (M2 <= (uint32_t)kCandCap) {
-                    for (int64_t i = tid; i < N; i += kSelectThreads) {
-                        const uint64_t key = __ldcg(keys + i);
-                        if (bucket_of(key) != b0 || (key >> shift) != prefix) continue;
-                        const uint32_t at = atomicAdd(&sm.n_cand, 1u);
-                        if (at < (uint32_t)kCandCap) { sm.cand_key[at] = key; sm.cand_id[at] = (int32_t)i; }
-                    }
-                    __syncthreads();
-                    const uint32_t base = sm.n_sure;
-                    take_best_candidates(sm, M2, need_r, base);
-                    done = true;
-                }
-                __syncthreads();
-            }
-            if (!done) {
-                // every remaining key equals `prefix`: the lowest ids win.
-                const uint32_t base = sm.n_sure;
-                uint32_t taken = 0;
-                for (int64_t i0 = 0; i0 < N && taken < need_r; i0 += kSelectThreads) {
-                    const int64_t i = i0 + tid;
-                    uint32_t flag = 0;
-                    uint64_t key = 0;
-                    if (i < N) {
-                        key = __ldcg(keys + i);
-                        flag = (bucket_of(key) == b0 && key == prefix) ? 1u : 0u;
-                    }
-                    const uint32_t incl2 = block_incl_scan(flag, sm.warp_tot);
-                    const uint32_t at = taken + incl2 - flag;
-                    if (flag && at < need_r && base + at < (uint32_t)KVI_MAX_K) {
-                        sm.sure_key[base + at] = key;
-                        sm.sure_id[base + at] = (int32_t)i;
-                    }
-                    taken += sm.warp_tot[31];  // block total of flags
-                    __syncthreads();
-                }
+#pragma unroll 4
+            for (int64_t i = tid; i < N; i += kSelectThreads) {
+                const uint64_t key = __ldcg(keys + i);
+                const uint32_t b = bucket_of(key);
+                if (b > b0) add_sure(sm, key, (int32_t)i, __ldcg(lens + i));
+                else if (b == b0 && direct) add_cand(sm, key, (int32_t)i, __ldcg(lens + i));
             }
         }
         __syncthreads();
+        if (direct) take_best_candidates(sm, M, need, above);
+        else select_crowded(sm, keys, lens, N, b0, need);
+        __syncthreads();
 
-        // 4. sort the k selected keys into rank order.
+        // 4. the k selected keys in rank order.
         for (int e = tid; e < k; e += kSelectThreads) {
             const uint64_t ke = sm.sure_key[e];
             const int32_t ie = sm.sure_id[e];
             int rank = 0;
+#pragma unroll 8
             for (int o = 0; o < k; ++o) rank += better(sm.sure_key[o], sm.sure_id[o], ke, ie);
             sm.out_key[rank] = ke;
             sm.out_id[rank] = ie;
+            sm.out_len[rank] = sm.sure_len[e];
         }
         __syncthreads();
     }
 
     for (int j = tid; j < k; j += kSelectThreads) {
         p.ids[(int64_t)r * k + j] = ok ? sm.out_id[j] : -1;
-        p.scores[(int64_t)r * k + j] = ok ? __double2float_rn(unorder_key(sm.out_key[j])) : __int_as_float(0x7fc00000);
+        p.scores[(int64_t)r * k + j] =
+            ok ? key_score(sm.out_key[j]) : __int_as_float(0x7fc00000);
     }
-    if (!p.place) return;
-
-    // 5. placement: rank order, back to back from the request's start.
-    if (!ok && tid == 0) record(p.status, KVI_ERR_OUT_OF_RANGE);
-    for (int j = tid; j < k; j += kSelectThreads) {
-        int32_t len = 0;
-        if (ok) {
-            const int32_t f = sm.out_id[j];
-            if (f >= 0 && (int64_t)f < N) {
-                const int64_t s0 = st.fact_start[f];
-                const int32_t l0 = st.fact_len[f];
-                if (l0 >= 0 && s0 >= 0 && s0 + l0 <= st.n_tokens) len = l0;
-                else record(p.status, KVI_ERR_OUT_OF_RANGE);
-            } else {
-                record(p.status, KVI_ERR_OUT_OF_RANGE);
-            }
-        }
-        sm.out_len[j] = len;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const int64_t start = p.start_pos[r];
-        const int32_t tl = p.table_lens[r];
-        int64_t run = 0;
-        for (int j = 0; j < k; ++j) {
-            p.cum[(int64_t)r * (k + 1) + j] = (int32_t)run;
-            p.pos[(int64_t)r * k + j] = (int32_t)(start + run);
-            run += sm.out_len[j];
-        }
-        p.cum[(int64_t)r * (k + 1) + k] = (int32_t)run;
-        int fit = 1;
-        if (tl < 0 || tl > p.max_blocks) { record(p.status, KVI_ERR_OUT_OF_RANGE); fit = 0; }
-        else if (start < 0 || start + run > (int64_t)tl * p.block_size) { record(p.status, KVI_ERR_CAPACITY); fit = 0; }
-        p.tok[r] = fit && ok ? run : 0;
-        __threadfence();
-        const uint32_t prev = atomicAdd(p.counter, 1u);
-        sm.last = (prev == (uint32_t)(p.R - 1));
-    }
-    __syncthreads();
-    if (!sm.last) return;
-    // 6. last CTA: request token offsets (exclusive prefix over requests).
-    __threadfence();
-    int64_t carry = 0;
-    for (int r0 = 0; r0 < p.R; r0 += kSelectThreads) {
-        const int rr = r0 + tid;
-        const uint64_t t = rr < p.R ? (uint64_t)__ldcg(p.tok + rr) : 0ull;
-        const uint64_t incl2 = block_incl_scan64(t, sm.warp_tot64);
-        if (rr < p.R) p.req_off[rr] = carry + (int64_t)(incl2 - t);
-        carry += (int64_t)sm.warp_tot64[31];
-        __syncthreads();
-    }
-    if (tid == 0) p.req_off[p.R] = carry;
+    if (p.place && tid < 32) place_request(p, sm, r, ok, st, start, tl);
 }
 
 // ---------------------------------------------------------------- placement
 
-__global__ void __launch_bounds__(256) place_kernel(const __grid_constant__ PlaceParams p)
+__global__ void __launch_bounds__(32) place_kernel(const __grid_constant__ PlaceParams p)
 {
-    __shared__ int32_t lens[KVI_MAX_K];
-    for (int j = threadIdx.x; j < p.n; j += blockDim.x) {
-        const int32_t f = p.ids[j];
-        int32_t len = 0;
-        if (f >= 0 && (int64_t)f < p.store.n_facts) len = max(0, p.store.fact_len[f]);
-        else record(p.status, KVI_ERR_OUT_OF_RANGE);
-        lens[j] = len;
+    const int lane = threadIdx.x;
+    const int per = (p.n + 31) / 32;
+    const int j0 = lane * per;
+    int64_t run = 0;
+    for (int m = 0; m < per && j0 + m < p.n; ++m) {
+        const int32_t f = p.ids[j0 + m];
+        if (f >= 0 && (int64_t)f < p.store.n_facts) run += max(0, p.store.fact_len[f]);
+        else record_status(p.status, KVI_ERR_OUT_OF_RANGE);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int64_t run = p.start;
-        for (int j = 0; j < p.n; ++j) {
-            p.pos[j] = (int32_t)run;
-            run += lens[j];
-        }
-        if (run > 0x7fffffff) record(p.status, KVI_ERR_OUT_OF_RANGE);
+    int64_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
     }
+    int64_t at = p.start + incl - run;
+    for (int m = 0; m < per && j0 + m < p.n; ++m) {
+        const int32_t f = p.ids[j0 + m];
+        p.pos[j0 + m] = (int32_t)at;
+        if (f >= 0 && (int64_t)f < p.store.n_facts) at += max(0, p.store.fact_len[f]);
+    }
+    if (lane == 31 && p.start + incl > 0x7fffffff) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
 }
 
 template <int NV>
 cudaError_t launch_score_nv(const ScoreParams &p, cudaStream_t s)
 {
-    const unsigned gx = (unsigned)((p.max_facts + p.rows_per_cta - 1) / p.rows_per_cta);
-    score_kernel<NV><<<dim3(gx, (unsigned)p.R), kScoreThreads, 0, s>>>(p);
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = (int64_t)p.R * p.max_facts;
+    const int64_t warps = (rows + 1) / 2;  // at least two rows per warp
+    const int64_t cap = (int64_t)di.sms * 2 * (kScoreThreads / 32);
+    const int64_t w = warps < cap ? warps : cap;
+    const unsigned blocks = (unsigned)((w + kScoreThreads / 32 - 1) / (kScoreThreads / 32));
+    score_kernel<NV><<<blocks, kScoreThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -515,6 +961,18 @@ cudaError_t launch_score_nv(const ScoreParams &p, cudaStream_t s)
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s)
 {
     const int E = p.g.embed_dim;
+    if (E * 4 <= 8192) {
+        DeviceInfo di;
+        cudaError_t e = device_info(&di);
+        if (e != cudaSuccess) return e;
+        const int smem = (int)sizeof(ScoreRingSmem);
+        e = smem_opt_in(score_ring_kernel, smem);
+        if (e != cudaSuccess) return e;
+        const int64_t rows = (int64_t)p.R * p.max_facts;
+        const int64_t blocks = rows < di.sms ? rows : di.sms;
+        score_ring_kernel<<<(unsigned)blocks, kRingThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    }
     if (E % 128 == 0) {
         switch (E / 128) {
         case 1: return launch_score_nv<1>(p, s);
@@ -531,19 +989,30 @@ cudaError_t launch_score(const ScoreParams &p, cudaStream_t s)
     return launch_score_nv<0>(p, s);
 }
 
-cudaError_t launch_select(const SelectParams &p, cudaStream_t s)
+cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl)
 {
     static_assert(sizeof(SelectSmem) <= 227 * 1024, "select smem");
     const int smem = (int)sizeof(SelectSmem);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = smem_opt_in(select_kernel, smem);
     if (e != cudaSuccess) return e;
-    select_kernel<<<(unsigned)p.R, kSelectThreads, smem, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.R);
+    cfg.blockDim = dim3(kSelectThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, select_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_place(const PlaceParams &p, cudaStream_t s)
 {
-    place_kernel<<<1, 256, 0, s>>>(p);
+    place_kernel<<<1, 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

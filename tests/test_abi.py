@@ -46,7 +46,7 @@ def test_only_declared_symbols_are_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(5):
+    for s in range(6):
         assert kvi.kvi_status_str(s)
     assert kvi.kvi_status_str(99) == "unknown status"
 
