@@ -14,12 +14,14 @@
 //   - work is cut into pieces: up to `ct` consecutive tokens of one fact that
 //     fall in one page (ct divides the page size), for one layer and one of
 //     K/V, at most 8 KB; in the store and in the page a piece is one
-//     contiguous run of bytes.  A CTA takes a contiguous range of
-//     (piece, K|V, layer) items, layer innermost;
-//   - a producer warp resolves 32 items at a time (one per lane) and its
-//     lane 0 moves each piece into the next of 24 shared-memory stages with
+//     contiguous run of bytes.  Items (piece, K|V, layer), layer innermost,
+//     are handed out in chunks of 24 from a counter in the workspace (fused
+//     calls), or as one contiguous range per CTA (split calls);
+//   - a producer warp resolves 32 items at a time (one per lane) and each
+//     lane moves its piece into its shared-memory stage (24 in all) with
 //     cp.async.bulk, completion tracked by the stage's "full" mbarrier, so up
-//     to 24 pieces (~170 KB) per SM are in flight whatever the registers;
+//     to 24 pieces (~170 KB) per SM are in flight whatever the registers
+//     (issuing from all lanes: one issuing thread caps the copy rate);
 //   - twelve consumer warps take the stages round-robin: a V piece is copied
 //     out unchanged, a K piece is rotated (each lane takes rotate-half pairs
 //     of one (token, vector) group, elements [8v, 8v+8) and
@@ -55,7 +57,8 @@ struct PieceDesc {
     uint32_t bytes;  // 0: nothing to do
     int32_t pos0;
     int32_t ntok;
-    int32_t kv;
+    int16_t kv;
+    int16_t stop;    // 1: no more pieces for this consumer
 };
 
 struct __align__(128) InjSmem {
@@ -354,20 +357,6 @@ __device__ Piece resolve_piece(const InjectParams &p, const int32_t *prefix, int
     return x;
 }
 
-__device__ __forceinline__ Piece shfl_piece(const Piece &x, int src)
-{
-    Piece y;
-    y.src = reinterpret_cast<const uint8_t *>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(x.src), src));
-    y.dst = reinterpret_cast<uint8_t *>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(x.dst), src));
-    y.bytes = __shfl_sync(0xffffffffu, x.bytes, src);
-    y.pos0 = __shfl_sync(0xffffffffu, x.pos0, src);
-    y.ntok = __shfl_sync(0xffffffffu, x.ntok, src);
-    y.kv = __shfl_sync(0xffffffffu, x.kv, src);
-    return y;
-}
-
 // counts in a[1..n] -> exclusive prefix a[0..n] (a[0] = 0), whole CTA.
 __device__ void cta_prefix(int32_t *a, int n, int32_t *part)
 {
@@ -446,50 +435,82 @@ inject_kernel(const __grid_constant__ InjectParams p)
     __syncthreads();
     cta_prefix(sm.prefix, count, sm.part);
     const int64_t total = (int64_t)sm.prefix[count] * 2 * p.L;
-    // this CTA's contiguous range of items
+    // static partition: a contiguous range of items per CTA (split calls);
+    // dynamic: producers take chunks of kInjRing items from a shared counter
+    // (fused calls), which balances pieces of unequal size across SMs
+    const bool dynamic = p.work != nullptr;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-    const int64_t it0 = (int64_t)blockIdx.x * per;
-    const int64_t n_items = total > it0 ? min(per, total - it0) : 0;
+    const int64_t it0 = dynamic ? 0 : (int64_t)blockIdx.x * per;
+    const int64_t n_static = total > it0 ? min(per, total - it0) : 0;
 
     if (warp == kInjConsumers) {
-        // producer
-        for (int64_t base = 0; base < n_items; base += 32) {
-            Piece mine{nullptr, nullptr, 0u, 0, 0, 0};
-            if (base + lane < n_items) mine = resolve_piece(p, sm.prefix, it0 + base + lane);
-            const int nb = (int)min((int64_t)32, n_items - base);
-            bool ok = true;
-            for (int i = 0; i < nb; ++i) {
-                const Piece x = shfl_piece(mine, i);
-                if (lane == 0) {
-                    const int64_t j = base + i;
-                    const int s = (int)(j % kInjRing);
-                    const int64_t round = j / kInjRing;
-                    if (round > 0 && !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1),
-                                                kWaitLimitNs)) {
-                        record_status(p.status, KVI_ERR_TIMEOUT);
-                        ok = false;
+        // producer warp: each lane resolves one of kInjRing consecutive items
+        // and issues its copy itself (a single issuing thread caps the
+        // bulk-copy rate well below the SM's share of HBM bandwidth); each
+        // lane waits on its own item's stage, and no two lanes of a batch
+        // share one
+        static_assert(kInjRing <= 32, "one batch per warp");
+        int64_t local = 0;   // items this CTA has staged
+        int64_t taken = 0;   // items of the static range taken
+        bool ok = true;
+        for (;;) {
+            int64_t first;
+            int nb;
+            if (dynamic) {
+                unsigned long long got = 0;
+                if (lane == 0) got = atomicAdd(p.work, (unsigned long long)kInjRing);
+                first = (int64_t)__shfl_sync(0xffffffffu, got, 0);
+                if (first >= total) break;
+                nb = (int)min((int64_t)kInjRing, total - first);
+            } else {
+                if (taken >= n_static) break;
+                first = it0 + taken;
+                nb = (int)min((int64_t)kInjRing, n_static - taken);
+                taken += nb;
+            }
+            const int64_t j = local + lane;
+            if (lane < nb) {
+                const Piece x = resolve_piece(p, sm.prefix, first + lane);
+                const int s = (int)(j % kInjRing);
+                const int64_t round = j / kInjRing;
+                if (round > 0 &&
+                    !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1), kWaitLimitNs)) {
+                    record_status(p.status, KVI_ERR_TIMEOUT);
+                    ok = false;
+                } else {
+                    sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
+                    const uint32_t fb = smem_u32(&sm.full[s]);
+                    if (x.bytes) {
+                        fence_async_smem();
+                        mbar_expect_tx(fb, x.bytes);
+                        bulk_load(smem_u32(sm.stage[s]), x.src, x.bytes, fb);
                     } else {
-                        sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, x.kv};
-                        const uint32_t fb = smem_u32(&sm.full[s]);
-                        if (x.bytes) {
-                            fence_async_smem();
-                            mbar_expect_tx(fb, x.bytes);
-                            bulk_load(smem_u32(sm.stage[s]), x.src, x.bytes, fb);
-                        } else {
-                            mbar_arrive(fb);
-                        }
+                        mbar_arrive(fb);
                     }
                 }
-                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             }
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            local += nb;
+            if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        // one stop descriptor for each consumer's next item
+        if (ok && lane < kInjConsumers) {
+            const int64_t j = local + lane;
+            const int s = (int)(j % kInjRing);
+            const int64_t round = j / kInjRing;
+            if (round > 0 &&
+                !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1), kWaitLimitNs)) {
+                record_status(p.status, KVI_ERR_TIMEOUT);
+            } else {
+                sm.desc[s] = PieceDesc{nullptr, 0u, 0, 0, 0, 1};
+                mbar_arrive(smem_u32(&sm.full[s]));
+            }
         }
     } else {
-        // consumers
+        // consumers: this CTA's staged items warp, warp + 12, ... until a stop
         TableCache tc;
         tc.p = -1;
         tc.v = -1;
-        for (int64_t j = warp; j < n_items; j += kInjConsumers) {
+        for (int64_t j = warp;; j += kInjConsumers) {
             const int s = (int)(j % kInjRing);
             const uint32_t parity = (uint32_t)((j / kInjRing) & 1);
             const bool ok = mbar_wait(smem_u32(&sm.full[s]), parity, kWaitLimitNs);
@@ -498,6 +519,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 break;
             }
             const PieceDesc d = sm.desc[s];
+            if (d.stop) break;
             const uint8_t *stg = sm.stage[s];
             if (d.bytes) {
                 if (d.kv) copy_piece(stg, d.dst, d.bytes, lane);

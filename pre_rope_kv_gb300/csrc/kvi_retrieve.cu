@@ -331,7 +331,8 @@ score_kernel(const __grid_constant__ ScoreParams p)
 }
 
 // Ring variant (rows of at most 8 KB, i.e. E <= 2048): one CTA per SM; a
-// producer lane streams the CTA's contiguous range of fact rows into a ring
+// producer warp (all lanes issuing) streams the CTA's contiguous range of
+// fact rows into a ring
 // of shared-memory stages (one row per stage, 192 KB in all) with
 // cp.async.bulk, and twelve consumer warps take the rows round-robin, each
 // lane reading its float4 slots from shared memory and keeping four
@@ -436,37 +437,40 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
     sc.ok = false;
 
     if (warp == kRingConsumers) {
-        // producer: one row per stage, stage index and phase kept incrementally
-        if (lane != 0) return;
-        RowCursor cur;
-        cur.init(g0, p.max_facts);
-        int s = 0;
-        uint32_t round = 0;
-        for (int64_t j = 0; j < n; ++j) {
-            if (round > 0 && !ring_wait(smem_addr(&sm.empty[s]), (round - 1) & 1u)) {
-                record_status(p.status, KVI_ERR_TIMEOUT);
-                return;
+        // producer warp: every lane issues copies, rows base + lane for
+        // base = 0, 32, 64, ... (a single issuing thread caps the bulk-copy
+        // rate far below the SM's share of HBM bandwidth); each lane waits on
+        // its own row's stage
+        for (int64_t base = 0; base < n; base += 32) {
+            const int64_t j = base + lane;
+            bool ok = true;
+            if (j < n) {
+                const int s = (int)(j % S);
+                const uint32_t round = (uint32_t)(j / S);
+                RowCursor cur;
+                cur.init(g0 + j, p.max_facts);
+                if (round > 0 && !ring_wait(smem_addr(&sm.empty[s]), (round - 1) & 1u)) {
+                    record_status(p.status, KVI_ERR_TIMEOUT);
+                    ok = false;
+                } else {
+                    sc.get(p, cur.r);
+                    const uint32_t fb = smem_addr(&sm.full[s]);
+                    if (sc.live(cur.i)) {
+                        if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                                     "r"(row_bytes)
+                                     : "memory");
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                            "%2, [%3];" ::"r"(smem_addr(sm.ring + (size_t)s * row_bytes)),
+                            "l"(sc.st.emb + cur.i * E), "r"(row_bytes), "r"(fb)
+                            : "memory");
+                    } else {
+                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
+                    }
+                }
             }
-            sc.get(p, cur.r);
-            const uint32_t fb = smem_addr(&sm.full[s]);
-            if (sc.live(cur.i)) {
-                if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                             "r"(row_bytes)
-                             : "memory");
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-                    "[%3];" ::"r"(smem_addr(sm.ring + (size_t)s * row_bytes)),
-                    "l"(sc.st.emb + cur.i * E), "r"(row_bytes), "r"(fb)
-                    : "memory");
-            } else {
-                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
-            }
-            cur.advance(1, p.max_facts);
-            if (++s == S) {
-                s = 0;
-                ++round;
-            }
+            if (!__all_sync(0xffffffffu, ok)) return;
         }
         return;
     }
@@ -911,6 +915,7 @@ select_kernel(const __grid_constant__ SelectParams p)
             ok ? key_score(sm.out_key[j]) : __int_as_float(0x7fc00000);
     }
     if (p.place && tid < 32) place_request(p, sm, r, ok, st, start, tl);
+    if (p.place && r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
 }
 
 // ---------------------------------------------------------------- placement
