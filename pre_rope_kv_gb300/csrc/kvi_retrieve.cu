@@ -583,16 +583,26 @@ struct SelectSmem {
     uint32_t n_sure, n_cand, bucket, above, digit, above2, pop;
 };
 
+// Rank of entry e among n entries (keys[], ids[]): how many of them are
+// better.  One warp per entry, the lanes splitting the comparisons.
+__device__ __forceinline__ uint32_t warp_rank(const uint64_t *keys, const int32_t *ids, uint32_t n,
+                                              uint64_t ke, int32_t ie, int lane)
+{
+    uint32_t rank = 0;
+    for (uint32_t o = lane; o < n; o += 32) rank += better(keys[o], ids[o], ke, ie);
+    return __reduce_add_sync(0xffffffffu, rank);
+}
+
 // Rank the n_cand candidates in shared memory and move the best `need` of
 // them to the sure list (positions base .. base + need).
 __device__ void take_best_candidates(SelectSmem &sm, uint32_t n_cand, uint32_t need, uint32_t base)
 {
-    for (uint32_t c = threadIdx.x; c < n_cand; c += kSelectThreads) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (uint32_t c = warp; c < n_cand; c += kSelectThreads / 32) {
         const uint64_t kc = sm.cand_key[c];
         const int32_t ic = sm.cand_id[c];
-        uint32_t rank = 0;
-        for (uint32_t o = 0; o < n_cand; ++o) rank += better(sm.cand_key[o], sm.cand_id[o], kc, ic);
-        if (rank < need && base + rank < (uint32_t)KVI_MAX_K) {
+        const uint32_t rank = warp_rank(sm.cand_key, sm.cand_id, n_cand, kc, ic, lane);
+        if (lane == 0 && rank < need && base + rank < (uint32_t)KVI_MAX_K) {
             sm.sure_key[base + rank] = kc;
             sm.sure_id[base + rank] = ic;
             sm.sure_len[base + rank] = sm.cand_len[c];
@@ -896,15 +906,18 @@ select_kernel(const __grid_constant__ SelectParams p)
         __syncthreads();
 
         // 4. the k selected keys in rank order.
-        for (int e = tid; e < k; e += kSelectThreads) {
-            const uint64_t ke = sm.sure_key[e];
-            const int32_t ie = sm.sure_id[e];
-            int rank = 0;
-#pragma unroll 8
-            for (int o = 0; o < k; ++o) rank += better(sm.sure_key[o], sm.sure_id[o], ke, ie);
-            sm.out_key[rank] = ke;
-            sm.out_id[rank] = ie;
-            sm.out_len[rank] = sm.sure_len[e];
+        {
+            const int lane = tid & 31, warp = tid >> 5;
+            for (int e = warp; e < k; e += kSelectThreads / 32) {
+                const uint64_t ke = sm.sure_key[e];
+                const int32_t ie = sm.sure_id[e];
+                const uint32_t rank = warp_rank(sm.sure_key, sm.sure_id, (uint32_t)k, ke, ie, lane);
+                if (lane == 0 && rank < (uint32_t)KVI_MAX_K) {
+                    sm.out_key[rank] = ke;
+                    sm.out_id[rank] = ie;
+                    sm.out_len[rank] = sm.sure_len[e];
+                }
+            }
         }
         __syncthreads();
     }
