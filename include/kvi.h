@@ -216,6 +216,36 @@ KVI_API kvi_status kvi_retrieve_and_inject(
     float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
     int32_t *d_status, kvi_stream_t stream);
 
+/* No-allocation retrieval.  The paper has no counterpart: this call exists
+ * for callers that cannot allocate device memory where they retrieve -- a
+ * serving engine that has reserved nearly all GPU memory for its own KV pool
+ * and gives a plugin only the buffers of a request, a latency-bound loop that
+ * must not call cudaMalloc/cudaFree (they can synchronise the device), or a
+ * C caller without an allocator.  It computes exactly what kvi_retrieve_topk
+ * computes (same kernels, same results) but keeps its scratch in a fixed
+ * array of KVI_NOALLOC_SCRATCH_BYTES of device memory that belongs to the
+ * library instead of a caller workspace; it calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   - The array exists on every GPU that loads the library, until the
+ *     process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps whatever the
+ *     last call left; nothing in it has to start at zero.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads, or before the
+ *     previous call's kernels have finished on an unordered stream) race on
+ *     it; order them on one stream.
+ *   - n_facts must be <= KVI_NOALLOC_MAX_FACTS; larger stores are rejected
+ *     with KVI_ERR_INVALID_ARG (use kvi_retrieve_topk with a workspace).
+ * Arguments, outputs and other errors are those of kvi_retrieve_topk. */
+#define KVI_NOALLOC_MAX_FACTS 65536
+#define KVI_NOALLOC_SCRATCH_BYTES (KVI_NOALLOC_MAX_FACTS * 12 + 65536)
+KVI_API kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store,
+                                             const float *d_query, int32_t k,
+                                             int32_t *d_ids, float *d_scores,
+                                             kvi_stream_t stream);
+
 /* Tracing: when n_events == 3, the calling thread's next
  * kvi_retrieve_and_inject calls record events[0] before the first kernel,
  * events[1] once retrieval and placement are enqueued and events[2] after

@@ -15,7 +15,8 @@ from ._binding import (  # noqa: F401
     LIB_PATH, MAX_REQUESTS,
     MAX_INJECT_FACTS, MAX_K, MAX_LAYERS, OK, Geometry, KviError, PagedCache, StoreSizes,
     StoreView, geometry, kvi_inject_paged, kvi_last_error, kvi_place, kvi_prepare_rope,
-    kvi_retrieve_and_inject, kvi_retrieve_topk, kvi_status_str, kvi_store_layout,
+    kvi_retrieve_and_inject, kvi_retrieve_topk, kvi_retrieve_topk_noalloc, kvi_status_str,
+    kvi_store_layout, NOALLOC_MAX_FACTS,
     kvi_trace_stages, kvi_workspace_bytes, load_library, pack_store_views, paged_cache,
     store_view,
 )

@@ -32,8 +32,9 @@ MAX_INJECT_FACTS = 4096
 EXPORTED_SYMBOLS = (
     "kvi_store_layout", "kvi_prepare_rope", "kvi_workspace_bytes", "kvi_retrieve_topk",
     "kvi_place", "kvi_inject_paged", "kvi_retrieve_and_inject", "kvi_trace_stages",
-    "kvi_status_str", "kvi_last_error",
+    "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc",
 )
+NOALLOC_MAX_FACTS = 65536
 
 
 class KviError(RuntimeError):
@@ -90,6 +91,7 @@ def load_library(path: str | None = None):
                                         i32, ctypes.POINTER(PagedCache), f64, P, P, P, P, sz,
                                         P, P]),
         "kvi_trace_stages": (S, [P, i32]),
+        "kvi_retrieve_topk_noalloc": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -189,6 +191,14 @@ def kvi_retrieve_topk(store: StoreView, query, k: int, ids, scores, ws, stream=N
     _check(load_library().kvi_retrieve_topk(
         ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)), "kvi_retrieve_topk")
+
+
+def kvi_retrieve_topk_noalloc(store: StoreView, query, k: int, ids, scores, stream=None) -> None:
+    """kvi_retrieve_topk without a workspace: the scratch is a fixed array of
+    the library (see include/kvi.h for who needs this and its limits)."""
+    _check(load_library().kvi_retrieve_topk_noalloc(
+        ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _stream(stream)),
+        "kvi_retrieve_topk_noalloc")
 
 
 def kvi_place(store: StoreView, ids, n: int, start: int, pos, status=None, stream=None) -> None:

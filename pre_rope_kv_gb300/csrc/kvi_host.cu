@@ -229,6 +229,10 @@ cudaError_t device_info(DeviceInfo *out)
     return cudaSuccess;
 }
 
+kvi_status set_error(kvi_status s, const char *msg) { return fail(s, "%s", msg); }
+
+kvi_status check_retrieval_store(const kvi_store_view *s) { return check_store(s, true, false); }
+
 cudaError_t smem_opt_in_raw(const void *kernel, int bytes)
 {
     int dev = 0;

@@ -134,6 +134,11 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl);
 cudaError_t launch_place(const PlaceParams &p, cudaStream_t s);
 cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl);
 
+// Record a message for kvi_last_error() on this thread and return `s`.
+kvi_status set_error(kvi_status s, const char *msg);
+// The store checks kvi_retrieve_topk applies (geometry, n_facts, emb).
+kvi_status check_retrieval_store(const kvi_store_view *s);
+
 // Device facts cached per device (SM count).
 struct DeviceInfo {
     int sms;
