@@ -436,8 +436,8 @@ inject_kernel(const __grid_constant__ InjectParams p)
     cta_prefix(sm.prefix, count, sm.part);
     const int64_t total = (int64_t)sm.prefix[count] * 2 * p.L;
     // static partition: a contiguous range of items per CTA (split calls);
-    // dynamic: producers take chunks of kInjRing items from a shared counter
-    // (fused calls), which balances pieces of unequal size across SMs
+    // dynamic: producers claim chunks of up to kInjRing items from a shared
+    // counter (fused calls), which balances pieces of unequal size across SMs
     const bool dynamic = p.work != nullptr;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t it0 = dynamic ? 0 : (int64_t)blockIdx.x * per;
@@ -452,16 +452,22 @@ inject_kernel(const __grid_constant__ InjectParams p)
         static_assert(kInjRing <= 32, "one batch per warp");
         int64_t local = 0;   // items this CTA has staged
         int64_t taken = 0;   // items of the static range taken
+        int want = kInjRing; // size of the next dynamic claim
         bool ok = true;
         for (;;) {
             int64_t first;
             int nb;
             if (dynamic) {
                 unsigned long long got = 0;
-                if (lane == 0) got = atomicAdd(p.work, (unsigned long long)kInjRing);
+                if (lane == 0) got = atomicAdd(p.work, (unsigned long long)want);
                 first = (int64_t)__shfl_sync(0xffffffffu, got, 0);
                 if (first >= total) break;
-                nb = (int)min((int64_t)kInjRing, total - first);
+                nb = (int)min((int64_t)want, total - first);
+                // guided self-scheduling: once fewer than two full claims per
+                // CTA are left, claim a share of what is left (at least 2),
+                // so that the CTAs run out of work at nearly the same time
+                const int64_t left = total - first - nb;
+                want = (int)max((int64_t)2, min((int64_t)kInjRing, left / (2 * (int64_t)gridDim.x)));
             } else {
                 if (taken >= n_static) break;
                 first = it0 + taken;

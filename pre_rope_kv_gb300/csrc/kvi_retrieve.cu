@@ -813,13 +813,14 @@ select_kernel(const __grid_constant__ SelectParams p)
         sm.n_cand = 0;
     }
 
-    // the request's own inputs can be read before the scoring kernel ends
+    // the request's own inputs (its store view, start and table length) can
+    // be read before the scoring kernel ends: only keys and lengths are its
     const int64_t start = (p.place && tid < 32) ? (int64_t)p.start_pos[r] : 0;
     const int32_t tl = (p.place && tid < 32) ? p.table_lens[r] : 0;
-    pdl_wait();  // keys and lengths of the scoring kernel
-    pdl_launch_dependents();
     const kvi_store_view st = load_store(p.store, r);
     const bool ok = !p.store.many || store_ok(st, p.g, p.max_facts, k);
+    pdl_wait();  // keys and lengths of the scoring kernel
+    pdl_launch_dependents();
     const int64_t N = ok ? st.n_facts : 0;
     const uint64_t *keys = p.keys + (int64_t)r * p.key_stride;
     const int32_t *lens = p.lens + (int64_t)r * p.key_stride;
