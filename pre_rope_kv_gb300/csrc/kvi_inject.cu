@@ -15,8 +15,13 @@
 //     fall in one page (ct divides the page size), for one layer and one of
 //     K/V, at most 8 KB; in the store and in the page a piece is one
 //     contiguous run of bytes.  Items (piece, K|V, layer), layer innermost,
-//     are handed out in chunks of 24 from a counter in the workspace (fused
-//     calls), or as one contiguous range per CTA (split calls);
+//     are handed out (fused calls) as one fixed first batch of 24 per CTA,
+//     then in claims from a counter in the workspace that shrink as the work
+//     runs out (guided self-scheduling), or (split calls) as one contiguous
+//     range per CTA;
+//   - small fused calls stage their requests' store views, block tables and
+//     per-fact rows, positions and piece prefixes in shared memory, so that
+//     resolving a piece takes no global round trip;
 //   - a producer warp resolves 32 items at a time (one per lane) and each
 //     lane moves its piece into its shared-memory stage (24 in all) with
 //     cp.async.bulk, completion tracked by the stage's "full" mbarrier, so up
@@ -61,6 +66,27 @@ struct PieceDesc {
     int16_t stop;    // 1: no more pieces for this consumer
 };
 
+// Small fused calls (at most kCacheReqs requests, kCacheFacts fact slots and
+// kCacheBlocks block-table entries) stage everything a piece's resolution
+// needs in shared memory once per CTA, so that the producer resolves pieces
+// without global round trips.
+constexpr int kCacheReqs = 16;
+constexpr int kCacheFacts = 272;   // R * (k + 1)
+constexpr int kCacheBlocks = 1024; // R * max_blocks
+
+struct ReqSlot {
+    const void *kv;
+    const int64_t *fact_start;
+    int64_t n_tokens;
+    int32_t table_len;
+};
+
+struct FactSlot {
+    int64_t row;  // the fact's first row in the store
+    int32_t pos;  // its first position in the prompt
+    int32_t len;  // its length (0: nothing to inject)
+};
+
 struct __align__(128) InjSmem {
     uint8_t stage[kInjRing][kPieceMax];
     uint64_t full[kInjRing];
@@ -68,7 +94,12 @@ struct __align__(128) InjSmem {
     PieceDesc desc[kInjRing];
     int32_t prefix[kMaxPrefix + 1];
     int32_t part[kInjThreads];
+    ReqSlot req[kCacheReqs];
+    FactSlot fact[kCacheFacts];
+    int32_t fpc[kCacheFacts];
+    int32_t btab[kCacheBlocks];
 };
+static_assert(sizeof(InjSmem) <= 227 * 1024, "inject shared memory");
 
 // ------------------------------------------------------ async-copy helpers
 
@@ -293,7 +324,80 @@ struct Piece {
     int32_t kv;
 };
 
-__device__ Piece resolve_piece(const InjectParams &p, const int32_t *prefix, int64_t it)
+// What a piece needs to know about its fact and request.
+struct FactRef {
+    int32_t m;       // piece index within the fact
+    int32_t len;     // fact length
+    int64_t pos;     // fact's first position
+    int64_t row;     // fact's first store row
+    const void *kv;
+    int64_t n_tokens;
+    const int32_t *bt;  // block table (global or shared memory)
+    int32_t tlen;
+};
+
+__device__ __forceinline__ FactRef fact_of_split(const InjectParams &p, const int32_t *prefix, int32_t piece)
+{
+    FactRef q;
+    const int j = search_le(prefix, p.n, piece);
+    q.m = piece - prefix[j];
+    const int32_t f = p.ids[j];
+    q.pos = p.pos[j];
+    const kvi_store_view &sv = p.store.single;
+    q.len = sv.fact_len[f];
+    q.row = sv.fact_start[f];
+    q.kv = sv.kv;
+    q.n_tokens = sv.n_tokens;
+    q.bt = p.block_tables;
+    q.tlen = p.table_len;
+    return q;
+}
+
+__device__ __forceinline__ FactRef fact_of_fused(const InjectParams &p, const int32_t *prefix, int32_t piece)
+{
+    FactRef q;
+    const int r = search_le(prefix, p.R, piece);
+    const int32_t local = piece - prefix[r];
+    const int32_t *pcr = p.pc + (int64_t)r * (p.k + 1);
+    const int j = search_le(pcr, p.k, local);
+    q.m = local - pcr[j];
+    const int32_t f = p.ids[(int64_t)r * p.k + j];
+    q.pos = p.pos[(int64_t)r * p.k + j];
+    q.len = p.slot_len[(int64_t)r * p.k + j];
+    const kvi_store_view *sv = p.store.many + r;
+    q.row = sv->fact_start[f];
+    q.kv = sv->kv;
+    q.n_tokens = sv->n_tokens;
+    q.bt = p.block_tables + (int64_t)r * p.max_blocks;
+    q.tlen = p.table_lens[r];
+    return q;
+}
+
+__device__ __forceinline__ FactRef fact_of_cached(const InjectParams &p, const InjSmem &sm, int32_t piece)
+{
+    FactRef q;
+    const int r = search_le(sm.prefix, p.R, piece);
+    const int32_t local = piece - sm.prefix[r];
+    const int32_t *pcr = sm.fpc + r * (p.k + 1);
+    const int j = search_le(pcr, p.k, local);
+    q.m = local - pcr[j];
+    const FactSlot &fs = sm.fact[r * p.k + j];
+    q.pos = fs.pos;
+    q.len = fs.len;
+    q.row = fs.row;
+    const ReqSlot &rq = sm.req[r];
+    q.kv = rq.kv;
+    q.n_tokens = rq.n_tokens;
+    q.bt = sm.btab + r * p.max_blocks;
+    q.tlen = rq.table_len;
+    return q;
+}
+
+// Source, destination and extent of item `it` = (piece, K|V, layer), layer
+// innermost; bytes = 0 (and the status set) when it falls outside the
+// block table, the pool or the RoPE table.
+__device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjSmem &sm, bool cached,
+                                               int64_t it)
 {
     Piece x{nullptr, nullptr, 0u, 0, 0, 0};
     const int L2 = 2 * p.L;
@@ -301,53 +405,29 @@ __device__ Piece resolve_piece(const InjectParams &p, const int32_t *prefix, int
     const int kl = (int)(it - piece * L2);
     const int kv = kl >= p.L ? 1 : 0;
     const int l = kl - kv * p.L;
-    int32_t f, m, len;
-    int64_t pos;
-    const int32_t *bt;
-    int32_t tlen;
-    const kvi_store_view *sv;
-    if (!p.fused) {
-        const int j = search_le(prefix, p.n, (int32_t)piece);
-        m = (int32_t)piece - prefix[j];
-        f = p.ids[j];
-        pos = p.pos[j];
-        sv = &p.store.single;
-        len = sv->fact_len[f];
-        bt = p.block_tables;
-        tlen = p.table_len;
-    } else {
-        const int r = search_le(prefix, p.R, (int32_t)piece);
-        const int32_t local = (int32_t)piece - prefix[r];
-        const int32_t *pcr = p.pc + (int64_t)r * (p.k + 1);
-        const int j = search_le(pcr, p.k, local);
-        m = local - pcr[j];
-        f = p.ids[(int64_t)r * p.k + j];
-        pos = p.pos[(int64_t)r * p.k + j];
-        len = p.slot_len[(int64_t)r * p.k + j];
-        sv = p.store.many + r;
-        bt = p.block_tables + (int64_t)r * p.max_blocks;
-        tlen = p.table_lens[r];
-    }
-    const int32_t mt = m / p.pg.units;
-    const int32_t hg = m - mt * p.pg.units;
-    const int64_t first = pos / p.pg.ct;
-    const int64_t a = max(pos, (first + mt) * p.pg.ct);
-    const int64_t b = min(pos + len, (first + mt + 1) * p.pg.ct);
+    const FactRef q = cached ? fact_of_cached(p, sm, (int32_t)piece)
+                      : p.fused ? fact_of_fused(p, sm.prefix, (int32_t)piece)
+                                : fact_of_split(p, sm.prefix, (int32_t)piece);
+    const int32_t mt = q.m / p.pg.units;
+    const int32_t hg = q.m - mt * p.pg.units;
+    const int64_t first = q.pos / p.pg.ct;
+    const int64_t a = max(q.pos, (first + mt) * p.pg.ct);
+    const int64_t b = min(q.pos + q.len, (first + mt + 1) * p.pg.ct);
     const int B = p.block_size;
-    if (a < 0 || b <= a || b > (int64_t)tlen * B || b > p.rope_positions) {
+    if (a < 0 || b <= a || b > (int64_t)q.tlen * B || b > p.rope_positions) {
         record_status(p.status, KVI_ERR_OUT_OF_RANGE);
         return x;
     }
-    const int32_t blk = bt[a / B];
+    const int32_t blk = q.bt[a / B];
     if (blk < 0 || blk >= p.num_blocks) {
         record_status(p.status, KVI_ERR_OUT_OF_RANGE);
         return x;
     }
     const int64_t HD = (int64_t)p.H * p.D;
     const int64_t hoff = (int64_t)hg * p.pg.hg * p.D;
-    const int64_t row = sv->fact_start[f] + (a - pos);
-    x.src = reinterpret_cast<const uint8_t *>(sv->kv) +
-            ((((int64_t)l * 2 + kv) * sv->n_tokens + row) * HD + hoff) * 2;
+    const int64_t row = q.row + (a - q.pos);
+    x.src = reinterpret_cast<const uint8_t *>(q.kv) +
+            ((((int64_t)l * 2 + kv) * q.n_tokens + row) * HD + hoff) * 2;
     x.dst = reinterpret_cast<uint8_t *>(p.layer_base[l]) +
             ((((int64_t)kv * p.num_blocks + blk) * B + (a % B)) * HD + hoff) * 2;
     x.ntok = (int32_t)(b - a);
@@ -405,11 +485,35 @@ inject_kernel(const __grid_constant__ InjectParams p)
         fence_async_smem();
     }
 
+    // small fused calls: the requests' inputs (store views, block tables,
+    // table lengths) are staged before the selection ends
+    const bool cached = p.fused && p.R <= kCacheReqs && p.R * (p.k + 1) <= kCacheFacts &&
+                        (int64_t)p.R * p.max_blocks <= kCacheBlocks;
+    if (cached) {
+        for (int i = tid; i < p.R * p.max_blocks; i += kInjThreads) sm.btab[i] = p.block_tables[i];
+        for (int r = tid; r < p.R; r += kInjThreads) {
+            const kvi_store_view &v = p.store.many[r];
+            sm.req[r] = ReqSlot{v.kv, v.fact_start, v.n_tokens, p.table_lens[r]};
+        }
+        __syncthreads();
+    }
+
     pdl_wait();  // selection and placement of the previous kernel
     int count;
     if (p.fused) {
         count = p.R;
         for (int r = tid; r < p.R; r += kInjThreads) sm.prefix[r + 1] = p.npc[r];
+        if (cached) {
+            for (int e = tid; e < p.R * (p.k + 1); e += kInjThreads) sm.fpc[e] = p.pc[e];
+            for (int e = tid; e < p.R * p.k; e += kInjThreads) {
+                const int r = e / p.k;
+                const int32_t len = p.slot_len[e];
+                // a slot with a positive length holds a fact id the selector
+                // checked against the store
+                const int64_t row = len > 0 ? sm.req[r].fact_start[p.ids[e]] : 0;
+                sm.fact[e] = FactSlot{row, p.pos[e], len};
+            }
+        }
     } else {
         count = p.n;
         const kvi_store_view &st = p.store.single;
@@ -436,12 +540,14 @@ inject_kernel(const __grid_constant__ InjectParams p)
     cta_prefix(sm.prefix, count, sm.part);
     const int64_t total = (int64_t)sm.prefix[count] * 2 * p.L;
     // static partition: a contiguous range of items per CTA (split calls);
-    // dynamic: producers claim chunks of up to kInjRing items from a shared
-    // counter (fused calls), which balances pieces of unequal size across SMs
+    // dynamic (fused calls): CTA c first takes items [24c, 24c + 24), then
+    // claims chunks of up to kInjRing items beyond the first 24 * grid from a
+    // shared counter, which balances pieces of unequal size across SMs
     const bool dynamic = p.work != nullptr;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t it0 = dynamic ? 0 : (int64_t)blockIdx.x * per;
     const int64_t n_static = total > it0 ? min(per, total - it0) : 0;
+    const int64_t dyn0 = min(total, (int64_t)gridDim.x * kInjRing);
 
     if (warp == kInjConsumers) {
         // producer warp: each lane resolves one of kInjRing consecutive items
@@ -451,32 +557,25 @@ inject_kernel(const __grid_constant__ InjectParams p)
         // share one
         static_assert(kInjRing <= 32, "one batch per warp");
         int64_t local = 0;   // items this CTA has staged
-        int64_t taken = 0;   // items of the static range taken
-        int want = kInjRing; // size of the next dynamic claim
+        int64_t first;
+        int nb;
+        int want = kInjRing;        // size of the claim in flight
+        unsigned long long claim = 0;  // lane 0: the claim in flight
+        if (dynamic) {
+            first = (int64_t)blockIdx.x * kInjRing;
+            nb = (int)max((int64_t)0, min((int64_t)kInjRing, dyn0 - first));
+            // the next claim goes out now; its latency overlaps this batch
+            if (lane == 0) claim = atomicAdd(p.work, (unsigned long long)want);
+        } else {
+            first = it0;
+            nb = (int)min((int64_t)kInjRing, n_static);
+        }
+        int64_t taken = nb;  // items of the static range taken
         bool ok = true;
         for (;;) {
-            int64_t first;
-            int nb;
-            if (dynamic) {
-                unsigned long long got = 0;
-                if (lane == 0) got = atomicAdd(p.work, (unsigned long long)want);
-                first = (int64_t)__shfl_sync(0xffffffffu, got, 0);
-                if (first >= total) break;
-                nb = (int)min((int64_t)want, total - first);
-                // guided self-scheduling: once fewer than two full claims per
-                // CTA are left, claim a share of what is left (at least 2),
-                // so that the CTAs run out of work at nearly the same time
-                const int64_t left = total - first - nb;
-                want = (int)max((int64_t)2, min((int64_t)kInjRing, left / (2 * (int64_t)gridDim.x)));
-            } else {
-                if (taken >= n_static) break;
-                first = it0 + taken;
-                nb = (int)min((int64_t)kInjRing, n_static - taken);
-                taken += nb;
-            }
             const int64_t j = local + lane;
             if (lane < nb) {
-                const Piece x = resolve_piece(p, sm.prefix, first + lane);
+                const Piece x = resolve_piece(p, sm, cached, first + lane);
                 const int s = (int)(j % kInjRing);
                 const int64_t round = j / kInjRing;
                 if (round > 0 &&
@@ -497,6 +596,22 @@ inject_kernel(const __grid_constant__ InjectParams p)
             }
             local += nb;
             if (!__all_sync(0xffffffffu, ok)) break;
+            if (dynamic) {
+                first = dyn0 + (int64_t)__shfl_sync(0xffffffffu, claim, 0);
+                if (first >= total) break;
+                nb = (int)min((int64_t)want, total - first);
+                // guided self-scheduling: once fewer than two full claims per
+                // CTA are left, claim a share of what is left (at least 2),
+                // so that the CTAs run out of work at nearly the same time
+                const int64_t left = total - first - nb;
+                want = (int)max((int64_t)2, min((int64_t)kInjRing, left / (2 * (int64_t)gridDim.x)));
+                if (lane == 0) claim = atomicAdd(p.work, (unsigned long long)want);
+            } else {
+                if (taken >= n_static) break;
+                first = it0 + taken;
+                nb = (int)min((int64_t)kInjRing, n_static - taken);
+                taken += nb;
+            }
         }
         // one stop descriptor for each consumer's next item
         if (ok && lane < kInjConsumers) {

@@ -17,12 +17,17 @@
 //                  float32 pair) and the pair becomes an exact 64-bit
 //                  selection key with integer ordering only (no float64).
 //                  The same warp validates the fact's extent in the store.
-//   select_kernel  one CTA per request: a shared-memory histogram of the keys'
-//                  float32 parts (a monotone map) finds the bucket that
-//                  holds the k-th key; buckets above it are taken whole, the
-//                  k-th bucket's keys are ranked exactly (or, when it is
-//                  crowded, refined by an 8-bit radix select on the full
-//                  64-bit key down to ties, which go to the lower fact id).
+//   select_kernel  one CTA per request.  First a lower bound on the k-th
+//                  key's top 16 bits is found from the best keys of 256
+//                  disjoint key groups (one warp, binary search); the keys
+//                  at or above it (usually little more than k) are ranked
+//                  exactly.  When too many keys tie at that bound, a
+//                  shared-memory histogram of the keys' float32 parts (a
+//                  monotone map) finds the bucket that holds the k-th key;
+//                  buckets above it are taken whole, the k-th bucket's keys
+//                  are ranked exactly (or, when it is crowded, refined by an
+//                  8-bit radix select on the full 64-bit key down to ties,
+//                  which go to the lower fact id).
 //                  In the fused path it also places the facts (rank order,
 //                  back to back from the request's start) and cuts them into
 //                  the inject kernel's pieces.
@@ -790,13 +795,138 @@ __device__ __forceinline__ void place_request(const SelectParams &p, SelectSmem 
     }
 }
 
+// Selection by histogram (the general path): a shared-memory histogram of
+// the keys' float32 parts finds the bucket that holds the k-th key; buckets
+// above it are taken whole and the k-th bucket's keys are ranked exactly or,
+// when it is crowded, refined by radix selection.  Keys stream from L2.  On
+// return sm.out_* hold the k best in rank order.  Kept out of line: it runs
+// only when many keys tie, and the common path's code stays contiguous.
+__device__ __noinline__ void select_by_histogram(SelectSmem &sm, const uint64_t *keys,
+                                                 const int32_t *lens, int64_t N, int32_t k)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // 1. histogram of the first-level buckets (hist is zero on entry)
+#pragma unroll 4
+    for (int64_t i = tid; i < N; i += kSelectThreads) atomicAdd(&sm.hist[bucket_of(__ldcg(keys + i))], 1u);
+    __syncthreads();
+    // 2. the bucket holding the k-th key (bucket 4095 is the best);
+    //    thread t owns buckets 4095-4t .. 4092-4t.
+    const int top = kHistBins - 1 - 4 * tid;
+    const uint32_t c0 = sm.hist[top], c1 = sm.hist[top - 1];
+    const uint32_t c2 = sm.hist[top - 2], c3 = sm.hist[top - 3];
+    const uint32_t incl = block_incl_scan<uint32_t>(c0 + c1 + c2 + c3, sm.warp_tot);
+    const uint32_t excl = incl - (c0 + c1 + c2 + c3);
+    if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+        const uint32_t cs[4] = {c0, c1, c2, c3};
+        uint32_t run = excl;
+        for (int j = 0; j < 4; ++j) {
+            if (run + cs[j] >= (uint32_t)k) {
+                sm.bucket = (uint32_t)(top - j);
+                sm.above = run;
+                sm.pop = cs[j];
+                break;
+            }
+            run += cs[j];
+        }
+    }
+    __syncthreads();
+    const uint32_t b0 = sm.bucket;
+    const uint32_t above = sm.above;
+    const uint32_t M = sm.pop;
+    const uint32_t need = (uint32_t)k - above;
+
+    // 3. keys above the bucket are in; keys in it are candidates.
+    const bool direct = M <= (uint32_t)kCandCap;
+#pragma unroll 4
+    for (int64_t i = tid; i < N; i += kSelectThreads) {
+        const uint64_t key = __ldcg(keys + i);
+        const uint32_t b = bucket_of(key);
+        if (b > b0) add_sure(sm, key, (int32_t)i, __ldcg(lens + i));
+        else if (b == b0 && direct) add_cand(sm, key, (int32_t)i, __ldcg(lens + i));
+    }
+    __syncthreads();
+    if (direct) {
+        // 4. the k selected keys in rank order, in one pass: every key above
+        //    the bucket is better than every key in it, so the former are
+        //    ranked among themselves (ranks 0 .. above-1) and the bucket's
+        //    keys among themselves (from rank `above`)
+        for (uint32_t e = warp; e < above + M; e += kSelectThreads / 32) {
+            if (e < above) {
+                const uint64_t ke = sm.sure_key[e];
+                const int32_t ie = sm.sure_id[e];
+                const uint32_t rank = warp_rank(sm.sure_key, sm.sure_id, above, ke, ie, lane);
+                if (lane == 0 && rank < above) {
+                    sm.out_key[rank] = ke;
+                    sm.out_id[rank] = ie;
+                    sm.out_len[rank] = sm.sure_len[e];
+                }
+            } else {
+                const uint32_t c = e - above;
+                const uint64_t kc = sm.cand_key[c];
+                const int32_t ic = sm.cand_id[c];
+                const uint32_t rank = warp_rank(sm.cand_key, sm.cand_id, M, kc, ic, lane);
+                if (lane == 0 && rank < need) {
+                    sm.out_key[above + rank] = kc;
+                    sm.out_id[above + rank] = ic;
+                    sm.out_len[above + rank] = sm.cand_len[c];
+                }
+            }
+        }
+    } else {
+        select_crowded(sm, keys, lens, N, b0, need);
+        __syncthreads();
+        // 4. the k selected keys in rank order.
+        for (int e = warp; e < k; e += kSelectThreads / 32) {
+            const uint64_t ke = sm.sure_key[e];
+            const int32_t ie = sm.sure_id[e];
+            const uint32_t rank = warp_rank(sm.sure_key, sm.sure_id, (uint32_t)k, ke, ie, lane);
+            if (lane == 0 && rank < (uint32_t)KVI_MAX_K) {
+                sm.out_key[rank] = ke;
+                sm.out_id[rank] = ie;
+                sm.out_len[rank] = sm.sure_len[e];
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Touch the first facts the inject kernel will move -- the best-ranked ones,
+// every layer's K and V rows -- with one 128-byte L2 prefetch each, which
+// warms their address translations.  Warps 1.. of the selecting CTA, while
+// warp 0 places the request.
+constexpr int kWarmFacts = 8;
+constexpr int kSelectGroups = 256;
+
+__device__ __forceinline__ void warm_first_facts(const SelectParams &p, const SelectSmem &sm,
+                                                 const kvi_store_view &st, int32_t k)
+{
+    const int t = threadIdx.x - 32;
+    const int L = p.g.layers;
+    const int64_t row_bytes = (int64_t)p.g.kv_heads * p.g.head_dim * 2;
+    const int nf = min(k, kWarmFacts);
+    for (int e = t; e < nf * 2 * L; e += kSelectThreads - 32) {
+        const int j = e / (2 * L);
+        const int plane = e - j * 2 * L;  // layer * 2 + (K|V)
+        const int32_t len = sm.out_len[j];
+        const int32_t f = sm.out_id[j];
+        // lengths are -1 unless the scoring kernel found the extent inside
+        // the store
+        if (len <= 0 || f < 0) continue;
+        const int64_t s0 = __ldg(st.fact_start + f);
+        if (s0 < 0 || s0 + len > st.n_tokens) continue;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(st.kv) +
+                             ((int64_t)plane * st.n_tokens + s0) * row_bytes;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 128;" ::"l"(src) : "memory");
+    }
+}
+
 __global__ void __launch_bounds__(kSelectThreads, 1)
 select_kernel(const __grid_constant__ SelectParams p)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     SelectSmem &sm = *reinterpret_cast<SelectSmem *>(smem_raw);
     const int r = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t k = p.k;
 
     for (int b = tid; b < kHistBins; b += kSelectThreads) sm.hist[b] = 0;
@@ -826,11 +956,10 @@ select_kernel(const __grid_constant__ SelectParams p)
     const int32_t *lens = p.lens + (int64_t)r * p.key_stride;
     // up to kSelectThreads * kKeysPerThread keys (and their lengths) are read
     // once, in one round trip, and kept in registers; larger stores stream
-    // them from L2 twice
+    // them from L2
     const bool in_regs = N <= (int64_t)kSelectThreads * kKeysPerThread;
     uint64_t kr[kKeysPerThread];
     int32_t lr[kKeysPerThread];
-    uint32_t br[kKeysPerThread];
     if (in_regs) {
 #pragma unroll
         for (int m = 0; m < kKeysPerThread; ++m) {
@@ -839,97 +968,131 @@ select_kernel(const __grid_constant__ SelectParams p)
             lr[m] = i < N ? __ldcg(lens + i) : -1;
         }
     }
-    __syncthreads();
 
+    // Fast path.  The top 16 bits of a key, h, are monotone in it.  The keys
+    // are split into 256 disjoint groups (4 threads' keys each).  Let t* be
+    // the largest t such that at least k groups hold a key with h >= t: then
+    // at least k keys have h >= t*, and any key with h < t* has k keys above
+    // it, so the top k all have h >= t*.  The groups' largest h go to shared
+    // memory and one warp finds t* by a binary search (16 steps, no block
+    // barriers); the keys with h >= t* are collected (typically little more
+    // than k) and ranked exactly.  If more than kCandCap keys qualify (heavy
+    // ties), select_by_histogram runs instead.
+    bool fast = false;
     if (ok) {
-        // 1. histogram of the first-level buckets
+        uint32_t mt = 0;  // this thread's largest h (0 also when it has no key)
+        static_assert(kSelectThreads / 4 == kSelectGroups, "groups of 4 threads");
         if (in_regs) {
 #pragma unroll
-            for (int m = 0; m < kKeysPerThread; ++m) {
-                br[m] = bucket_of(kr[m]);
-                if (tid + (int64_t)m * kSelectThreads < N) atomicAdd(&sm.hist[br[m]], 1u);
-            }
+            for (int m = 0; m < kKeysPerThread; ++m)
+                if (tid + (int64_t)m * kSelectThreads < N) mt = max(mt, (uint32_t)(kr[m] >> 48));
         } else {
-#pragma unroll 4
+            for (int64_t i = tid; i < N; i += kSelectThreads) mt = max(mt, (uint32_t)(__ldcg(keys + i) >> 48));
+        }
+        // groups of 4 threads (256 groups): group g = threads 4g .. 4g+3
+        mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        if ((lane & 3) == 0) sm.hist[tid >> 2] = mt;
+        __syncthreads();
+        if (warp == 0) {
+            // t = 0 always qualifies here: with fewer than k groups holding
+            // keys it stays 0 and every key becomes a candidate
+            uint32_t v[kSelectGroups / 32];
+#pragma unroll
+            for (int i = 0; i < kSelectGroups / 32; ++i) v[i] = sm.hist[i * 32 + lane];
+            uint32_t lo = 0, hi = 1u << 16;
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) >> 1;
+                uint32_t c = 0;
+#pragma unroll
+                for (int i = 0; i < kSelectGroups / 32; ++i) c += v[i] >= mid ? 1u : 0u;
+                if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)k) lo = mid;
+                else hi = mid;
+            }
+            if (lane == 0) sm.bucket = lo;
+        }
+        __syncthreads();
+        const uint32_t lo = sm.bucket;
+        // this thread's qualifying keys go to one warp-aggregated slot range
+        uint32_t cnt = 0;
+        if (in_regs) {
+#pragma unroll
+            for (int m = 0; m < kKeysPerThread; ++m)
+                cnt += (tid + (int64_t)m * kSelectThreads < N && (uint32_t)(kr[m] >> 48) >= lo) ? 1u : 0u;
+        } else {
             for (int64_t i = tid; i < N; i += kSelectThreads)
-                atomicAdd(&sm.hist[bucket_of(__ldcg(keys + i))], 1u);
+                cnt += ((uint32_t)(__ldcg(keys + i) >> 48) >= lo) ? 1u : 0u;
         }
-        __syncthreads();
-        // 2. the bucket holding the k-th key (bucket 4095 is the best);
-        //    thread t owns buckets 4095-4t .. 4092-4t.
-        const int top = kHistBins - 1 - 4 * tid;
-        const uint32_t c0 = sm.hist[top], c1 = sm.hist[top - 1];
-        const uint32_t c2 = sm.hist[top - 2], c3 = sm.hist[top - 3];
-        const uint32_t incl = block_incl_scan<uint32_t>(c0 + c1 + c2 + c3, sm.warp_tot);
-        const uint32_t excl = incl - (c0 + c1 + c2 + c3);
-        if (excl < (uint32_t)k && incl >= (uint32_t)k) {
-            const uint32_t cs[4] = {c0, c1, c2, c3};
-            uint32_t run = excl;
-            for (int j = 0; j < 4; ++j) {
-                if (run + cs[j] >= (uint32_t)k) {
-                    sm.bucket = (uint32_t)(top - j);
-                    sm.above = run;
-                    sm.pop = cs[j];
-                    break;
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t base = 0;
+        if (lane == 31 && incl) base = atomicAdd(&sm.n_cand, incl);
+        uint32_t at = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+        if (cnt) {
+            if (in_regs) {
+#pragma unroll
+                for (int m = 0; m < kKeysPerThread; ++m) {
+                    const int64_t i = tid + (int64_t)m * kSelectThreads;
+                    if (i < N && (uint32_t)(kr[m] >> 48) >= lo) {
+                        if (at < (uint32_t)kCandCap) {
+                            sm.cand_key[at] = kr[m];
+                            sm.cand_id[at] = (int32_t)i;
+                            sm.cand_len[at] = lr[m];
+                        }
+                        ++at;
+                    }
                 }
-                run += cs[j];
+            } else {
+                for (int64_t i = tid; i < N; i += kSelectThreads) {
+                    const uint64_t key = __ldcg(keys + i);
+                    if ((uint32_t)(key >> 48) >= lo) {
+                        if (at < (uint32_t)kCandCap) {
+                            sm.cand_key[at] = key;
+                            sm.cand_id[at] = (int32_t)i;
+                            sm.cand_len[at] = __ldcg(lens + i);
+                        }
+                        ++at;
+                    }
+                }
             }
         }
         __syncthreads();
-        const uint32_t b0 = sm.bucket;
-        const uint32_t above = sm.above;
-        const uint32_t M = sm.pop;
-        const uint32_t need = (uint32_t)k - above;
-
-        // 3. keys above the bucket are in; keys in it are candidates.
-        const bool direct = M <= (uint32_t)kCandCap;
-        if (in_regs) {
-#pragma unroll
-            for (int m = 0; m < kKeysPerThread; ++m) {
-                const int64_t i = tid + (int64_t)m * kSelectThreads;
-                if (i >= N) continue;
-                const uint32_t b = br[m];
-                if (b > b0) add_sure(sm, kr[m], (int32_t)i, lr[m]);
-                else if (b == b0 && direct) add_cand(sm, kr[m], (int32_t)i, lr[m]);
+        const uint32_t C = sm.n_cand;
+        fast = C <= (uint32_t)kCandCap;
+        if (fast) {
+            for (uint32_t c = warp; c < C; c += kSelectThreads / 32) {
+                const uint64_t kc = sm.cand_key[c];
+                const int32_t ic = sm.cand_id[c];
+                const uint32_t rank = warp_rank(sm.cand_key, sm.cand_id, C, kc, ic, lane);
+                if (lane == 0 && rank < (uint32_t)k) {
+                    sm.out_key[rank] = kc;
+                    sm.out_id[rank] = ic;
+                    sm.out_len[rank] = sm.cand_len[c];
+                }
             }
         } else {
-#pragma unroll 4
-            for (int64_t i = tid; i < N; i += kSelectThreads) {
-                const uint64_t key = __ldcg(keys + i);
-                const uint32_t b = bucket_of(key);
-                if (b > b0) add_sure(sm, key, (int32_t)i, __ldcg(lens + i));
-                else if (b == b0 && direct) add_cand(sm, key, (int32_t)i, __ldcg(lens + i));
-            }
-        }
-        __syncthreads();
-        if (direct) take_best_candidates(sm, M, need, above);
-        else select_crowded(sm, keys, lens, N, b0, need);
-        __syncthreads();
-
-        // 4. the k selected keys in rank order.
-        {
-            const int lane = tid & 31, warp = tid >> 5;
-            for (int e = warp; e < k; e += kSelectThreads / 32) {
-                const uint64_t ke = sm.sure_key[e];
-                const int32_t ie = sm.sure_id[e];
-                const uint32_t rank = warp_rank(sm.sure_key, sm.sure_id, (uint32_t)k, ke, ie, lane);
-                if (lane == 0 && rank < (uint32_t)KVI_MAX_K) {
-                    sm.out_key[rank] = ke;
-                    sm.out_id[rank] = ie;
-                    sm.out_len[rank] = sm.sure_len[e];
-                }
-            }
+            // the fallback starts from a zero histogram and empty lists
+            for (int b = tid; b < kHistBins; b += kSelectThreads) sm.hist[b] = 0;
+            if (tid == 0) sm.n_cand = 0;
         }
         __syncthreads();
     }
+    if (ok && !fast) select_by_histogram(sm, keys, lens, N, k);
 
     for (int j = tid; j < k; j += kSelectThreads) {
         p.ids[(int64_t)r * k + j] = ok ? sm.out_id[j] : -1;
         p.scores[(int64_t)r * k + j] =
             ok ? key_score(sm.out_key[j]) : __int_as_float(0x7fc00000);
     }
-    if (p.place && tid < 32) place_request(p, sm, r, ok, st, start, tl);
-    if (p.place && r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
+    if (p.place) {
+        if (tid < 32) place_request(p, sm, r, ok, st, start, tl);
+        else if (ok) warm_first_facts(p, sm, st, k);
+        if (r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
+    }
 }
 
 // ---------------------------------------------------------------- placement

@@ -58,6 +58,24 @@ def test_multi_request_ragged_full_pool():
     fused_and_check(b)
 
 
+@pytest.mark.parametrize("R,k,B", [(8, 40, 16), (16, 15, 16), (17, 12, 16), (1, 37, 1), (2, 30, 4)])
+def test_fused_staging_limits(R, k, B):
+    # small fused calls stage their facts and block tables in shared memory;
+    # these straddle the limits (request count, fact slots, table entries) so
+    # that both the staged and the global resolution run
+    w = W(requests=R, n_facts=300, k=k, block_size=B, layers=2, kv_heads=2, head_dim=64,
+          seed=300 + R + k + B)
+    fused_and_check(synth.build_workload(w))
+
+
+def test_selection_streams_large_store():
+    # more keys than the selector keeps in registers: both of its passes
+    # stream the keys from L2
+    w = W(n_facts=15000, k=50, layers=1, kv_heads=1, head_dim=64, embed_dim=64, len_hi=8,
+          seed=311)
+    fused_and_check(synth.build_workload(w))
+
+
 @pytest.mark.parametrize("D,H,E,L", [(16, 1, 100, 1), (64, 3, 384, 2), (256, 2, 1536, 9),
                                      (128, 8, 1024, 4), (32, 5, 4, 3), (512, 1, 132, 2)])
 def test_geometries(D, H, E, L):
