@@ -130,7 +130,7 @@ def profile_traffic():
     vals = {}
     for line in open(PROFILE):
         if ":" in line and line.startswith("- "):
-            key, _, v = line[2:].partition(":")
+            key, _, v = line[2:].rpartition(":")  # keys may hold a colon
             vals[key.strip()] = v.strip().strip("`")
     if vals.get("kvi_inject.cu sha256[:16]") != digest:
         return None
