@@ -276,6 +276,7 @@ WsLayout ws_layout(int32_t R, int64_t max_facts, int32_t k)
     w.slot_len = at; at = up(at + (size_t)R * (size_t)k * 4);
     w.pc = at;       at = up(at + (size_t)R * (size_t)(k + 1) * 4);
     w.npc = at;      at = up(at + (size_t)R * 4);
+    w.rows = at;     at = up(at + (size_t)R * (size_t)k * 8);
     w.work = at;     at = up(at + 8);
     w.total = at;
     return w;
@@ -546,6 +547,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     lp.slot_len = reinterpret_cast<int32_t *>(ws + w.slot_len);
     lp.pc = reinterpret_cast<int32_t *>(ws + w.pc);
     lp.npc = reinterpret_cast<int32_t *>(ws + w.npc);
+    lp.rows = reinterpret_cast<int64_t *>(ws + w.rows);
     lp.work = reinterpret_cast<unsigned long long *>(ws + w.work);
     lp.status = d_status;
     KVI_CUDA(launch_select(lp, s, true));
@@ -565,6 +567,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     ip.slot_len = lp.slot_len;
     ip.pc = lp.pc;
     ip.npc = lp.npc;
+    ip.rows = lp.rows;
     ip.work = lp.work;
     ip.block_tables = d_block_tables;
     ip.table_lens = d_table_lens;

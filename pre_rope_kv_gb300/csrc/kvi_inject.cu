@@ -20,8 +20,8 @@
 //     runs out (guided self-scheduling), or (split calls) as one contiguous
 //     range per CTA;
 //   - small fused calls stage their requests' store views, block tables and
-//     per-fact rows, positions and piece prefixes in shared memory, so that
-//     resolving a piece takes no global round trip;
+//     per-fact rows (written by the selector), positions and piece prefixes
+//     in shared memory, so that resolving a piece takes no global round trip;
 //   - a producer warp resolves 32 items at a time (one per lane) and each
 //     lane moves its piece into its shared-memory stage (24 in all) with
 //     cp.async.bulk, completion tracked by the stage's "full" mbarrier, so up
@@ -76,7 +76,6 @@ constexpr int kCacheBlocks = 1024; // R * max_blocks
 
 struct ReqSlot {
     const void *kv;
-    const int64_t *fact_start;
     int64_t n_tokens;
     int32_t table_len;
 };
@@ -361,11 +360,10 @@ __device__ __forceinline__ FactRef fact_of_fused(const InjectParams &p, const in
     const int32_t *pcr = p.pc + (int64_t)r * (p.k + 1);
     const int j = search_le(pcr, p.k, local);
     q.m = local - pcr[j];
-    const int32_t f = p.ids[(int64_t)r * p.k + j];
     q.pos = p.pos[(int64_t)r * p.k + j];
     q.len = p.slot_len[(int64_t)r * p.k + j];
+    q.row = p.rows[(int64_t)r * p.k + j];
     const kvi_store_view *sv = p.store.many + r;
-    q.row = sv->fact_start[f];
     q.kv = sv->kv;
     q.n_tokens = sv->n_tokens;
     q.bt = p.block_tables + (int64_t)r * p.max_blocks;
@@ -493,7 +491,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
         for (int i = tid; i < p.R * p.max_blocks; i += kInjThreads) sm.btab[i] = p.block_tables[i];
         for (int r = tid; r < p.R; r += kInjThreads) {
             const kvi_store_view &v = p.store.many[r];
-            sm.req[r] = ReqSlot{v.kv, v.fact_start, v.n_tokens, p.table_lens[r]};
+            sm.req[r] = ReqSlot{v.kv, v.n_tokens, p.table_lens[r]};
         }
         __syncthreads();
     }
@@ -506,12 +504,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
         if (cached) {
             for (int e = tid; e < p.R * (p.k + 1); e += kInjThreads) sm.fpc[e] = p.pc[e];
             for (int e = tid; e < p.R * p.k; e += kInjThreads) {
-                const int r = e / p.k;
-                const int32_t len = p.slot_len[e];
-                // a slot with a positive length holds a fact id the selector
-                // checked against the store
-                const int64_t row = len > 0 ? sm.req[r].fact_start[p.ids[e]] : 0;
-                sm.fact[e] = FactSlot{row, p.pos[e], len};
+                sm.fact[e] = FactSlot{p.rows[e], p.pos[e], p.slot_len[e]};
             }
         }
     } else {
@@ -536,8 +529,9 @@ inject_kernel(const __grid_constant__ InjectParams p)
             sm.prefix[j + 1] = pieces;
         }
     }
+    if (tid == 0) sm.prefix[0] = 0;
     __syncthreads();
-    cta_prefix(sm.prefix, count, sm.part);
+    if (count > 1) cta_prefix(sm.prefix, count, sm.part);  // one request: [0, npc] already
     const int64_t total = (int64_t)sm.prefix[count] * 2 * p.L;
     // static partition: a contiguous range of items per CTA (split calls);
     // dynamic (fused calls): CTA c first takes items [24c, 24c + 24), then

@@ -40,6 +40,7 @@ struct WsLayout {
     size_t slot_len;  // int32  [R][k] length of each selected fact
     size_t pc;        // int32  [R][k + 1] piece prefix of the selected facts
     size_t npc;       // int32  [R] pieces of each request (0: nothing to inject)
+    size_t rows;      // int64  [R][k] first store row of each selected fact
     size_t work;      // uint64 [1] next inject item to hand out (zeroed by select)
     size_t total;
     int64_t key_stride;
@@ -88,6 +89,7 @@ struct SelectParams {
     int32_t *slot_len;          // [R][k]
     int32_t *pc;                // [R][k + 1]
     int32_t *npc;               // [R]
+    int64_t *rows;              // [R][k] first store row of each selected fact
     unsigned long long *work;   // inject work counter, zeroed here
     int32_t *status;
 };
@@ -113,6 +115,7 @@ struct InjectParams {
     const int32_t *slot_len;   // fused [R][k]
     const int32_t *pc;         // fused [R][k + 1]
     const int32_t *npc;        // fused [R]
+    const int64_t *rows;       // fused [R][k] first store row of each fact
     unsigned long long *work;  // fused: shared item counter (dynamic balance); split: null
     const int32_t *block_tables;  // split [table_len], fused [R][max_blocks]
     const int32_t *table_lens;    // fused [R]

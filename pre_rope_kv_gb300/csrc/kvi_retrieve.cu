@@ -890,28 +890,35 @@ __device__ __noinline__ void select_by_histogram(SelectSmem &sm, const uint64_t 
     __syncthreads();
 }
 
-// Touch the first facts the inject kernel will move -- the best-ranked ones,
-// every layer's K and V rows -- with one 128-byte L2 prefetch each, which
-// warms their address translations.  Warps 1.. of the selecting CTA, while
-// warp 0 places the request.
+// Warps 1.. of the selecting CTA, while warp 0 places the request: write
+// the first store row of every selected fact for the inject kernel (so that
+// it needs no dependent load of fact_start), and touch the first facts it
+// will move -- the best-ranked ones, every layer's K and V rows -- with one
+// 128-byte L2 prefetch each, which warms their address translations.
 constexpr int kWarmFacts = 8;
 constexpr int kSelectGroups = 256;
 
-__device__ __forceinline__ void warm_first_facts(const SelectParams &p, const SelectSmem &sm,
-                                                 const kvi_store_view &st, int32_t k)
+__device__ __forceinline__ void fact_rows(const SelectParams &p, const SelectSmem &sm,
+                                          const kvi_store_view &st, int r, int32_t k)
 {
     const int t = threadIdx.x - 32;
     const int L = p.g.layers;
     const int64_t row_bytes = (int64_t)p.g.kv_heads * p.g.head_dim * 2;
+    // lengths are -1 unless the scoring kernel found the extent inside the
+    // store; only such facts have a row (the others inject nothing)
+    for (int j = t; j < k; j += kSelectThreads - 32) {
+        const int32_t f = sm.out_id[j];
+        int64_t s0 = 0;
+        if (sm.out_len[j] > 0 && f >= 0 && (int64_t)f < st.n_facts) s0 = __ldg(st.fact_start + f);
+        p.rows[(int64_t)r * k + j] = s0;
+    }
     const int nf = min(k, kWarmFacts);
     for (int e = t; e < nf * 2 * L; e += kSelectThreads - 32) {
         const int j = e / (2 * L);
         const int plane = e - j * 2 * L;  // layer * 2 + (K|V)
         const int32_t len = sm.out_len[j];
         const int32_t f = sm.out_id[j];
-        // lengths are -1 unless the scoring kernel found the extent inside
-        // the store
-        if (len <= 0 || f < 0) continue;
+        if (len <= 0 || f < 0 || (int64_t)f >= st.n_facts) continue;
         const int64_t s0 = __ldg(st.fact_start + f);
         if (s0 < 0 || s0 + len > st.n_tokens) continue;
         const uint8_t *src = reinterpret_cast<const uint8_t *>(st.kv) +
@@ -1090,7 +1097,7 @@ select_kernel(const __grid_constant__ SelectParams p)
     }
     if (p.place) {
         if (tid < 32) place_request(p, sm, r, ok, st, start, tl);
-        else if (ok) warm_first_facts(p, sm, st, k);
+        else if (ok) fact_rows(p, sm, st, r, k);
         if (r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
     }
 }
