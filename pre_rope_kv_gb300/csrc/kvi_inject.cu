@@ -399,8 +399,16 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
 {
     Piece x{nullptr, nullptr, 0u, 0, 0, 0};
     const int L2 = 2 * p.L;
-    const int64_t piece = it / L2;
-    const int kl = (int)(it - piece * L2);
+    int64_t piece;
+    int kl;
+    if (it <= 0x7fffffff) {  // 32-bit division whenever the index allows it
+        const uint32_t pu = (uint32_t)it / (uint32_t)L2;
+        piece = pu;
+        kl = (int)((uint32_t)it - pu * (uint32_t)L2);
+    } else {
+        piece = it / L2;
+        kl = (int)(it - piece * L2);
+    }
     const int kv = kl >= p.L ? 1 : 0;
     const int l = kl - kv * p.L;
     const FactRef q = cached ? fact_of_cached(p, sm, (int32_t)piece)
@@ -408,7 +416,9 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
                                 : fact_of_split(p, sm.prefix, (int32_t)piece);
     const int32_t mt = q.m / p.pg.units;
     const int32_t hg = q.m - mt * p.pg.units;
-    const int64_t first = q.pos / p.pg.ct;
+    // positions are non-negative int32 here: a fact that could be placed at
+    // a negative or 64-bit position has no pieces
+    const int64_t first = (uint32_t)q.pos / (uint32_t)p.pg.ct;
     const int64_t a = max(q.pos, (first + mt) * p.pg.ct);
     const int64_t b = min(q.pos + q.len, (first + mt + 1) * p.pg.ct);
     const int B = p.block_size;
@@ -416,7 +426,9 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
         record_status(p.status, KVI_ERR_OUT_OF_RANGE);
         return x;
     }
-    const int32_t blk = q.bt[a / B];
+    const uint32_t au = (uint32_t)a;  // 0 <= a < b <= rope_positions < 2^31
+    const uint32_t page = au / (uint32_t)B;
+    const int32_t blk = q.bt[page];
     if (blk < 0 || blk >= p.num_blocks) {
         record_status(p.status, KVI_ERR_OUT_OF_RANGE);
         return x;
@@ -427,7 +439,7 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
     x.src = reinterpret_cast<const uint8_t *>(q.kv) +
             ((((int64_t)l * 2 + kv) * q.n_tokens + row) * HD + hoff) * 2;
     x.dst = reinterpret_cast<uint8_t *>(p.layer_base[l]) +
-            ((((int64_t)kv * p.num_blocks + blk) * B + (a % B)) * HD + hoff) * 2;
+            ((((int64_t)kv * p.num_blocks + blk) * B + (au - page * (uint32_t)B)) * HD + hoff) * 2;
     x.ntok = (int32_t)(b - a);
     x.bytes = (uint32_t)(x.ntok * p.pg.hg * p.D * 2);
     x.pos0 = (int32_t)a;
@@ -538,7 +550,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
     // claims chunks of up to kInjRing items beyond the first 24 * grid from a
     // shared counter, which balances pieces of unequal size across SMs
     const bool dynamic = p.work != nullptr;
-    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t per = dynamic ? 0 : (total + gridDim.x - 1) / gridDim.x;
     const int64_t it0 = dynamic ? 0 : (int64_t)blockIdx.x * per;
     const int64_t n_static = total > it0 ? min(per, total - it0) : 0;
     const int64_t dyn0 = min(total, (int64_t)gridDim.x * kInjRing);
@@ -580,7 +592,9 @@ inject_kernel(const __grid_constant__ InjectParams p)
                     sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
                     const uint32_t fb = smem_u32(&sm.full[s]);
                     if (x.bytes) {
-                        fence_async_smem();
+                        // the stage's previous contents were read by the
+                        // consumers (generic proxy) before this async write
+                        if (round > 0) fence_async_smem();
                         mbar_expect_tx(fb, x.bytes);
                         bulk_load(smem_u32(sm.stage[s]), x.src, x.bytes, fb);
                     } else {
