@@ -28,6 +28,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libkvi_oracle.so")
 
 OK, BAD_ARG, OUT_OF_RANGE, CAPACITY = 0, 1, 2, 3
+PAIR_HALF, PAIR_INTERLEAVED = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +82,18 @@ def _load():
         lib.kvo_request.argtypes = [
             P, P, i64, i64, i32, P, i32, i32, i32, i64, P, P, i64, f64, P, P, P, P, i64]
         lib.kvo_request.restype = i64
+        lib.kvo_rotate_pairs.argtypes = [P, i32, P, i32, f64, P]
+        lib.kvo_rotate_pairs.restype = None
+        lib.kvo_rotate_cs.argtypes = [P, i32, P, P, i32, P]
+        lib.kvo_rotate_cs.restype = None
+        lib.kvo_rope_omega_llama3.argtypes = [f64, i32, f64, f64, f64, f64, P]
+        lib.kvo_rope_omega_llama3.restype = None
+        lib.kvo_token_rows_ex.argtypes = [P, i32, i32, i32, i64, i64, P, i32, P, P, i64, i64, P, P]
+        lib.kvo_token_rows_ex.restype = ctypes.c_int
+        lib.kvo_inject_expected_ex.argtypes = [
+            P, i32, i32, i32, i64, P, P, i64, P, P, i32, P, i32, i32, i32, P, i32, P, P, i64,
+            P, P]
+        lib.kvo_inject_expected_ex.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -144,6 +157,53 @@ def rotate(x: np.ndarray, theta: float, p: float) -> np.ndarray:
     return y
 
 
+def rope_omega_llama3(theta: float, d: int, factor: float, low: float, high: float,
+                      orig: float) -> np.ndarray:
+    """Llama 3.1 scaled frequencies (see kvo_rope_omega_llama3)."""
+    out = np.empty(d // 2, np.float64)
+    _load().kvo_rope_omega_llama3(float(theta), int(d), float(factor), float(low),
+                                  float(high), float(orig), _p(out))
+    return out
+
+
+def rotate_pairs(x: np.ndarray, omega: np.ndarray, pairing: int, p: float) -> np.ndarray:
+    """Rotate one head vector with explicit frequencies and pairing."""
+    x = _c(x, np.float64)
+    omega = _c(omega, np.float64)
+    y = np.empty_like(x)
+    _load().kvo_rotate_pairs(_p(x), x.shape[0], _p(omega), int(pairing), float(p), _p(y))
+    return y
+
+
+def rotate_cs(x: np.ndarray, c: np.ndarray, s: np.ndarray, pairing: int) -> np.ndarray:
+    """Rotate one head vector by given cos/sin per pair."""
+    x = _c(x, np.float64)
+    c = _c(c, np.float64)
+    s = _c(s, np.float64)
+    y = np.empty_like(x)
+    _load().kvo_rotate_cs(_p(x), x.shape[0], _p(c), _p(s), int(pairing), _p(y))
+    return y
+
+
+def rope_spec(theta: float, d: int, pairing: int = PAIR_HALF, llama3=None,
+              cos_table=None, sin_table=None) -> dict:
+    """How the oracle rotates: frequencies (plain or Llama 3.1 scaled, llama3 =
+    (factor, low, high, orig)) or a cos/sin table (float32 [P][D/2]), and the
+    pairing."""
+    if cos_table is not None:
+        return {"omega": np.zeros(d // 2), "pairing": int(pairing),
+                "cos": _c(cos_table, np.float32), "sin": _c(sin_table, np.float32)}
+    omega = rope_omega_llama3(theta, d, *llama3) if llama3 else rope_omega(theta, d)
+    return {"omega": omega, "pairing": int(pairing), "cos": None, "sin": None}
+
+
+def _rope_args(rope: dict):
+    cos, sin = rope["cos"], rope["sin"]
+    n = 0 if cos is None else cos.shape[0]
+    return (_p(_c(rope["omega"], np.float64)), int(rope["pairing"]),
+            None if cos is None else _p(cos), None if sin is None else _p(sin), n)
+
+
 def slot(p: int, block_table: np.ndarray, block_size: int, num_blocks: int):
     """(block, offset) of position p, or None when out of range."""
     bt = _c(block_table, np.int32)
@@ -165,37 +225,44 @@ def slots(positions, block_table, block_size: int, num_blocks: int):
     return blk, off
 
 
-def token_rows(kv_bits: np.ndarray, row: int, theta: float, p: int):
+def token_rows(kv_bits: np.ndarray, row: int, theta: float, p: int, rope: dict | None = None):
     """Expected (K float64 [L][H][D], V bits uint16 [L][H][D]) of one token.
 
     kv_bits: uint16 array shaped [L][2][n_tokens][H][D] (bf16 bit patterns).
+    rope: a rope_spec(); None is the plain reading (rotate-half, theta).
     """
     kv_bits = _c(kv_bits, np.uint16)
     L, two, n_tokens, H, D = kv_bits.shape
     assert two == 2
     k_out = np.empty((L, H, D), np.float64)
     v_out = np.empty((L, H, D), np.uint16)
-    rc = _load().kvo_token_rows(_p(kv_bits), L, H, D, n_tokens, int(row),
-                                float(theta), int(p), _p(k_out), _p(v_out))
+    if rope is None:
+        rc = _load().kvo_token_rows(_p(kv_bits), L, H, D, n_tokens, int(row),
+                                    float(theta), int(p), _p(k_out), _p(v_out))
+    else:
+        rc = _load().kvo_token_rows_ex(_p(kv_bits), L, H, D, n_tokens, int(row),
+                                       *_rope_args(rope), int(p), _p(k_out), _p(v_out))
     if rc != OK:
         raise ValueError("oracle token_rows: store row out of range")
     return k_out, v_out
 
 
-def token_rows_from_rows(k_rows: np.ndarray, v_rows: np.ndarray, theta: float, p: int):
+def token_rows_from_rows(k_rows: np.ndarray, v_rows: np.ndarray, theta: float, p: int,
+                         rope: dict | None = None):
     """Same as token_rows for one token whose K and V rows ([L][H][D] bf16
     bits each) were already gathered from a store too large to pass whole."""
     k_rows = _c(k_rows, np.uint16)
     v_rows = _c(v_rows, np.uint16)
     L, H, D = k_rows.shape
     kv = np.stack([k_rows, v_rows], axis=1).reshape(L, 2, 1, H, D)
-    return token_rows(kv, 0, theta, p)
+    return token_rows(kv, 0, theta, p, rope)
 
 
 def inject_expected(kv_bits, fact_start, fact_len, ids, starts, block_table,
-                    num_blocks: int, block_size: int, theta: float):
+                    num_blocks: int, block_size: int, theta: float, rope: dict | None = None):
     """Expected pool after injecting facts ids[] at positions starts[].
 
+    rope: a rope_spec(); None is the plain reading (rotate-half, theta).
     Returns (status, expect float64 [L][2][NB][B][H][D], written uint8 same).
     """
     kv_bits = _c(kv_bits, np.uint16)
@@ -208,10 +275,16 @@ def inject_expected(kv_bits, fact_start, fact_len, ids, starts, block_table,
     shape = (L, 2, num_blocks, block_size, H, D)
     expect = np.empty(shape, np.float64)
     written = np.empty(shape, np.uint8)
-    rc = _load().kvo_inject_expected(
-        _p(kv_bits), L, H, D, n_tokens, _p(fact_start), _p(fact_len),
-        fact_len.shape[0], _p(ids), _p(starts), ids.shape[0], _p(bt), bt.shape[0],
-        int(num_blocks), int(block_size), float(theta), _p(expect), _p(written))
+    if rope is None:
+        rc = _load().kvo_inject_expected(
+            _p(kv_bits), L, H, D, n_tokens, _p(fact_start), _p(fact_len),
+            fact_len.shape[0], _p(ids), _p(starts), ids.shape[0], _p(bt), bt.shape[0],
+            int(num_blocks), int(block_size), float(theta), _p(expect), _p(written))
+    else:
+        rc = _load().kvo_inject_expected_ex(
+            _p(kv_bits), L, H, D, n_tokens, _p(fact_start), _p(fact_len),
+            fact_len.shape[0], _p(ids), _p(starts), ids.shape[0], _p(bt), bt.shape[0],
+            int(num_blocks), int(block_size), *_rope_args(rope), _p(expect), _p(written))
     return rc, expect, written
 
 

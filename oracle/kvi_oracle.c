@@ -27,6 +27,8 @@
  *   - top-k order is the total order (score descending, fact id ascending);
  *   - rotary pairing is rotate-half: element i pairs with i + D/2, with
  *     frequency omega_i = theta^(-2i/D) (RoFormer frequencies, no scaling);
+ *     the variants below (interleaved pairing, Llama 3.1 frequency scaling,
+ *     a caller's cos/sin table) are the other conventions an engine may use;
  *   - facts are placed contiguously in rank order from a start position.
  *
  * Every function below is pinned by the CPU tests against closed forms,
@@ -42,6 +44,8 @@
 
 /* Status codes returned by the oracle (independent of the library's own). */
 enum { KVO_OK = 0, KVO_BAD_ARG = 1, KVO_OUT_OF_RANGE = 2, KVO_CAPACITY = 3 };
+/* Rotary pairings (see kvo_pair). */
+enum { KVO_PAIR_HALF = 0, KVO_PAIR_INTERLEAVED = 1 };
 
 /* bf16 -> double: a bf16 value is the upper 16 bits of an IEEE binary32. */
 double kvo_bf16_to_double(uint16_t b)
@@ -138,6 +142,74 @@ void kvo_rotate(const double *x, int32_t d, double theta, double p, double *y)
     }
 }
 
+/* Variants of step 4-5.  The pairing maps pair i to its two elements:
+ *   KVO_PAIR_HALF        (i, i + D/2)   -- rotate-half, as kvo_rotate;
+ *   KVO_PAIR_INTERLEAVED (2i, 2i + 1)   -- GPT-J / RoFormer's original form.
+ * Element a of pair i is the one multiplied by cos in its own output:
+ *   y_a = x_a cos - x_b sin,   y_b = x_b cos + x_a sin. */
+static void kvo_pair(int32_t pairing, int32_t d, int32_t i, int32_t *a, int32_t *b)
+{
+    if (pairing == KVO_PAIR_INTERLEAVED) {
+        *a = 2 * i;
+        *b = 2 * i + 1;
+    } else {
+        *a = i;
+        *b = i + d / 2;
+    }
+}
+
+/* Rotate x[D] to position p with explicit per-pair frequencies omega[D/2]. */
+void kvo_rotate_pairs(const double *x, int32_t d, const double *omega, int32_t pairing,
+                      double p, double *y)
+{
+    for (int32_t i = 0; i < d / 2; ++i) {
+        int32_t ia, ib;
+        kvo_pair(pairing, d, i, &ia, &ib);
+        const double ang = p * omega[i];
+        const double c = cos(ang), sn = sin(ang);
+        y[ia] = x[ia] * c - x[ib] * sn;
+        y[ib] = x[ib] * c + x[ia] * sn;
+    }
+}
+
+/* Rotate x[D] by given cos/sin values of each pair (a caller's table row):
+ * the exact rotation with those coefficients. */
+void kvo_rotate_cs(const double *x, int32_t d, const double *c, const double *sn,
+                   int32_t pairing, double *y)
+{
+    for (int32_t i = 0; i < d / 2; ++i) {
+        int32_t ia, ib;
+        kvo_pair(pairing, d, i, &ia, &ib);
+        y[ia] = x[ia] * c[i] - x[ib] * sn[i];
+        y[ib] = x[ib] * c[i] + x[ia] * sn[i];
+    }
+}
+
+/* Llama 3.1 frequency scaling of omega_i = theta^(-2i/D) (the published
+ * "llama3" rope scaling, restated): with wavelength lambda = 2 pi / omega,
+ * a component whose wavelength is shorter than orig / high keeps omega, one
+ * longer than orig / low is slowed down to omega / factor, and in between
+ * the two are blended with weight g = (orig / lambda - low) / (high - low):
+ *   omega' = (1 - g) omega / factor + g omega. */
+void kvo_rope_omega_llama3(double theta, int32_t d, double factor, double low,
+                           double high, double orig, double *omega)
+{
+    const double two_pi = 2.0 * acos(-1.0);
+    kvo_rope_omega(theta, d, omega);
+    for (int32_t i = 0; i < d / 2; ++i) {
+        const double w = omega[i];
+        const double lambda = two_pi / w;
+        if (lambda < orig / high) {
+            omega[i] = w;
+        } else if (lambda > orig / low) {
+            omega[i] = w / factor;
+        } else {
+            const double g = (orig / lambda - low) / (high - low);
+            omega[i] = (1.0 - g) * w / factor + g * w;
+        }
+    }
+}
+
 /* Paged slot of token position p: block table entry p div B, offset p mod B
  * (vLLM PagedAttention layout behind the Section 3.4 scatter-copy).  Returns
  * KVO_OUT_OF_RANGE if p lies beyond the table or the entry is not a block of
@@ -155,19 +227,31 @@ int kvo_slot(int64_t p, const int32_t *block_table, int32_t table_len,
     return KVO_OK;
 }
 
-/* Expected rows of one injected token: fact `fact`, token t of that fact, at
- * position p.  Store layout kv[L][2][n_tokens][H][D] (bf16 bits), fact f's
- * token t at store row fact_start[f] + t.
+/* Expected rows of one injected token: store row `row`, at position p.
+ * Store layout kv[L][2][n_tokens][H][D] (bf16 bits).
  *   k_out[L][H][D]: float64 rotated K (unrounded),
  *   v_out[L][H][D]: V bits, copied unchanged.
- * Returns KVO_OUT_OF_RANGE if the row lies outside the store. */
-int kvo_token_rows(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
-                   int64_t n_tokens, int64_t row, double theta, int64_t p,
-                   double *k_out, uint16_t *v_out)
+ * The rotation: with cos_tab/sin_tab (float32 [tab_positions][D/2]) the
+ * table row p; otherwise the frequencies omega[D/2]; pairs per `pairing`.
+ * Returns KVO_OUT_OF_RANGE if the row lies outside the store or p outside
+ * the table. */
+int kvo_token_rows_ex(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                      int64_t n_tokens, int64_t row, const double *omega,
+                      int32_t pairing, const float *cos_tab, const float *sin_tab,
+                      int64_t tab_positions, int64_t p, double *k_out, uint16_t *v_out)
 {
     if (row < 0 || row >= n_tokens) return KVO_OUT_OF_RANGE;
+    if (cos_tab && (p < 0 || p >= tab_positions)) return KVO_OUT_OF_RANGE;
     double *x = (double *)malloc((size_t)D * sizeof *x);
-    if (!x) return KVO_BAD_ARG;
+    double *c = (double *)malloc((size_t)D * sizeof *c);
+    double *sn = (double *)malloc((size_t)D * sizeof *sn);
+    if (!x || !c || !sn) { free(x); free(c); free(sn); return KVO_BAD_ARG; }
+    if (cos_tab) {
+        for (int32_t i = 0; i < D / 2; ++i) {
+            c[i] = (double)cos_tab[p * (D / 2) + i];
+            sn[i] = (double)sin_tab[p * (D / 2) + i];
+        }
+    }
     const int64_t hd = (int64_t)H * D;
     for (int32_t l = 0; l < L; ++l) {
         const uint16_t *krow = kv + (((int64_t)l * 2 + 0) * n_tokens + row) * hd;
@@ -175,13 +259,31 @@ int kvo_token_rows(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
         for (int32_t h = 0; h < H; ++h) {
             for (int32_t i = 0; i < D; ++i)
                 x[i] = kvo_bf16_to_double(krow[(int64_t)h * D + i]);
-            kvo_rotate(x, D, theta, (double)p, k_out + ((int64_t)l * H + h) * D);
+            double *y = k_out + ((int64_t)l * H + h) * D;
+            if (cos_tab) kvo_rotate_cs(x, D, c, sn, pairing, y);
+            else kvo_rotate_pairs(x, D, omega, pairing, (double)p, y);
             for (int32_t i = 0; i < D; ++i)
                 v_out[((int64_t)l * H + h) * D + i] = vrow[(int64_t)h * D + i];
         }
     }
     free(x);
+    free(c);
+    free(sn);
     return KVO_OK;
+}
+
+/* The plain reading: rotate-half with omega_i = theta^(-2i/D). */
+int kvo_token_rows(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                   int64_t n_tokens, int64_t row, double theta, int64_t p,
+                   double *k_out, uint16_t *v_out)
+{
+    double *omega = (double *)malloc((size_t)(D / 2 + 1) * sizeof *omega);
+    if (!omega) return KVO_BAD_ARG;
+    kvo_rope_omega(theta, D, omega);
+    const int rc = kvo_token_rows_ex(kv, L, H, D, n_tokens, row, omega, KVO_PAIR_HALF,
+                                     NULL, NULL, 0, p, k_out, v_out);
+    free(omega);
+    return rc;
 }
 
 /* Step 6, expected cache for one request (Section 3.4 scatter-copy).
@@ -199,13 +301,14 @@ int kvo_token_rows(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
  *
  * Returns KVO_OK, KVO_OUT_OF_RANGE (id, store row or slot out of range) or
  * KVO_CAPACITY (a slot written twice: overlapping positions). */
-int kvo_inject_expected(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
-                        int64_t n_tokens, const int64_t *fact_start,
-                        const int32_t *fact_len, int64_t n_facts,
-                        const int32_t *ids, const int64_t *starts, int32_t n,
-                        const int32_t *block_table, int32_t table_len,
-                        int32_t num_blocks, int32_t block_size, double theta,
-                        double *expect, uint8_t *written)
+int kvo_inject_expected_ex(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                           int64_t n_tokens, const int64_t *fact_start,
+                           const int32_t *fact_len, int64_t n_facts,
+                           const int32_t *ids, const int64_t *starts, int32_t n,
+                           const int32_t *block_table, int32_t table_len,
+                           int32_t num_blocks, int32_t block_size, const double *omega,
+                           int32_t pairing, const float *cos_tab, const float *sin_tab,
+                           int64_t tab_positions, double *expect, uint8_t *written)
 {
     const int64_t hd = (int64_t)H * D;
     const int64_t tok_per_kv = (int64_t)num_blocks * block_size;
@@ -225,8 +328,11 @@ int kvo_inject_expected(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
             int32_t blk, off;
             if (kvo_slot(p, block_table, table_len, block_size, num_blocks,
                          &blk, &off) != KVO_OK) { rc = KVO_OUT_OF_RANGE; break; }
-            if (kvo_token_rows(kv, L, H, D, n_tokens, fact_start[f] + t, theta,
-                               p, kr, vr) != KVO_OK) { rc = KVO_OUT_OF_RANGE; break; }
+            if (kvo_token_rows_ex(kv, L, H, D, n_tokens, fact_start[f] + t, omega, pairing,
+                                  cos_tab, sin_tab, tab_positions, p, kr, vr) != KVO_OK) {
+                rc = KVO_OUT_OF_RANGE;
+                break;
+            }
             for (int32_t l = 0; l < L; ++l) {
                 for (int32_t c = 0; c < 2; ++c) {
                     const int64_t base =
@@ -245,6 +351,26 @@ int kvo_inject_expected(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
     }
     free(kr);
     free(vr);
+    return rc;
+}
+
+/* The plain reading of kvo_inject_expected_ex: rotate-half, theta. */
+int kvo_inject_expected(const uint16_t *kv, int32_t L, int32_t H, int32_t D,
+                        int64_t n_tokens, const int64_t *fact_start,
+                        const int32_t *fact_len, int64_t n_facts,
+                        const int32_t *ids, const int64_t *starts, int32_t n,
+                        const int32_t *block_table, int32_t table_len,
+                        int32_t num_blocks, int32_t block_size, double theta,
+                        double *expect, uint8_t *written)
+{
+    double *omega = (double *)malloc((size_t)(D / 2 + 1) * sizeof *omega);
+    if (!omega) return KVO_BAD_ARG;
+    kvo_rope_omega(theta, D, omega);
+    const int rc = kvo_inject_expected_ex(kv, L, H, D, n_tokens, fact_start, fact_len,
+                                          n_facts, ids, starts, n, block_table, table_len,
+                                          num_blocks, block_size, omega, KVO_PAIR_HALF, NULL,
+                                          NULL, 0, expect, written);
+    free(omega);
     return rc;
 }
 

@@ -2,7 +2,9 @@
 
 Each mutant is a one-line edit of oracle/kvi_oracle.c (a dropped term, a
 flipped sign, a wrong frequency, a reversed tie-break, an off-by-one in
-placement, a div/mod swap in paging, a stride slip, a bad bf16 decode),
+placement, a div/mod swap in paging, a stride slip, a bad bf16 decode, a
+swapped interleaved pair, a reversed or misplaced Llama 3.1 blend, a table
+rotation sign),
 compiled to a temporary library on the CPU; the pin suite is then run against
 it in a subprocess and must fail.  Nothing here touches a GPU.
 """
@@ -41,6 +43,14 @@ MUTANTS = {
         "const uint16_t *vrow = kv + (((int64_t)l * 2 + 1) * n_tokens + row) * hd;",
         "const uint16_t *vrow = kv + (((int64_t)l * 2 + 0) * n_tokens + row) * hd;"),
     "bf16_decode_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
+    "interleaved_pair_swapped": (
+        "*a = 2 * i;\n        *b = 2 * i + 1;", "*a = 2 * i + 1;\n        *b = 2 * i;"),
+    "llama3_blend_reversed": (
+        "omega[i] = (1.0 - g) * w / factor + g * w;", "omega[i] = g * w / factor + (1.0 - g) * w;"),
+    "llama3_edges_swapped": (
+        "if (lambda < orig / high) {", "if (lambda < orig / low) {"),
+    "table_rotation_sign": (
+        "y[ia] = x[ia] * c[i] - x[ib] * sn[i];", "y[ia] = x[ia] * c[i] + x[ib] * sn[i];"),
 }
 
 

@@ -391,3 +391,148 @@ def test_request_composes_the_steps():
             k1, v1 = oracle.token_rows(kv, starts[f] + t, 1e4, pos[j] + t)
             assert np.array_equal(kr[tok], k1) and np.array_equal(vr[tok], v1)
             tok += 1
+
+
+# ------------------------------------------------------- rotary variants
+#
+# Interleaved pairing (2i, 2i+1), Llama 3.1 frequency scaling and rotation
+# by a caller's cos/sin table: the conventions an engine may use other than
+# the plain reading.  Pinned by closed forms, regime invariants and
+# identities that the plain rotation already satisfies.
+
+def test_interleaved_d2_closed_form():
+    # with one pair both pairings coincide: (1, 0) at p -> (cos p, sin p)
+    for pairing in (oracle.PAIR_HALF, oracle.PAIR_INTERLEAVED):
+        y = oracle.rotate_pairs(np.array([1.0, 0.0]), np.array([1.0]), pairing, 0.7)
+        np.testing.assert_allclose(y, [math.cos(0.7), math.sin(0.7)], rtol=0, atol=1e-15)
+
+
+def test_interleaved_d4_pairs_adjacent_elements():
+    # D = 4, omega = (1, 0.01): interleaved pairs are (0, 1) and (2, 3)
+    omega = np.array([1.0, 0.01])
+    y = oracle.rotate_pairs(np.array([0.0, 0.0, 1.0, 0.0]), omega, oracle.PAIR_INTERLEAVED, 100.0)
+    np.testing.assert_allclose(y, [0.0, 0.0, math.cos(1.0), math.sin(1.0)], atol=1e-15)
+    y = oracle.rotate_pairs(np.array([0.0, 1.0, 0.0, 0.0]), omega, oracle.PAIR_INTERLEAVED, 2.0)
+    np.testing.assert_allclose(y, [-math.sin(2.0), math.cos(2.0), 0.0, 0.0], atol=1e-15)
+    # the same inputs under rotate-half pair (0, 2) and (1, 3) instead
+    y = oracle.rotate_pairs(np.array([0.0, 0.0, 1.0, 0.0]), omega, oracle.PAIR_HALF, 100.0)
+    np.testing.assert_allclose(y, [-math.sin(100.0), 0.0, math.cos(100.0), 0.0], atol=1e-13)
+
+
+def test_interleaved_is_a_permuted_rotate_half():
+    # moving element 2i to i and 2i+1 to i + D/2 turns one pairing into the
+    # other: interleaved(x) = P^-1 half(P x)
+    rng = np.random.default_rng(17)
+    D = 128
+    x = rng.standard_normal(D)
+    omega = oracle.rope_omega(5e5, D)
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])  # P x = x[perm]
+    for p in (0.0, 3.0, 1234.0, 39167.0):
+        yi = oracle.rotate_pairs(x, omega, oracle.PAIR_INTERLEAVED, p)
+        yh = oracle.rotate_pairs(x[perm], omega, oracle.PAIR_HALF, p)
+        back = np.empty(D)
+        back[perm] = yh
+        np.testing.assert_allclose(yi, back, rtol=0, atol=1e-14)
+
+
+def test_rotate_pairs_half_agrees_with_plain_rotation():
+    rng = np.random.default_rng(18)
+    x = rng.standard_normal(64)
+    omega = oracle.rope_omega(1e4, 64)
+    for p in (0.0, 1.0, 77.0, 30000.0):
+        np.testing.assert_allclose(oracle.rotate_pairs(x, omega, oracle.PAIR_HALF, p),
+                                   oracle.rotate(x, 1e4, p), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("pairing", [0, 1])
+def test_variants_keep_norms_composition_and_relocation(pairing):
+    rng = np.random.default_rng(19 + pairing)
+    D = 64
+    omega = oracle.rope_omega_llama3(5e5, D, 8.0, 1.0, 4.0, 8192.0)
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    a, b, s = 311.0, 9000.0, 20011.0
+    # pair norms
+    y = oracle.rotate_pairs(k, omega, pairing, a)
+    if pairing:
+        pn = lambda v: v[0::2] ** 2 + v[1::2] ** 2
+    else:
+        pn = lambda v: v[:D // 2] ** 2 + v[D // 2:] ** 2
+    np.testing.assert_allclose(pn(y), pn(k), rtol=1e-12)
+    # composition
+    np.testing.assert_allclose(oracle.rotate_pairs(y, omega, pairing, b),
+                               oracle.rotate_pairs(k, omega, pairing, a + b), atol=1e-9)
+    # relocation: <R_m q, R_n k> depends only on m - n
+    d1 = oracle.rotate_pairs(q, omega, pairing, a) @ oracle.rotate_pairs(k, omega, pairing, b)
+    d2 = oracle.rotate_pairs(q, omega, pairing, a + s) @ oracle.rotate_pairs(k, omega, pairing, b + s)
+    assert abs(d1 - d2) <= 1e-9 * (1 + abs(d1))
+
+
+def test_llama3_scaling_regimes():
+    # Llama 3.1 parameters: theta 5e5, D 128, factor 8, low 1, high 4,
+    # original context 8192 -> wavelengths below 2048 keep their frequency,
+    # above 8192 are divided by 8, in between lie strictly between the two
+    D, theta = 128, 5e5
+    base = oracle.rope_omega(theta, D)
+    scaled = oracle.rope_omega_llama3(theta, D, 8.0, 1.0, 4.0, 8192.0)
+    lam = 2 * math.pi / base
+    hi, lo, mid = lam < 2048, lam > 8192, (lam >= 2048) & (lam <= 8192)
+    assert hi.sum() > 0 and lo.sum() > 0 and mid.sum() > 0
+    np.testing.assert_array_equal(scaled[hi], base[hi])
+    np.testing.assert_allclose(scaled[lo], base[lo] / 8.0, rtol=1e-15)
+    assert np.all(scaled[mid] < base[mid]) and np.all(scaled[mid] > base[mid] / 8.0)
+    assert np.all(np.diff(scaled) < 0)  # still strictly decreasing
+    assert scaled[0] == 1.0
+
+
+def test_llama3_midpoint_closed_form():
+    # D = 4: omega_1 = theta^(-1/2).  Choose theta so that omega_1's
+    # wavelength is 8192 / 2.5; the blend weight is then exactly 1/2 and
+    # omega_1' = omega_1 (1/8 + 1) / 2 = 0.5625 omega_1.
+    lam = 8192.0 / 2.5
+    w1 = 2 * math.pi / lam
+    theta = (1.0 / w1) ** 2
+    scaled = oracle.rope_omega_llama3(theta, 4, 8.0, 1.0, 4.0, 8192.0)
+    assert scaled[0] == 1.0
+    assert abs(scaled[1] - 0.5625 * w1) <= 1e-12 * w1
+
+
+def test_llama3_is_continuous_at_both_edges():
+    # just inside and just outside each edge of the blend region
+    for edge, expect in ((8192.0 / 4.0, 1.0), (8192.0 / 1.0, 1.0 / 8.0)):
+        ratios = []
+        for lam in (edge * (1 - 1e-9), edge * (1 + 1e-9)):
+            w1 = 2 * math.pi / lam
+            theta = (1.0 / w1) ** 2
+            ratios.append(oracle.rope_omega_llama3(theta, 4, 8.0, 1.0, 4.0, 8192.0)[1] / w1)
+        assert abs(ratios[0] - expect) < 1e-6 and abs(ratios[1] - expect) < 1e-6
+
+
+@pytest.mark.parametrize("pairing", [0, 1])
+def test_table_rotation_closed_forms(pairing):
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal(8)
+    one, zero = np.ones(4), np.zeros(4)
+    np.testing.assert_array_equal(oracle.rotate_cs(x, one, zero, pairing), x)
+    y = oracle.rotate_cs(x, zero, one, pairing)  # a quarter turn of every pair
+    a, b = (np.arange(0, 8, 2), np.arange(1, 8, 2)) if pairing else (np.arange(4), np.arange(4, 8))
+    np.testing.assert_array_equal(y[a], -x[b])
+    np.testing.assert_array_equal(y[b], x[a])
+
+
+def test_table_rows_in_token_rows():
+    # a cos/sin table of the exact angles reproduces the computed rotation
+    # within float32 rounding of the table; positions beyond it are refused
+    rng = np.random.default_rng(29)
+    L, H, D, P = 2, 2, 16, 40
+    kv = (rng.standard_normal((L, 2, 3, H, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    omega = oracle.rope_omega(1e4, D)
+    ang = np.arange(P)[:, None] * omega[None, :]
+    rope = oracle.rope_spec(1e4, D, oracle.PAIR_INTERLEAVED, cos_table=np.cos(ang), sin_table=np.sin(ang))
+    plain = oracle.rope_spec(1e4, D, oracle.PAIR_INTERLEAVED)
+    for p in (0, 1, 39):
+        kt, vt = oracle.token_rows(kv, 1, 0.0, p, rope)
+        kp, vp = oracle.token_rows(kv, 1, 1e4, p, plain)
+        np.testing.assert_allclose(kt, kp, atol=1e-6 * np.abs(kp).max())
+        np.testing.assert_array_equal(vt, vp)
+    with pytest.raises(ValueError):
+        oracle.token_rows(kv, 1, 0.0, P, rope)
