@@ -239,6 +239,7 @@ class Bench:
         self.stream = torch.cuda.current_stream()
         kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, tl * w.block_size)
         self.bufs = {}
+        self.rope = None  # a kvi.Rope for the rotary-variant timings
 
     def buffers(self, k):
         if k not in self.bufs:
@@ -261,11 +262,42 @@ class Bench:
     def step(self, i, k, query=None):
         bf = self.buffers(k)
         q = self.queries[i % N_QUERIES:i % N_QUERIES + 1] if query is None else query
+        if self.rope is not None:
+            self.kvi.kvi_retrieve_and_inject_ex(
+                self.g, 1, self.d_views, self.w.n_facts, q, k, self.start,
+                self.tables[i % N_QUERIES:i % N_QUERIES + 1], self.table_len,
+                int(self.tables.shape[1]), self.cache, self.rope, bf["ids"], bf["scores"],
+                bf["pos"], bf["ws"], self.status, self.stream)
+            return
         self.kvi.kvi_retrieve_and_inject(
             self.g, 1, self.d_views, self.w.n_facts, q, k, self.start,
             self.tables[i % N_QUERIES:i % N_QUERIES + 1], self.table_len, int(self.tables.shape[1]),
             self.cache, self.w.rope_theta, bf["ids"], bf["scores"], bf["pos"], bf["ws"],
             self.status, self.stream)
+
+    def rope_variants(self, k, steps, warmup):
+        """Median step time (s) of the same workload under each rotary
+        variant: interleaved pairing, Llama 3.1 scaling, an engine table."""
+        import numpy as np
+        w = self.w
+        P = int(self.tables.shape[1]) * w.block_size
+        D = w.head_dim
+        inv = 1.0 / np.power(np.float32(w.rope_theta), np.arange(0, D, 2, dtype=np.float32) / np.float32(D))
+        ang = np.arange(P, dtype=np.float32)[:, None] * inv.astype(np.float32)[None, :]
+        cos_t, sin_t = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+        variants = {
+            "interleaved": self.kvi.rope(w.rope_theta, self.kvi.ROPE_PAIR_INTERLEAVED),
+            "llama3_scaling": self.kvi.rope(w.rope_theta, llama3=(8.0, 1.0, 4.0, 8192.0)),
+            "engine_table": self.kvi.rope(cos_table=cos_t, sin_table=sin_t, table_id=424242),
+        }
+        out = {}
+        for name, spec in variants.items():
+            self.kvi.kvi_prepare_rope_ex(spec, D, P)
+            self.rope = spec
+            ts, _ = self.timed(k, steps, warmup)
+            out[name] = statistics.median(ts)
+        self.rope = None
+        return out
 
     def injected_tokens(self, k):
         """Tokens each query injects (from the step's own outputs)."""
@@ -471,6 +503,9 @@ def run_ours(args):
             ts, _ = bench.timed(kk, max(10, args.steps), args.warmup)
             lat[str(kk)] = round(statistics.median(ts) * 1e6, 2)
         out["latency_us_per_request"] = lat
+    if not args.no_sweep:
+        var = bench.rope_variants(k, max(10, args.steps), args.warmup)
+        out["rope_variants_us_per_request"] = {n: round(v * 1e6, 2) for n, v in var.items()}
     if not args.no_e2e:
         e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
         e_max = max_over_ranks(dist, sum(e_times), dev)

@@ -148,6 +148,57 @@ KVI_API kvi_status kvi_store_layout(const kvi_geometry *g, const int32_t *fact_l
 KVI_API kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim,
                             int32_t max_position);
 
+/* Rotary-encoding variants.  The paper names only "rotary position
+ * embedding" (RoFormer); the plain calls above and below use rotate-half
+ * pairing with omega_i = theta^(-2i/D).  A kvi_rope selects the other
+ * conventions a serving engine may use, so that injected keys match the
+ * engine's own query rotation:
+ *   pairing  KVI_ROPE_PAIR_HALF        element i pairs with i + D/2
+ *                                      (Llama, Mistral, Qwen);
+ *            KVI_ROPE_PAIR_INTERLEAVED element 2i pairs with 2i + 1
+ *                                      (GPT-J, RoFormer's original form);
+ *   scaling  KVI_ROPE_SCALE_NONE       omega_i = theta^(-2i/D);
+ *            KVI_ROPE_SCALE_LLAMA3     Llama 3.1 scaling of those
+ *                                      frequencies: with wavelength
+ *                                      w = 2 pi / omega, components with
+ *                                      w < original / high_freq_factor keep
+ *                                      omega, those with w > original /
+ *                                      low_freq_factor use omega / factor,
+ *                                      and in between the two are blended
+ *                                      linearly in original / w;
+ *   table    cos_table/sin_table (host float32 [table_positions][D/2], pair
+ *            i at column i) with table_id != 0: the engine's own
+ *            coefficients, used as given (theta and scaling are ignored).
+ *            The library copies a table the first time it sees table_id on
+ *            a device and reuses that copy afterwards: never reuse an id
+ *            for other contents.  Positions at or beyond table_positions
+ *            are out of range (KVI_ERR_OUT_OF_RANGE on the device).
+ * Computed tables keep the float64 hi/lo precision described under
+ * kvi_prepare_rope; a caller's table is applied in float32 as given. */
+#define KVI_ROPE_PAIR_HALF 0
+#define KVI_ROPE_PAIR_INTERLEAVED 1
+#define KVI_ROPE_SCALE_NONE 0
+#define KVI_ROPE_SCALE_LLAMA3 1
+typedef struct {
+    double theta;                  /* base, > 0 (unless a table is given) */
+    int32_t pairing;               /* KVI_ROPE_PAIR_* */
+    int32_t scaling;               /* KVI_ROPE_SCALE_* */
+    double factor;                 /* LLAMA3: > 0 (Llama 3.1: 8) */
+    double low_freq_factor;        /* LLAMA3: > 0 (1) */
+    double high_freq_factor;       /* LLAMA3: > low_freq_factor (4) */
+    double original_max_positions; /* LLAMA3: > 0 (8192) */
+    const float *cos_table;        /* optional host table, see above */
+    const float *sin_table;
+    int32_t table_positions;
+    int64_t table_id;
+} kvi_rope;
+
+/* kvi_prepare_rope for any kvi_rope (head_dim as there).  Errors:
+ * KVI_ERR_INVALID_ARG (a field outside the ranges above, a table with
+ * table_id == 0 or fewer than max_position rows), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_prepare_rope_ex(const kvi_rope *rope, int32_t head_dim,
+                                       int32_t max_position);
+
 /* Device scratch bytes needed by kvi_retrieve_topk (R = 1) and
  * kvi_retrieve_and_inject for R requests of at most max_facts facts and k
  * retrieved facts each.  Returns 0 for invalid sizes. */
@@ -191,6 +242,16 @@ KVI_API kvi_status kvi_inject_paged(const kvi_store_view *store,
                             const kvi_paged_cache *cache, double rope_theta,
                             int32_t *d_status, kvi_stream_t stream);
 
+/* kvi_inject_paged with the rotation given by *rope instead of rope_theta
+ * (Section 5.1 Chunked RoPE under another rotary convention; the variants
+ * are described at kvi_rope).  Same arguments and errors otherwise. */
+KVI_API kvi_status kvi_inject_paged_ex(const kvi_store_view *store,
+                                       const int32_t *d_fact_ids,
+                                       const int32_t *d_start_pos, int32_t n,
+                                       const int32_t *d_block_table, int32_t table_len,
+                                       const kvi_paged_cache *cache, const kvi_rope *rope,
+                                       int32_t *d_status, kvi_stream_t stream);
+
 /* Fused retrieve + place + inject for R independent requests (Figure 2
  * serving path; Section 6.4's concurrent users).  Request r scores its own
  * store d_stores[r] (device array of R kvi_store_view, all with geometry g)
@@ -213,6 +274,17 @@ KVI_API kvi_status kvi_retrieve_and_inject(
     const int32_t *d_start_pos, const int32_t *d_block_tables,
     const int32_t *d_table_lens, int32_t max_blocks,
     const kvi_paged_cache *cache, double rope_theta, int32_t *d_ids,
+    float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
+    int32_t *d_status, kvi_stream_t stream);
+
+/* kvi_retrieve_and_inject with the rotation given by *rope instead of
+ * rope_theta (variants at kvi_rope).  Same arguments and errors otherwise. */
+KVI_API kvi_status kvi_retrieve_and_inject_ex(
+    const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+    int64_t max_facts, const float *d_queries, int32_t k,
+    const int32_t *d_start_pos, const int32_t *d_block_tables,
+    const int32_t *d_table_lens, int32_t max_blocks,
+    const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids,
     float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
     int32_t *d_status, kvi_stream_t stream);
 

@@ -32,7 +32,8 @@ MAX_INJECT_FACTS = 4096
 EXPORTED_SYMBOLS = (
     "kvi_store_layout", "kvi_prepare_rope", "kvi_workspace_bytes", "kvi_retrieve_topk",
     "kvi_place", "kvi_inject_paged", "kvi_retrieve_and_inject", "kvi_trace_stages",
-    "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc",
+    "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc", "kvi_prepare_rope_ex",
+    "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex",
 )
 NOALLOC_MAX_FACTS = 65536
 
@@ -57,6 +58,20 @@ class StoreView(ctypes.Structure):
 class StoreSizes(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int64), ("kv_bytes", ctypes.c_size_t),
                 ("emb_bytes", ctypes.c_size_t), ("offsets_bytes", ctypes.c_size_t)]
+
+
+ROPE_PAIR_HALF, ROPE_PAIR_INTERLEAVED = 0, 1
+ROPE_SCALE_NONE, ROPE_SCALE_LLAMA3 = 0, 1
+
+
+class Rope(ctypes.Structure):
+    """kvi_rope: rotary variant (pairing, Llama 3.1 scaling, caller table)."""
+    _fields_ = [("theta", ctypes.c_double), ("pairing", ctypes.c_int32),
+                ("scaling", ctypes.c_int32), ("factor", ctypes.c_double),
+                ("low_freq_factor", ctypes.c_double), ("high_freq_factor", ctypes.c_double),
+                ("original_max_positions", ctypes.c_double),
+                ("cos_table", ctypes.c_void_p), ("sin_table", ctypes.c_void_p),
+                ("table_positions", ctypes.c_int32), ("table_id", ctypes.c_int64)]
 
 
 class PagedCache(ctypes.Structure):
@@ -91,6 +106,12 @@ def load_library(path: str | None = None):
                                         i32, ctypes.POINTER(PagedCache), f64, P, P, P, P, sz,
                                         P, P]),
         "kvi_trace_stages": (S, [P, i32]),
+        "kvi_prepare_rope_ex": (S, [ctypes.POINTER(Rope), i32, i32]),
+        "kvi_inject_paged_ex": (S, [ctypes.POINTER(StoreView), P, P, i32, P, i32,
+                                    ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P]),
+        "kvi_retrieve_and_inject_ex": (S, [ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P,
+                                           P, i32, ctypes.POINTER(PagedCache),
+                                           ctypes.POINTER(Rope), P, P, P, P, sz, P, P]),
         "kvi_retrieve_topk_noalloc": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
@@ -183,6 +204,37 @@ def kvi_prepare_rope(rope_theta: float, head_dim: int, max_position: int) -> Non
            "kvi_prepare_rope")
 
 
+def rope(theta: float = 0.0, pairing: int = ROPE_PAIR_HALF, llama3=None, cos_table=None,
+         sin_table=None, table_id: int = 0) -> Rope:
+    """A kvi_rope.  llama3 = (factor, low_freq_factor, high_freq_factor,
+    original_max_positions).  cos_table / sin_table: contiguous host float32
+    arrays [positions][D/2] (numpy or CPU torch), kept alive by the caller for
+    the call that first uses table_id."""
+    r = Rope()
+    r.theta = float(theta)
+    r.pairing = int(pairing)
+    if llama3 is not None:
+        r.scaling = ROPE_SCALE_LLAMA3
+        r.factor, r.low_freq_factor, r.high_freq_factor, r.original_max_positions = map(float, llama3)
+    if cos_table is not None:
+        r.cos_table = _host_ptr(cos_table)
+        r.sin_table = _host_ptr(sin_table)
+        r.table_positions = int(cos_table.shape[0])
+        r.table_id = int(table_id)
+    return r
+
+
+def _host_ptr(a) -> int:
+    if hasattr(a, "data_ptr"):
+        return a.data_ptr()
+    return a.ctypes.data
+
+
+def kvi_prepare_rope_ex(spec: Rope, head_dim: int, max_position: int) -> None:
+    _check(load_library().kvi_prepare_rope_ex(ctypes.byref(spec), int(head_dim), int(max_position)),
+           "kvi_prepare_rope_ex")
+
+
 def kvi_workspace_bytes(R: int, max_facts: int, k: int) -> int:
     return int(load_library().kvi_workspace_bytes(int(R), int(max_facts), int(k)))
 
@@ -212,6 +264,25 @@ def kvi_inject_paged(store: StoreView, fact_ids, start_pos, n: int, block_table,
         ctypes.byref(store), _ptr(fact_ids), _ptr(start_pos), int(n), _ptr(block_table),
         int(table_len), ctypes.byref(cache.struct), float(rope_theta), _ptr(status),
         _stream(stream)), "kvi_inject_paged")
+
+
+def kvi_inject_paged_ex(store: StoreView, fact_ids, start_pos, n: int, block_table, table_len: int,
+                        cache: _Cache, spec: Rope, status=None, stream=None) -> None:
+    _check(load_library().kvi_inject_paged_ex(
+        ctypes.byref(store), _ptr(fact_ids), _ptr(start_pos), int(n), _ptr(block_table),
+        int(table_len), ctypes.byref(cache.struct), ctypes.byref(spec), _ptr(status),
+        _stream(stream)), "kvi_inject_paged_ex")
+
+
+def kvi_retrieve_and_inject_ex(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,
+                               start_pos, block_tables, table_lens, max_blocks: int, cache: _Cache,
+                               spec: Rope, ids, scores, pos, ws, status=None, stream=None) -> None:
+    _check(load_library().kvi_retrieve_and_inject_ex(
+        ctypes.byref(g), int(R), _ptr(stores_dev), int(max_facts), _ptr(queries), int(k),
+        _ptr(start_pos), _ptr(block_tables), _ptr(table_lens), int(max_blocks),
+        ctypes.byref(cache.struct), ctypes.byref(spec), _ptr(ids), _ptr(scores), _ptr(pos),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+        "kvi_retrieve_and_inject_ex")
 
 
 def kvi_retrieve_and_inject(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,

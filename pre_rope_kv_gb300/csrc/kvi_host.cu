@@ -103,15 +103,93 @@ std::vector<DeviceInfo> g_dev;  // indexed by device ordinal; sms == 0 = unknown
 
 // ---------------------------------------------------------------- RoPE table
 
+// One device table per (device, head_dim, frequencies): the pairing does not
+// change the table, only how the kernel applies it.
 struct RopeEntry {
     int device;
-    double theta;
     int32_t head_dim;
+    kvi_rope key;  // theta, scaling and its parameters, or table_id
     int32_t positions;
     float4 *table;
 };
 std::mutex g_rope_mu;
 std::vector<RopeEntry> g_rope;
+
+bool same_table(const kvi_rope &a, const kvi_rope &b)
+{
+    if (a.table_id || b.table_id) return a.table_id == b.table_id;
+    if (a.theta != b.theta || a.scaling != b.scaling) return false;
+    return a.scaling == KVI_ROPE_SCALE_NONE ||
+           (a.factor == b.factor && a.low_freq_factor == b.low_freq_factor &&
+            a.high_freq_factor == b.high_freq_factor &&
+            a.original_max_positions == b.original_max_positions);
+}
+
+kvi_rope plain_rope(double theta)
+{
+    kvi_rope r{};
+    r.theta = theta;
+    r.pairing = KVI_ROPE_PAIR_HALF;
+    r.scaling = KVI_ROPE_SCALE_NONE;
+    return r;
+}
+
+bool finite_pos(double x) { return x > 0.0 && std::isfinite(x); }
+
+kvi_status check_rope(const kvi_rope *r)
+{
+    if (!r) return fail(KVI_ERR_INVALID_ARG, "rope is NULL");
+    if (r->pairing != KVI_ROPE_PAIR_HALF && r->pairing != KVI_ROPE_PAIR_INTERLEAVED)
+        return fail(KVI_ERR_INVALID_ARG, "rope pairing=%d is not a KVI_ROPE_PAIR_* value", r->pairing);
+    if (r->cos_table || r->sin_table || r->table_id) {
+        if (!r->cos_table || !r->sin_table || r->table_id == 0 || r->table_positions <= 0 ||
+            r->table_positions > kMaxRopePositions)
+            return fail(KVI_ERR_INVALID_ARG,
+                        "a rope table needs cos_table, sin_table, table_id != 0 and "
+                        "table_positions in [1, 2^22]");
+        return KVI_OK;
+    }
+    if (!finite_pos(r->theta)) return fail(KVI_ERR_INVALID_ARG, "rope theta must be finite and > 0");
+    if (r->scaling == KVI_ROPE_SCALE_LLAMA3) {
+        if (!finite_pos(r->factor) || !finite_pos(r->low_freq_factor) ||
+            !finite_pos(r->high_freq_factor) || !finite_pos(r->original_max_positions) ||
+            !(r->high_freq_factor > r->low_freq_factor))
+            return fail(KVI_ERR_INVALID_ARG,
+                        "LLAMA3 rope scaling needs factor, low_freq_factor, "
+                        "original_max_positions > 0 and high_freq_factor > low_freq_factor");
+    } else if (r->scaling != KVI_ROPE_SCALE_NONE) {
+        return fail(KVI_ERR_INVALID_ARG, "rope scaling=%d is not a KVI_ROPE_SCALE_* value", r->scaling);
+    }
+    return KVI_OK;
+}
+
+// Frequencies omega_i, i < D/2: theta^(-2i/D), optionally with the Llama 3.1
+// scaling (components by wavelength: kept, divided by `factor`, or blended
+// linearly in original / wavelength between the two edges).
+std::vector<double> rope_omega(const kvi_rope &r, int32_t D)
+{
+    const int32_t half = D / 2;
+    std::vector<double> omega(half);
+    const double two_pi = 2.0 * std::acos(-1.0);
+    for (int32_t i = 0; i < half; ++i) {
+        const double w = std::pow(r.theta, -2.0 * (double)i / (double)D);
+        double out = w;
+        if (r.scaling == KVI_ROPE_SCALE_LLAMA3) {
+            const double wavelength = two_pi / w;
+            const double short_edge = r.original_max_positions / r.high_freq_factor;
+            const double long_edge = r.original_max_positions / r.low_freq_factor;
+            if (wavelength > long_edge) {
+                out = w / r.factor;
+            } else if (wavelength >= short_edge) {
+                const double g = (r.original_max_positions / wavelength - r.low_freq_factor) /
+                                 (r.high_freq_factor - r.low_freq_factor);
+                out = g * w + (1.0 - g) * (w / r.factor);
+            }
+        }
+        omega[i] = out;
+    }
+    return omega;
+}
 
 // Round a double to 16 significant bits (head) and keep the float32 tail.
 void split16(double x, float &hi, float &lo)
@@ -124,21 +202,28 @@ void split16(double x, float &hi, float &lo)
     lo = (float)(x - (double)hi);
 }
 
-void fill_rope_rows(double theta, int32_t D, int32_t p0, int32_t p1, float4 *out)
+// Rows [p0, p1) of the device table: two adjacent frequencies per 32 bytes,
+// the layout the kernels read as packed float32 pairs:
+// {cos_hi[i], cos_hi[i+1], cos_lo[i], cos_lo[i+1]},
+// {sin_hi[i], sin_hi[i+1], sin_lo[i], sin_lo[i+1]}, i even.  A caller's
+// table is taken as given: hi = its value, lo = 0.
+void fill_rope_rows(const double *omega, const kvi_rope *tab, int32_t D, int32_t p0, int32_t p1,
+                    float4 *out)
 {
     const int32_t half = D / 2;
-    std::vector<double> omega(half);
-    for (int32_t i = 0; i < half; ++i) omega[i] = std::pow(theta, -2.0 * (double)i / (double)D);
-    // two adjacent frequencies per 32 bytes, the layout the kernels read as
-    // packed float32 pairs: {cos_hi[i], cos_hi[i+1], cos_lo[i], cos_lo[i+1]},
-    // {sin_hi[i], sin_hi[i+1], sin_lo[i], sin_lo[i+1]}, i even
     for (int32_t p = p0; p < p1; ++p) {
         for (int32_t i = 0; i < half; i += 2) {
             float ch[2], cl[2], sh[2], sl[2];
             for (int u = 0; u < 2; ++u) {
-                const double a = (double)p * omega[i + u];
-                split16(std::cos(a), ch[u], cl[u]);
-                split16(std::sin(a), sh[u], sl[u]);
+                if (tab) {
+                    ch[u] = tab->cos_table[(size_t)p * half + i + u];
+                    sh[u] = tab->sin_table[(size_t)p * half + i + u];
+                    cl[u] = sl[u] = 0.0f;
+                } else {
+                    const double a = (double)p * omega[i + u];
+                    split16(std::cos(a), ch[u], cl[u]);
+                    split16(std::sin(a), sh[u], sl[u]);
+                }
             }
             out[(size_t)p * half + i] = make_float4(ch[0], ch[1], cl[0], cl[1]);
             out[(size_t)p * half + i + 1] = make_float4(sh[0], sh[1], sl[0], sl[1]);
@@ -146,16 +231,19 @@ void fill_rope_rows(double theta, int32_t D, int32_t p0, int32_t p1, float4 *out
     }
 }
 
-// Returns the table of the current device covering >= needed positions.
-kvi_status rope_get(double theta, int32_t D, int32_t needed, cudaStream_t stream,
+// Returns the table of the current device covering >= needed positions (a
+// caller's table covers its own rows, whatever is needed).
+kvi_status rope_get(const kvi_rope &spec, int32_t D, int32_t needed, cudaStream_t stream,
                     const float4 **table, int32_t *positions)
 {
     int dev = 0;
     KVI_CUDA(cudaGetDevice(&dev));
+    const bool given = spec.table_id != 0;
+    if (given) needed = spec.table_positions;
     std::lock_guard<std::mutex> lock(g_rope_mu);
     RopeEntry *hit = nullptr;
     for (auto &e : g_rope)
-        if (e.device == dev && e.theta == theta && e.head_dim == D) hit = &e;
+        if (e.device == dev && e.head_dim == D && same_table(e.key, spec)) hit = &e;
     if (hit && hit->positions >= needed) {
         *table = hit->table;
         *positions = hit->positions;
@@ -167,17 +255,18 @@ kvi_status rope_get(double theta, int32_t D, int32_t needed, cudaStream_t stream
         if (cap != cudaStreamCaptureStatusNone)
             return fail(KVI_ERR_INVALID_ARG,
                         "RoPE table for theta=%g, D=%d, %d positions is missing during stream "
-                        "capture; call kvi_prepare_rope first", theta, D, needed);
+                        "capture; call kvi_prepare_rope first", spec.theta, D, needed);
     }
-    const int32_t P = std::min(kMaxRopePositions, ((needed + 1023) / 1024) * 1024);
+    const int32_t P = given ? needed : std::min(kMaxRopePositions, ((needed + 1023) / 1024) * 1024);
     const int32_t half = D / 2;
+    const std::vector<double> omega = given ? std::vector<double>() : rope_omega(spec, D);
     std::vector<float4> host((size_t)P * half);
     const unsigned hw = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
     const int32_t nthr = (int32_t)std::min<unsigned>(hw, (unsigned)((P + 1023) / 1024));
     std::vector<std::thread> pool;
     for (int32_t t = 0; t < nthr; ++t) {
         const int32_t a = (int32_t)((int64_t)P * t / nthr), b = (int32_t)((int64_t)P * (t + 1) / nthr);
-        pool.emplace_back(fill_rope_rows, theta, D, a, b, host.data());
+        pool.emplace_back(fill_rope_rows, omega.data(), given ? &spec : nullptr, D, a, b, host.data());
     }
     for (auto &th : pool) th.join();
     float4 *d = nullptr;
@@ -194,7 +283,9 @@ kvi_status rope_get(double theta, int32_t D, int32_t needed, cudaStream_t stream
         hit->table = d;
         hit->positions = P;
     } else {
-        g_rope.push_back(RopeEntry{dev, theta, D, P, d});
+        kvi_rope key = spec;
+        key.cos_table = key.sin_table = nullptr;  // the copy is kept, not the caller's arrays
+        g_rope.push_back(RopeEntry{dev, D, key, P, d});
     }
     *table = d;
     *positions = P;
@@ -324,18 +415,27 @@ kvi_status kvi_store_layout(const kvi_geometry *g, const int32_t *fact_len, int6
     return KVI_OK;
 }
 
-kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim, int32_t max_position)
+kvi_status kvi_prepare_rope_ex(const kvi_rope *rope, int32_t head_dim, int32_t max_position)
 {
-    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
-        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    kvi_status st = check_rope(rope);
+    if (st != KVI_OK) return st;
     if (head_dim < 16 || head_dim > KVI_MAX_HEAD_DIM || head_dim % 16)
         return fail(KVI_ERR_INVALID_ARG, "head_dim=%d must be a multiple of 16 in [16, %d]",
                     head_dim, KVI_MAX_HEAD_DIM);
     if (max_position <= 0 || max_position > kMaxRopePositions)
         return fail(KVI_ERR_INVALID_ARG, "max_position=%d outside [1, 2^22]", max_position);
+    if (rope->table_id && max_position > rope->table_positions)
+        return fail(KVI_ERR_INVALID_ARG, "the rope table has %d rows, fewer than max_position=%d",
+                    rope->table_positions, max_position);
     const float4 *t;
     int32_t n;
-    return rope_get(rope_theta, head_dim, max_position, nullptr, &t, &n);
+    return rope_get(*rope, head_dim, max_position, nullptr, &t, &n);
+}
+
+kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim, int32_t max_position)
+{
+    const kvi_rope r = plain_rope(rope_theta);
+    return kvi_prepare_rope_ex(&r, head_dim, max_position);
 }
 
 size_t kvi_workspace_bytes(int32_t R, int64_t max_facts, int32_t k)
@@ -430,6 +530,16 @@ kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_i
                             int32_t table_len, const kvi_paged_cache *cache, double rope_theta,
                             int32_t *d_status, kvi_stream_t stream)
 {
+    const kvi_rope r = plain_rope(rope_theta);
+    return kvi_inject_paged_ex(store, d_fact_ids, d_start_pos, n, d_block_table, table_len, cache,
+                               &r, d_status, stream);
+}
+
+kvi_status kvi_inject_paged_ex(const kvi_store_view *store, const int32_t *d_fact_ids,
+                               const int32_t *d_start_pos, int32_t n, const int32_t *d_block_table,
+                               int32_t table_len, const kvi_paged_cache *cache, const kvi_rope *rope,
+                               int32_t *d_status, kvi_stream_t stream)
+{
     kvi_status st = check_store(store, false, true);
     if (st != KVI_OK) return st;
     if (n < 1 || n > KVI_MAX_INJECT_FACTS)
@@ -439,12 +549,12 @@ kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_i
     if (table_len < 1) return fail(KVI_ERR_INVALID_ARG, "table_len < 1");
     st = check_cache(cache, store->g);
     if (st != KVI_OK) return st;
-    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
-        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    st = check_rope(rope);
+    if (st != KVI_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float4 *table;
     int32_t positions;
-    st = rope_get(rope_theta, store->g.head_dim,
+    st = rope_get(*rope, store->g.head_dim,
                   clamp_rope((int64_t)table_len * cache->block_size), s, &table, &positions);
     if (st != KVI_OK) return st;
 
@@ -465,6 +575,7 @@ kvi_status kvi_inject_paged(const kvi_store_view *store, const int32_t *d_fact_i
     ip.block_size = cache->block_size;
     ip.rope = table;
     ip.rope_positions = positions;
+    ip.pairing = rope->pairing;
     ip.status = d_status;
     for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
     KVI_CUDA(launch_inject(ip, s, false));
@@ -478,6 +589,20 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
                                    const kvi_paged_cache *cache, double rope_theta, int32_t *d_ids,
                                    float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
                                    int32_t *d_status, kvi_stream_t stream)
+{
+    const kvi_rope r = plain_rope(rope_theta);
+    return kvi_retrieve_and_inject_ex(g, R, d_stores, max_facts, d_queries, k, d_start_pos,
+                                      d_block_tables, d_table_lens, max_blocks, cache, &r, d_ids,
+                                      d_scores, d_pos, d_ws, ws_bytes, d_status, stream);
+}
+
+kvi_status kvi_retrieve_and_inject_ex(const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+                                      int64_t max_facts, const float *d_queries, int32_t k,
+                                      const int32_t *d_start_pos, const int32_t *d_block_tables,
+                                      const int32_t *d_table_lens, int32_t max_blocks,
+                                      const kvi_paged_cache *cache, const kvi_rope *rope,
+                                      int32_t *d_ids, float *d_scores, int32_t *d_pos, void *d_ws,
+                                      size_t ws_bytes, int32_t *d_status, kvi_stream_t stream)
 {
     kvi_status st = check_geometry(g);
     if (st != KVI_OK) return st;
@@ -495,8 +620,8 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     if (st != KVI_OK) return st;
     if ((int64_t)max_blocks * cache->block_size > 0x7fffffff)
         return fail(KVI_ERR_INVALID_ARG, "max_blocks * block_size must be < 2^31");
-    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
-        return fail(KVI_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    st = check_rope(rope);
+    if (st != KVI_OK) return st;
     if (!d_ids || !d_scores || !d_pos) return fail(KVI_ERR_INVALID_ARG, "ids, scores or pos is NULL");
     const WsLayout w = ws_layout(R, max_facts, k);
     if (!d_ws || !aligned(d_ws, 256) || ws_bytes < w.total)
@@ -504,7 +629,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float4 *table;
     int32_t positions;
-    st = rope_get(rope_theta, g->head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), s,
+    st = rope_get(*rope, g->head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), s,
                   &table, &positions);
     if (st != KVI_OK) return st;
 
@@ -576,6 +701,7 @@ kvi_status kvi_retrieve_and_inject(const kvi_geometry *g, int32_t R, const kvi_s
     ip.block_size = cache->block_size;
     ip.rope = table;
     ip.rope_positions = positions;
+    ip.pairing = rope->pairing;
     ip.status = d_status;
     for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
     KVI_CUDA(launch_inject(ip, s, !trace));

@@ -232,22 +232,52 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v)
 // {sin_hi[i], sin_hi[i+1], sin_lo[i], sin_lo[i+1]}.  x * hi products are exact
 // (8 x 16 significant bits), so y0 = x0 c - x1 s and y1 = x1 c + x0 s get one
 // rounding of their main part plus a float32 tail correction.
+// Rotate two pairs at once: x0 holds their first elements, x1 their second,
+// c / sn the pairs' table entries.
+__device__ __forceinline__ void rotate2(uint64_t x0, uint64_t x1, const float4 &c, const float4 &sn,
+                                        uint64_t &y0, uint64_t &y1)
+{
+    const uint64_t chi = f2(c.x, c.y), clo = f2(c.z, c.w);
+    const uint64_t shi = f2(sn.x, sn.y), slo = f2(sn.z, sn.w);
+    y0 = add2(sub2(mul2(x0, chi), mul2(x1, shi)), sub2(mul2(x0, clo), mul2(x1, slo)));
+    y1 = add2(add2(mul2(x1, chi), mul2(x0, shi)), add2(mul2(x1, clo), mul2(x0, slo)));
+}
+
 __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float4 *cs)
 {
     uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
     uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const uint64_t x0 = bf2_to_f2(pl[w]);
-        const uint64_t x1 = bf2_to_f2(ph[w]);
-        const float4 c = cs[2 * w], sn = cs[2 * w + 1];
-        const uint64_t chi = f2(c.x, c.y), clo = f2(c.z, c.w);
-        const uint64_t shi = f2(sn.x, sn.y), slo = f2(sn.z, sn.w);
-        const uint64_t y0 = add2(sub2(mul2(x0, chi), mul2(x1, shi)), sub2(mul2(x0, clo), mul2(x1, slo)));
-        const uint64_t y1 = add2(add2(mul2(x1, chi), mul2(x0, shi)), add2(mul2(x1, clo), mul2(x0, slo)));
+        uint64_t y0, y1;
+        rotate2(bf2_to_f2(pl[w]), bf2_to_f2(ph[w]), cs[2 * w], cs[2 * w + 1], y0, y1);
         pl[w] = f2_to_bf2(y0);
         ph[w] = f2_to_bf2(y1);
     }
+}
+
+// Interleaved pairing: 16 consecutive elements a (8) then b (8) hold pairs
+// (2i, 2i+1) for 8 consecutive i, one pair per 32-bit word.  The first and
+// second elements of two adjacent pairs are gathered into float32 pairs,
+// rotated as above and interleaved back.
+__device__ __forceinline__ void rotate8_interleaved(uint4 &a, uint4 &b, const float4 *cs)
+{
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t u = w[2 * g], v = w[2 * g + 1];
+        const uint64_t x0 = f2(__uint_as_float(u << 16), __uint_as_float(v << 16));
+        const uint64_t x1 = f2(__uint_as_float(u & 0xffff0000u), __uint_as_float(v & 0xffff0000u));
+        uint64_t y0, y1;
+        rotate2(x0, x1, cs[2 * g], cs[2 * g + 1], y0, y1);
+        float y0a, y0b, y1a, y1b;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(y0a), "=f"(y0b) : "l"(y0));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(y1a), "=f"(y1b) : "l"(y1));
+        w[2 * g] = pack_bf16(y0a, y1a);
+        w[2 * g + 1] = pack_bf16(y0b, y1b);
+    }
+    a = make_uint4(w[0], w[1], w[2], w[3]);
+    b = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // cos/sin entries of one (position, vector) pair group, kept in registers
@@ -258,10 +288,12 @@ struct TableCache {
 };
 
 // Rotate a staged K piece ([ntok][hg][D] bf16) and write it to dst.  Lane
-// c takes the (token, vector) group t = c / vph, v = c % vph, loads its 8
-// cos/sin entries (cached across the layers of the piece) and walks the
-// piece's heads.  Eight lanes of one token cover 128 contiguous bytes of a
-// head, in shared memory and in the page.
+// c takes the (token, vector) group t = c / vph, v = c % vph -- pairs
+// 8v .. 8v+7 -- loads their 8 cos/sin entries (cached across the layers of
+// the piece) and walks the piece's heads.  Rotate-half: elements [8v, 8v+8)
+// with [D/2+8v, D/2+8v+8); interleaved: elements [16v, 16v+16).  Lanes of
+// one token cover contiguous bytes of a head, in shared memory and in the
+// page.
 __device__ __forceinline__ void rotate_piece(const InjectParams &p, const uint8_t *stg, uint8_t *dst,
                                              int ntok, int32_t pos0, int lane, TableCache &tc)
 {
@@ -277,6 +309,19 @@ __device__ __forceinline__ void rotate_piece(const InjectParams &p, const uint8_
             for (int e = 0; e < 8; ++e) tc.cs[e] = __ldg(tp + e);
             tc.p = pp;
             tc.v = v;
+        }
+        if (p.pairing == KVI_ROPE_PAIR_INTERLEAVED) {
+            // group v: pairs 8v .. 8v+7 = elements 16v .. 16v+15
+#pragma unroll 2
+            for (int h = 0; h < HG; ++h) {
+                const int off = ((t * HG + h) * D + 16 * v) * 2;
+                uint4 a = *reinterpret_cast<const uint4 *>(stg + off);
+                uint4 b = *reinterpret_cast<const uint4 *>(stg + off + 16);
+                if (pp != 0) rotate8_interleaved(a, b, tc.cs);
+                st_u4(dst + off, a);
+                st_u4(dst + off + 16, b);
+            }
+            continue;
         }
 #pragma unroll 2
         for (int h = 0; h < HG; ++h) {

@@ -124,6 +124,7 @@ struct InjectParams {
     int32_t num_blocks, block_size;
     const float4 *rope;        // [rope_positions][D/2]: pairs of frequencies, see kvi_host.cu
     int32_t rope_positions;
+    int32_t pairing;           // KVI_ROPE_PAIR_*
     int32_t *status;
     void *layer_base[KVI_MAX_LAYERS];
 };

@@ -55,10 +55,11 @@ def device_views(views):
 class Fused:
     """Device buffers of one kvi_retrieve_and_inject call."""
 
-    def __init__(self, b: synth.Built, k: int | None = None):
+    def __init__(self, b: synth.Built, k: int | None = None, rope=None):
         w = b.w
         self.b = b
         self.k = k or b.k
+        self.rope = rope  # a kvi.Rope for the _ex call, or None for rope_theta
         R = w.requests
         self.g = geometry_of(w)
         self.d_views = device_views(views_of(b))
@@ -75,6 +76,12 @@ class Fused:
 
     def __call__(self, stream=None):
         w = self.b.w
+        if self.rope is not None:
+            kvi.kvi_retrieve_and_inject_ex(
+                self.g, w.requests, self.d_views, w.n_facts, self.b.queries, self.k, self.start,
+                self.bt, self.tl, self.b.max_blocks, self.cache, self.rope, self.ids,
+                self.scores, self.pos, self.ws, self.status, stream)
+            return
         kvi.kvi_retrieve_and_inject(
             self.g, w.requests, self.d_views, w.n_facts, self.b.queries, self.k, self.start,
             self.bt, self.tl, self.b.max_blocks, self.cache, w.rope_theta, self.ids, self.scores,
@@ -86,8 +93,8 @@ class Fused:
                 int(self.status.item()))
 
 
-def run_fused(b: synth.Built, k: int | None = None):
-    f = Fused(b, k)
+def run_fused(b: synth.Built, k: int | None = None, rope=None):
+    f = Fused(b, k, rope)
     f()
     return f.results()
 
@@ -137,9 +144,10 @@ def check_k_v(gk, gv_bits, ek, ev_bits, where=""):
         raise AssertionError(f"{where}: V bits differ at {tuple(i)}")
 
 
-def check_pool_full(b: synth.Built, placements):
+def check_pool_full(b: synth.Built, placements, rope: dict | None = None):
     """placements: per request (ids[n], starts[n]) to expect.  Small pools:
-    the whole pool is compared with the oracle's expected pool."""
+    the whole pool is compared with the oracle's expected pool.  rope: the
+    oracle's rope_spec for a rotary variant (None: rotate-half, theta)."""
     kv_np = b.kv_np
     if kv_np is None:  # drawn on the device: read the store bits back
         kv_np = b.kv.view(torch.int16).cpu().numpy().view(np.uint16)
@@ -150,7 +158,7 @@ def check_pool_full(b: synth.Built, placements):
         st = b.stores[r]
         bt = b.block_tables[r, :b.table_lens[r]]
         rc, expect, written = oracle.inject_expected(
-            kv_np, st.start_np, st.len_np, ids, starts, bt, NB, B, b.w.rope_theta)
+            kv_np, st.start_np, st.len_np, ids, starts, bt, NB, B, b.w.rope_theta, rope)
         assert rc == oracle.OK, f"oracle rejected request {r}: {rc}"
         m = written.astype(bool)
         assert not (written_all.astype(bool) & m).any(), "requests overlap"
@@ -178,7 +186,8 @@ def token_list(b: synth.Built, placements):
     return cat(rr).astype(np.int64), cat(ff).astype(np.int64), cat(tt), cat(pp).astype(np.int64)
 
 
-def check_pool_sampled(b: synth.Built, placements, n_samples: int, seed: int = 0):
+def check_pool_sampled(b: synth.Built, placements, n_samples: int, seed: int = 0,
+                       rope: dict | None = None):
     """Large pools: compare sampled tokens' rows (all layers, K and V) with
     the oracle, reading the store bits back from the device."""
     rr, ff, tt, pp = token_list(b, placements)
@@ -208,7 +217,7 @@ def check_pool_sampled(b: synth.Built, placements, n_samples: int, seed: int = 0
     sbits = b.kv[:, :, ri].view(torch.int16).cpu().numpy().view(np.uint16)
     for n, i in enumerate(pick):
         ek, ev = oracle.token_rows_from_rows(sbits[:, 0, n], sbits[:, 1, n], b.w.rope_theta,
-                                             int(pp[i]))
+                                             int(pp[i]), rope)
         check_k_v(gvals[:, 0, n], gbits[:, 1, n], ek, ev,
                   f"request {rr[i]} fact {ff[i]} token {tt[i]} pos {pp[i]}")
     return pick.shape[0]

@@ -234,3 +234,27 @@ def test_missing_library_fails_loudly(tmp_path):
             "try:\n    b.load_library()\nexcept RuntimeError as e:\n    print('raised', e)\n")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert "raised" in r.stdout and "not built" in r.stdout
+
+
+def test_rope_spec_validation():
+    import numpy as np
+    lib_ok = kvi.load_library()
+    assert lib_ok is not None
+    bad = [
+        kvi.rope(0.0),                                   # theta must be > 0
+        kvi.rope(1e4, pairing=2),                        # unknown pairing
+        kvi.rope(1e4, llama3=(8.0, 4.0, 1.0, 8192.0)),   # high <= low
+        kvi.rope(1e4, llama3=(0.0, 1.0, 4.0, 8192.0)),   # factor <= 0
+    ]
+    for spec in bad:
+        with pytest.raises(kvi.KviError):
+            kvi.kvi_prepare_rope_ex(spec, 64, 128)
+    c = np.ones((8, 32), np.float32)
+    with pytest.raises(kvi.KviError):  # a table needs an id
+        kvi.kvi_prepare_rope_ex(kvi.rope(cos_table=c, sin_table=c, table_id=0), 64, 8)
+    with pytest.raises(kvi.KviError):  # fewer rows than max_position
+        kvi.kvi_prepare_rope_ex(kvi.rope(cos_table=c, sin_table=c, table_id=5), 64, 9)
+    spec = kvi.rope(1e4)
+    spec.scaling = 3
+    with pytest.raises(kvi.KviError):
+        kvi.kvi_prepare_rope_ex(spec, 64, 128)
