@@ -85,6 +85,7 @@ typedef enum {
 #define KVI_MAX_REQUESTS 4096     /* requests per kvi_retrieve_and_inject call */
 #define KVI_MAX_HEAD_DIM 512      /* D, a multiple of 16 */
 #define KVI_MAX_EMBED_DIM 8192    /* E, a multiple of 4 */
+#define KVI_MAX_SHARED_QUERIES 256 /* queries per shared-store call */
 
 typedef struct {
     int32_t layers;    /* L */
@@ -287,6 +288,41 @@ KVI_API kvi_status kvi_retrieve_and_inject_ex(
     const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids,
     float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
     int32_t *d_status, kvi_stream_t stream);
+
+/* Shared-store retrieval: R queries against ONE store (Section 6.4, where
+ * concurrent users query one conversation's memory).  Scoring R queries
+ * against the same embeddings is the dense contraction S = Q E^T, which runs
+ * on the tensor cores (TF32, float32 accumulation) and gives each score an
+ * interval that provably contains the exact value.  The facts whose interval
+ * can reach the k-th score are then rescored exactly (the same compensated
+ * dot product as kvi_retrieve_topk), so the result is the exact top-k under
+ * (score descending, fact id ascending): identical to kvi_retrieve_topk run
+ * once per query, at one read of the embeddings instead of R.
+ *   store      one kvi_store_view (host struct; device pointers inside)
+ *   d_queries  [R][E] float32 device, 16-byte aligned;
+ *              1 <= R <= KVI_MAX_SHARED_QUERIES
+ *   d_ids, d_scores  [R][k] (rank order)
+ *   d_ws       >= kvi_workspace_bytes_shared(R, n_facts, k) bytes,
+ *              256-byte aligned, no initialisation needed
+ *   d_status   device int32 or NULL (a timed-out wait records
+ *              KVI_ERR_TIMEOUT)
+ * Errors: KVI_ERR_INVALID_ARG, KVI_ERR_CUDA. */
+KVI_API size_t kvi_workspace_bytes_shared(int32_t R, int64_t n_facts, int32_t k);
+KVI_API kvi_status kvi_retrieve_topk_shared(const kvi_store_view *store, int32_t R,
+                                            const float *d_queries, int32_t k, int32_t *d_ids,
+                                            float *d_scores, void *d_ws, size_t ws_bytes,
+                                            int32_t *d_status, kvi_stream_t stream);
+
+/* kvi_retrieve_and_inject for R requests that share one store: the shared
+ * retrieval above, then placement and injection of each request through its
+ * own block table row (arguments as in kvi_retrieve_and_inject_ex, with the
+ * store as one host kvi_store_view). */
+KVI_API kvi_status kvi_retrieve_and_inject_shared(
+    const kvi_store_view *store, int32_t R, const float *d_queries, int32_t k,
+    const int32_t *d_start_pos, const int32_t *d_block_tables, const int32_t *d_table_lens,
+    int32_t max_blocks, const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids,
+    float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes, int32_t *d_status,
+    kvi_stream_t stream);
 
 /* No-allocation retrieval.  The paper has no counterpart: this call exists
  * for callers that cannot allocate device memory where they retrieve -- a

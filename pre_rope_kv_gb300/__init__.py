@@ -20,4 +20,6 @@ from ._binding import (  # noqa: F401
     kvi_trace_stages, kvi_workspace_bytes, load_library, pack_store_views, paged_cache,
     store_view, Rope, rope, kvi_prepare_rope_ex, kvi_inject_paged_ex, kvi_retrieve_and_inject_ex,
     ROPE_PAIR_HALF, ROPE_PAIR_INTERLEAVED, ROPE_SCALE_NONE, ROPE_SCALE_LLAMA3,
+    MAX_SHARED_QUERIES, kvi_workspace_bytes_shared, kvi_retrieve_topk_shared,
+    kvi_retrieve_and_inject_shared,
 )

@@ -33,8 +33,10 @@ EXPORTED_SYMBOLS = (
     "kvi_store_layout", "kvi_prepare_rope", "kvi_workspace_bytes", "kvi_retrieve_topk",
     "kvi_place", "kvi_inject_paged", "kvi_retrieve_and_inject", "kvi_trace_stages",
     "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc", "kvi_prepare_rope_ex",
-    "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex",
+    "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex", "kvi_workspace_bytes_shared",
+    "kvi_retrieve_topk_shared", "kvi_retrieve_and_inject_shared",
 )
+MAX_SHARED_QUERIES = 256
 NOALLOC_MAX_FACTS = 65536
 
 
@@ -107,6 +109,11 @@ def load_library(path: str | None = None):
                                         P, P]),
         "kvi_trace_stages": (S, [P, i32]),
         "kvi_prepare_rope_ex": (S, [ctypes.POINTER(Rope), i32, i32]),
+        "kvi_workspace_bytes_shared": (sz, [i32, i64, i32]),
+        "kvi_retrieve_topk_shared": (S, [ctypes.POINTER(StoreView), i32, P, i32, P, P, P, sz, P, P]),
+        "kvi_retrieve_and_inject_shared": (S, [ctypes.POINTER(StoreView), i32, P, i32, P, P, P, i32,
+                                               ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P,
+                                               P, P, P, sz, P, P]),
         "kvi_inject_paged_ex": (S, [ctypes.POINTER(StoreView), P, P, i32, P, i32,
                                     ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P]),
         "kvi_retrieve_and_inject_ex": (S, [ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P,
@@ -283,6 +290,28 @@ def kvi_retrieve_and_inject_ex(g: Geometry, R: int, stores_dev, max_facts: int, 
         ctypes.byref(cache.struct), ctypes.byref(spec), _ptr(ids), _ptr(scores), _ptr(pos),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
         "kvi_retrieve_and_inject_ex")
+
+
+def kvi_workspace_bytes_shared(R: int, n_facts: int, k: int) -> int:
+    return int(load_library().kvi_workspace_bytes_shared(int(R), int(n_facts), int(k)))
+
+
+def kvi_retrieve_topk_shared(store: StoreView, R: int, queries, k: int, ids, scores, ws,
+                             status=None, stream=None) -> None:
+    _check(load_library().kvi_retrieve_topk_shared(
+        ctypes.byref(store), int(R), _ptr(queries), int(k), _ptr(ids), _ptr(scores), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(status), _stream(stream)), "kvi_retrieve_topk_shared")
+
+
+def kvi_retrieve_and_inject_shared(store: StoreView, R: int, queries, k: int, start_pos,
+                                   block_tables, table_lens, max_blocks: int, cache: _Cache,
+                                   spec: Rope, ids, scores, pos, ws, status=None,
+                                   stream=None) -> None:
+    _check(load_library().kvi_retrieve_and_inject_shared(
+        ctypes.byref(store), int(R), _ptr(queries), int(k), _ptr(start_pos), _ptr(block_tables),
+        _ptr(table_lens), int(max_blocks), ctypes.byref(cache.struct), ctypes.byref(spec),
+        _ptr(ids), _ptr(scores), _ptr(pos), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(status), _stream(stream)), "kvi_retrieve_and_inject_shared")
 
 
 def kvi_retrieve_and_inject(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,

@@ -373,6 +373,28 @@ WsLayout ws_layout(int32_t R, int64_t max_facts, int32_t k)
     return w;
 }
 
+// Shared-store calls: the plain regions plus the coarse intervals and the
+// candidate lists.
+struct SharedWs {
+    WsLayout w;
+    size_t lo, hi, cand, cand_n, total;
+};
+
+SharedWs shared_layout(int32_t R, int64_t n_facts, int32_t k)
+{
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    SharedWs x{};
+    x.w = ws_layout(R, n_facts, k);
+    const size_t plane = (size_t)R * (size_t)x.w.key_stride * 4;
+    size_t at = x.w.total;
+    x.lo = at;     at = up(at + plane);
+    x.hi = at;     at = up(at + plane);
+    x.cand = at;   at = up(at + plane);
+    x.cand_n = at; at = up(at + (size_t)R * 4);
+    x.total = at;
+    return x;
+}
+
 }  // namespace kvi
 
 // ------------------------------------------------------------------ the ABI
@@ -683,6 +705,191 @@ kvi_status kvi_retrieve_and_inject_ex(const kvi_geometry *g, int32_t R, const kv
     ip.L = g->layers;
     ip.H = g->kv_heads;
     ip.D = g->head_dim;
+    ip.pg = pg;
+    ip.fused = 1;
+    ip.ids = d_ids;
+    ip.pos = d_pos;
+    ip.R = R;
+    ip.k = k;
+    ip.slot_len = lp.slot_len;
+    ip.pc = lp.pc;
+    ip.npc = lp.npc;
+    ip.rows = lp.rows;
+    ip.work = lp.work;
+    ip.block_tables = d_block_tables;
+    ip.table_lens = d_table_lens;
+    ip.max_blocks = max_blocks;
+    ip.num_blocks = cache->num_blocks;
+    ip.block_size = cache->block_size;
+    ip.rope = table;
+    ip.rope_positions = positions;
+    ip.pairing = rope->pairing;
+    ip.status = d_status;
+    for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
+    KVI_CUDA(launch_inject(ip, s, !trace));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[2], s));
+    return KVI_OK;
+}
+
+size_t kvi_workspace_bytes_shared(int32_t R, int64_t n_facts, int32_t k)
+{
+    if (R < 1 || R > KVI_MAX_SHARED_QUERIES || n_facts < 1 || n_facts > 0x7fffffff || k < 1 ||
+        k > KVI_MAX_K)
+        return 0;
+    return shared_layout(R, n_facts, k).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks and the three retrieval kernels of a shared-store call: tensor-core
+// coarse intervals, candidates per query, their exact keys.
+kvi_status shared_retrieve(const kvi_store_view *store, bool inject, int32_t R, const float *d_queries,
+                           int32_t k, void *d_ws, size_t ws_bytes, int32_t *d_status, cudaStream_t s,
+                           SharedWs &L)
+{
+    kvi_status st = check_store(store, true, inject);
+    if (st != KVI_OK) return st;
+    if (R < 1 || R > KVI_MAX_SHARED_QUERIES)
+        return fail(KVI_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, KVI_MAX_SHARED_QUERIES);
+    if (!d_queries || !aligned(d_queries, 16))
+        return fail(KVI_ERR_INVALID_ARG, "queries must be a 16-byte aligned device pointer");
+    if (k < 1 || k > KVI_MAX_K || (int64_t)k > store->n_facts)
+        return fail(KVI_ERR_INVALID_ARG, "k=%d outside [1, min(%d, n_facts=%lld)]", k, KVI_MAX_K,
+                    (long long)store->n_facts);
+    L = shared_layout(R, store->n_facts, k);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < L.total)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", L.total);
+    char *ws = static_cast<char *>(d_ws);
+    CoarseParams cp{};
+    cp.N = (int32_t)store->n_facts;
+    cp.R = R;
+    cp.Rp = ((R + 15) / 16) * 16;
+    cp.E = store->g.embed_dim;
+    cp.stride = L.w.key_stride;
+    cp.lo = reinterpret_cast<float *>(ws + L.lo);
+    cp.hi = reinterpret_cast<float *>(ws + L.hi);
+    cp.status = d_status;
+    KVI_CUDA(launch_coarse(cp, store->emb, store->n_facts, d_queries, s));
+    CandParams cd{};
+    cd.lo = cp.lo;
+    cd.hi = cp.hi;
+    cd.stride = cp.stride;
+    cd.N = cp.N;
+    cd.R = R;
+    cd.k = k;
+    cd.cand = reinterpret_cast<int32_t *>(ws + L.cand);
+    cd.cand_n = reinterpret_cast<int32_t *>(ws + L.cand_n);
+    KVI_CUDA(launch_candidates(cd, s));
+    RescoreParams rp{};
+    rp.store = *store;
+    rp.queries = d_queries;
+    rp.R = R;
+    rp.stride = cp.stride;
+    rp.cand = cd.cand;
+    rp.cand_n = cd.cand_n;
+    rp.keys = reinterpret_cast<uint64_t *>(ws + L.w.keys);
+    rp.lens = reinterpret_cast<int32_t *>(ws + L.w.lens);
+    KVI_CUDA(launch_rescore(rp, s));
+    return KVI_OK;
+}
+
+SelectParams shared_select_params(const kvi_store_view *store, int32_t R, int32_t k, const SharedWs &L,
+                                  char *ws, int32_t *d_ids, float *d_scores)
+{
+    SelectParams lp{};
+    lp.store.single = *store;
+    lp.store.many = nullptr;
+    lp.g = store->g;
+    lp.R = R;
+    lp.k = k;
+    lp.max_facts = store->n_facts;
+    lp.key_stride = L.w.key_stride;
+    lp.keys = reinterpret_cast<uint64_t *>(ws + L.w.keys);
+    lp.lens = reinterpret_cast<int32_t *>(ws + L.w.lens);
+    lp.cand = reinterpret_cast<int32_t *>(ws + L.cand);
+    lp.cand_n = reinterpret_cast<int32_t *>(ws + L.cand_n);
+    lp.ids = d_ids;
+    lp.scores = d_scores;
+    return lp;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvi_status kvi_retrieve_topk_shared(const kvi_store_view *store, int32_t R, const float *d_queries,
+                                    int32_t k, int32_t *d_ids, float *d_scores, void *d_ws,
+                                    size_t ws_bytes, int32_t *d_status, kvi_stream_t stream)
+{
+    if (!d_ids || !d_scores) return fail(KVI_ERR_INVALID_ARG, "ids or scores is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    SharedWs L;
+    kvi_status st = shared_retrieve(store, false, R, d_queries, k, d_ws, ws_bytes, d_status, s, L);
+    if (st != KVI_OK) return st;
+    SelectParams lp = shared_select_params(store, R, k, L, static_cast<char *>(d_ws), d_ids, d_scores);
+    lp.place = 0;
+    lp.status = d_status;
+    KVI_CUDA(launch_select(lp, s, false));
+    return KVI_OK;
+}
+
+kvi_status kvi_retrieve_and_inject_shared(const kvi_store_view *store, int32_t R, const float *d_queries,
+                                          int32_t k, const int32_t *d_start_pos,
+                                          const int32_t *d_block_tables, const int32_t *d_table_lens,
+                                          int32_t max_blocks, const kvi_paged_cache *cache,
+                                          const kvi_rope *rope, int32_t *d_ids, float *d_scores,
+                                          int32_t *d_pos, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                                          kvi_stream_t stream)
+{
+    if (!d_ids || !d_scores || !d_pos) return fail(KVI_ERR_INVALID_ARG, "ids, scores or pos is NULL");
+    if (!d_start_pos || !d_block_tables || !d_table_lens)
+        return fail(KVI_ERR_INVALID_ARG, "start positions, block tables or table lengths is NULL");
+    if (max_blocks < 1) return fail(KVI_ERR_INVALID_ARG, "max_blocks < 1");
+    if (!store) return fail(KVI_ERR_INVALID_ARG, "store is NULL");
+    kvi_status st = check_cache(cache, store->g);
+    if (st != KVI_OK) return st;
+    if ((int64_t)max_blocks * cache->block_size > 0x7fffffff)
+        return fail(KVI_ERR_INVALID_ARG, "max_blocks * block_size must be < 2^31");
+    st = check_rope(rope);
+    if (st != KVI_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float4 *table;
+    int32_t positions;
+    st = rope_get(*rope, store->g.head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), s, &table,
+                  &positions);
+    if (st != KVI_OK) return st;
+    const bool trace = t_trace_n == 3;
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[0], s));
+    SharedWs L;
+    st = shared_retrieve(store, true, R, d_queries, k, d_ws, ws_bytes, d_status, s, L);
+    if (st != KVI_OK) return st;
+    char *ws = static_cast<char *>(d_ws);
+    const PieceGeom pg = piece_geom(store->g.kv_heads, store->g.head_dim, cache->block_size);
+    SelectParams lp = shared_select_params(store, R, k, L, ws, d_ids, d_scores);
+    lp.place = 1;
+    lp.start_pos = d_start_pos;
+    lp.table_lens = d_table_lens;
+    lp.max_blocks = max_blocks;
+    lp.block_size = cache->block_size;
+    lp.pg = pg;
+    lp.pos = d_pos;
+    lp.slot_len = reinterpret_cast<int32_t *>(ws + L.w.slot_len);
+    lp.pc = reinterpret_cast<int32_t *>(ws + L.w.pc);
+    lp.npc = reinterpret_cast<int32_t *>(ws + L.w.npc);
+    lp.rows = reinterpret_cast<int64_t *>(ws + L.w.rows);
+    lp.work = reinterpret_cast<unsigned long long *>(ws + L.w.work);
+    lp.status = d_status;
+    KVI_CUDA(launch_select(lp, s, false));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
+
+    InjectParams ip{};
+    ip.store.single = *store;
+    ip.store.many = nullptr;
+    ip.L = store->g.layers;
+    ip.H = store->g.kv_heads;
+    ip.D = store->g.head_dim;
     ip.pg = pg;
     ip.fused = 1;
     ip.ids = d_ids;

@@ -397,6 +397,12 @@ __device__ __forceinline__ FactRef fact_of_split(const InjectParams &p, const in
     return q;
 }
 
+// Request r's store: its own view, or the one store all requests share.
+__device__ __forceinline__ const kvi_store_view &store_of(const InjectParams &p, int r)
+{
+    return p.store.many ? p.store.many[r] : p.store.single;
+}
+
 __device__ __forceinline__ FactRef fact_of_fused(const InjectParams &p, const int32_t *prefix, int32_t piece)
 {
     FactRef q;
@@ -408,9 +414,9 @@ __device__ __forceinline__ FactRef fact_of_fused(const InjectParams &p, const in
     q.pos = p.pos[(int64_t)r * p.k + j];
     q.len = p.slot_len[(int64_t)r * p.k + j];
     q.row = p.rows[(int64_t)r * p.k + j];
-    const kvi_store_view *sv = p.store.many + r;
-    q.kv = sv->kv;
-    q.n_tokens = sv->n_tokens;
+    const kvi_store_view &sv = store_of(p, r);
+    q.kv = sv.kv;
+    q.n_tokens = sv.n_tokens;
     q.bt = p.block_tables + (int64_t)r * p.max_blocks;
     q.tlen = p.table_lens[r];
     return q;
@@ -547,7 +553,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
     if (cached) {
         for (int i = tid; i < p.R * p.max_blocks; i += kInjThreads) sm.btab[i] = p.block_tables[i];
         for (int r = tid; r < p.R; r += kInjThreads) {
-            const kvi_store_view &v = p.store.many[r];
+            const kvi_store_view &v = store_of(p, r);
             sm.req[r] = ReqSlot{v.kv, v.n_tokens, p.table_lens[r]};
         }
         __syncthreads();

@@ -76,6 +76,10 @@ struct SelectParams {
     int64_t key_stride;
     const uint64_t *keys;
     const int32_t *lens;
+    // shared-store path: keys[r][j] belong to fact cand[r][j] (ids ascending)
+    // for j < cand_n[r]; null for the plain path (keys[r][i] = fact i)
+    const int32_t *cand;
+    const int32_t *cand_n;
     int32_t *ids;     // [R][k]
     float *scores;    // [R][k]
     // placement (fused path only; place == 0 skips it)
@@ -128,6 +132,39 @@ struct InjectParams {
     int32_t *status;
     void *layer_base[KVI_MAX_LAYERS];
 };
+
+// Shared-store scoring (kvi_shared.cu): tensor-core coarse scores with a
+// guaranteed interval [lo, hi] around every exact score.
+struct CoarseParams {
+    int32_t N, R, Rp, E;       // facts, queries, queries padded to 16, embedding dim
+    int32_t stages, tmem_cols; // set by the launcher
+    int64_t stride;            // row stride of lo / hi
+    float *lo, *hi;            // [R][stride]
+    int32_t *status;
+};
+cudaError_t launch_coarse(const CoarseParams &p, const float *emb, int64_t n_facts, const float *queries,
+                          cudaStream_t s);
+
+// Per query r: candidates = facts whose hi reaches a lower bound of the k-th
+// largest lo, in id order (cand[r][0..cand_n[r])); then their exact keys.
+struct CandParams {
+    const float *lo, *hi;
+    int64_t stride;
+    int32_t N, R, k;
+    int32_t *cand, *cand_n;
+};
+cudaError_t launch_candidates(const CandParams &p, cudaStream_t s);
+
+struct RescoreParams {
+    kvi_store_view store;
+    const float *queries;  // [R][E]
+    int32_t R;
+    int64_t stride;
+    const int32_t *cand, *cand_n;
+    uint64_t *keys;
+    int32_t *lens;
+};
+cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s);
 
 // Launchers (return the CUDA error of the launch).  `pdl` launches the kernel
 // with programmatic stream serialization so that it can start while the

@@ -958,7 +958,7 @@ select_kernel(const __grid_constant__ SelectParams p)
     const bool ok = !p.store.many || store_ok(st, p.g, p.max_facts, k);
     pdl_wait();  // keys and lengths of the scoring kernel
     pdl_launch_dependents();
-    const int64_t N = ok ? st.n_facts : 0;
+    const int64_t N = ok ? (p.cand ? (int64_t)p.cand_n[r] : st.n_facts) : 0;
     const uint64_t *keys = p.keys + (int64_t)r * p.key_stride;
     const int32_t *lens = p.lens + (int64_t)r * p.key_stride;
     // up to kSelectThreads * kKeysPerThread keys (and their lengths) are read
@@ -1089,6 +1089,13 @@ select_kernel(const __grid_constant__ SelectParams p)
         __syncthreads();
     }
     if (ok && !fast) select_by_histogram(sm, keys, lens, N, k);
+    if (ok && p.cand) {
+        // shared-store path: ranks were taken over candidate slots, whose
+        // order is the fact ids' order; map the slots to fact ids
+        for (int j = tid; j < k; j += kSelectThreads)
+            sm.out_id[j] = __ldcg(p.cand + (int64_t)r * p.key_stride + sm.out_id[j]);
+        __syncthreads();
+    }
 
     for (int j = tid; j < k; j += kSelectThreads) {
         p.ids[(int64_t)r * k + j] = ok ? sm.out_id[j] : -1;
@@ -1099,6 +1106,96 @@ select_kernel(const __grid_constant__ SelectParams p)
         if (tid < 32) place_request(p, sm, r, ok, st, start, tl);
         else if (ok) fact_rows(p, sm, st, r, k);
         if (r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
+    }
+}
+
+// ------------------------------------------------------ shared-store path
+
+// One CTA per query: t* = the largest t such that at least k of 256 groups
+// of facts hold a lo whose key's top 16 bits are >= t (so at least k facts
+// have lo >= T = the smallest value with those bits, i.e. T is at most the
+// k-th largest lo, itself at most the k-th largest exact score); every fact
+// with hi >= T is a candidate, and no other fact can be in the top k.
+// Thread t scans a contiguous id range, so a block scan of the counts
+// writes the candidates in id order.
+__global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_constant__ CandParams p)
+{
+    __shared__ uint32_t gmax[kSelectGroups];
+    __shared__ uint32_t wtot[32];
+    __shared__ uint32_t t_star;
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *lo = p.lo + (int64_t)r * p.stride;
+    const float *hi = p.hi + (int64_t)r * p.stride;
+    const int64_t N = p.N;
+    const int64_t per = (N + kSelectThreads - 1) / kSelectThreads;
+    const int64_t i0 = min(N, (int64_t)tid * per), i1 = min(N, i0 + per);
+    uint32_t mt = 0;
+    for (int64_t i = i0; i < i1; ++i) mt = max(mt, order32(__ldcg(lo + i)) >> 16);
+    mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    if ((lane & 3) == 0) gmax[tid >> 2] = mt;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v[kSelectGroups / 32];
+#pragma unroll
+        for (int i = 0; i < kSelectGroups / 32; ++i) v[i] = gmax[i * 32 + lane];
+        uint32_t a = 0, b = 1u << 16;  // t = 0 admits every fact
+        while (b - a > 1) {
+            const uint32_t mid = (a + b) >> 1;
+            uint32_t c = 0;
+#pragma unroll
+            for (int i = 0; i < kSelectGroups / 32; ++i) c += v[i] >= mid ? 1u : 0u;
+            if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)p.k) a = mid;
+            else b = mid;
+        }
+        if (lane == 0) t_star = a;
+    }
+    __syncthreads();
+    const uint32_t T = t_star << 16;
+    uint32_t cnt = 0;
+    for (int64_t i = i0; i < i1; ++i) cnt += order32(__ldcg(hi + i)) >= T ? 1u : 0u;
+    const uint32_t incl = block_incl_scan<uint32_t>(cnt, wtot);
+    uint32_t at = incl - cnt;
+    int32_t *cand = p.cand + (int64_t)r * p.stride;
+    for (int64_t i = i0; i < i1; ++i)
+        if (order32(__ldcg(hi + i)) >= T) cand[at++] = (int32_t)i;
+    if (tid == kSelectThreads - 1) p.cand_n[r] = (int32_t)incl;
+}
+
+// Exact keys of the candidates: one warp per candidate, the same Dot2
+// accumulation, combination and warp reduction as the scoring kernels, so a
+// candidate's key is bit for bit the key the plain path computes for it.
+constexpr int kRescoreWarps = 8;
+constexpr int kRescoreBlocksPerQuery = 16;
+
+__global__ void __launch_bounds__(kRescoreWarps * 32) rescore_kernel(const __grid_constant__ RescoreParams p)
+{
+    const int r = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int E = p.store.g.embed_dim;
+    const int32_t n = p.cand_n[r];
+    const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)r * E);
+    for (int64_t j = (int64_t)blockIdx.x * kRescoreWarps + (threadIdx.x >> 5); j < n;
+         j += (int64_t)gridDim.x * kRescoreWarps) {
+        const int32_t f = __ldg(p.cand + (int64_t)r * p.stride + j);
+        const float4 *row = reinterpret_cast<const float4 *>(p.store.emb + (int64_t)f * E);
+        int64_t s0 = 0;
+        int32_t l0 = -1;
+        if (lane == 1) {
+            s0 = __ldg(p.store.fact_start + f);
+            l0 = __ldg(p.store.fact_len + f);
+        }
+        Dot2x4 acc;
+        acc.zero();
+#pragma unroll 4
+        for (int v = lane; v < E / 4; v += 32) acc.add(__ldg(q4 + v), ld_stream_f4(row + v));
+        float s, c;
+        acc.combine(s, c);
+        warp_reduce_pair(s, c);
+        const int64_t at = (int64_t)r * p.stride + j;
+        if (lane == 0) p.keys[at] = score_key(s, c);
+        if (lane == 1) p.lens[at] = (l0 >= 0 && s0 >= 0 && s0 + l0 <= p.store.n_tokens) ? l0 : -1;
     }
 }
 
@@ -1196,6 +1293,18 @@ cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl)
     cfg.numAttrs = pdl ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, select_kernel, p);
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_candidates(const CandParams &p, cudaStream_t s)
+{
+    cand_kernel<<<p.R, kSelectThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s)
+{
+    rescore_kernel<<<dim3(kRescoreBlocksPerQuery, p.R), kRescoreWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
