@@ -60,6 +60,9 @@ def parse_args(argv=None):
     # profiling case only (not a bench line): a smaller store with the same
     # geometry, so that an ncu capture holds a few GB on the device
     ap.add_argument("--facts", type=int, default=0)
+    # profiling case only: shared-store retrieval of R queries over the
+    # workload's embeddings, with a one-token K/V store (~0.1 GB on the device)
+    ap.add_argument("--shared-retrieval", type=int, default=0, metavar="R")
     return ap.parse_args(argv)
 
 
@@ -344,6 +347,80 @@ class Bench:
                 stages.append((e[0].elapsed_time(e[1]) / 1e3, e[1].elapsed_time(e[2]) / 1e3))
         return times, stages
 
+    def shared_store(self, R, k, steps, warmup):
+        """R concurrent requests over this one store (Section 6.4): median
+        times (s) of retrieval alone -- one shared call (tensor-core scores +
+        exact rescoring) against R plain calls -- and of the whole fused
+        step, shared call against the plain batched call."""
+        t, kvi, w = self.torch, self.kvi, self.w
+        rng = np.random.default_rng(w.seed + 31)
+        q = t.from_numpy(self.synth.query_rows(rng, R, w.embed_dim)).cuda()
+        view = self.kvi.store_view(self.g, self.b.kv, self.b.stores[0].emb, self.b.stores[0].fact_start,
+                                   self.b.stores[0].fact_len)
+        tl = int(self.tables.shape[1])
+        L, H, D, B = w.layers, w.kv_heads, w.head_dim, w.block_size
+        pool = t.empty((L, 2, R * tl, B, H, D), dtype=t.bfloat16, device="cuda")
+        cache = kvi.paged_cache([pool[l] for l in range(L)], B)
+        tables = t.from_numpy(rng.permutation(R * tl).astype(np.int32).reshape(R, tl)).cuda()
+        tls = t.full((R,), tl, dtype=t.int32, device="cuda")
+        start = t.full((R,), int(self.b.start_pos[0]), dtype=t.int32, device="cuda")
+        d_views = t.frombuffer(bytearray(kvi.pack_store_views([view] * R)), dtype=t.uint8).cuda()
+        ids = t.empty((R, k), dtype=t.int32, device="cuda")
+        sc = t.empty((R, k), dtype=t.float32, device="cuda")
+        pos = t.empty((R, k), dtype=t.int32, device="cuda")
+        ws_s = t.empty(kvi.kvi_workspace_bytes_shared(R, w.n_facts, k), dtype=t.uint8, device="cuda")
+        ws_p = t.empty(kvi.kvi_workspace_bytes(R, w.n_facts, k), dtype=t.uint8, device="cuda")
+        ws_1 = t.empty(kvi.kvi_workspace_bytes(1, w.n_facts, k), dtype=t.uint8, device="cuda")
+        spec = kvi.rope(w.rope_theta)
+
+        def ret_shared():
+            kvi.kvi_retrieve_topk_shared(view, R, q, k, ids, sc, ws_s, self.status, self.stream)
+
+        def ret_plain():
+            for r in range(R):
+                kvi.kvi_retrieve_topk(view, q[r], k, ids[r], sc[r], ws_1, self.stream)
+
+        def fused_shared():
+            kvi.kvi_retrieve_and_inject_shared(view, R, q, k, start, tables, tls, tl, cache, spec, ids,
+                                               sc, pos, ws_s, self.status, self.stream)
+
+        def fused_plain():
+            kvi.kvi_retrieve_and_inject(self.g, R, d_views, w.n_facts, q, k, start, tables, tls, tl,
+                                        cache, w.rope_theta, ids, sc, pos, ws_p, self.status,
+                                        self.stream)
+
+        def timeit(fn):
+            for _ in range(warmup):
+                self.flush()
+                fn()
+            ts = []
+            for _ in range(steps):
+                self.flush()
+                e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                t.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / 1e3)
+            return statistics.median(ts)
+
+        out = {"requests": R, "k": k}
+        fused_plain()
+        t.cuda.synchronize()
+        want = ids.cpu().numpy().copy()
+        fused_shared()
+        t.cuda.synchronize()
+        out["same_ids_as_plain"] = bool(np.array_equal(ids.cpu().numpy(), want))
+        assert int(self.status.item()) == 0
+        out["retrieve_us"] = {"shared": round(timeit(ret_shared) * 1e6, 2),
+                              "plain_per_query_calls": round(timeit(ret_plain) * 1e6, 2)}
+        out["fused_us"] = {"shared": round(timeit(fused_shared) * 1e6, 2),
+                           "plain": round(timeit(fused_plain) * 1e6, 2)}
+        flops = 2.0 * R * w.n_facts * w.embed_dim
+        out["coarse_tf32_gflop_per_call"] = round(flops / 1e9, 3)
+        del pool
+        return out
+
     def e2e(self, k, steps, warmup):
         """Same step through the C ABI from pinned host buffers: the query,
         start position and block table go host->device and the ids, scores,
@@ -506,6 +583,7 @@ def run_ours(args):
     if not args.no_sweep:
         var = bench.rope_variants(k, max(10, args.steps), args.warmup)
         out["rope_variants_us_per_request"] = {n: round(v * 1e6, 2) for n, v in var.items()}
+        out["shared_store_64_requests"] = bench.shared_store(64, k, 10, args.warmup)
     if not args.no_e2e:
         e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
         e_max = max_over_ranks(dist, sum(e_times), dev)
@@ -523,6 +601,46 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_shared_retrieval(args):
+    """R queries against the workload's fact embeddings through
+    kvi_retrieve_topk_shared: tensor-core coarse scores, candidates, exact
+    rescoring and selection.  Prints one JSON line (not the bench line)."""
+    import torch
+    import pre_rope_kv_gb300 as kvi
+    from pre_rope_kv_gb300 import build as kbuild
+    from tests import synth
+    kbuild.build()
+    w = synth.WORKLOADS[WORKLOAD]
+    R, k = args.shared_retrieval, args.k
+    rng = np.random.default_rng(w.seed)
+    emb = torch.from_numpy(synth.unit_rows(rng, w.n_facts, w.embed_dim)).cuda()
+    q = torch.from_numpy(synth.query_rows(rng, R, w.embed_dim)).cuda()
+    kv = torch.zeros((w.layers, 2, 1, w.kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    fs = torch.zeros(w.n_facts, dtype=torch.int64, device="cuda")
+    fl = torch.ones(w.n_facts, dtype=torch.int32, device="cuda")
+    g = kvi.geometry(w.layers, w.kv_heads, w.head_dim, w.embed_dim)
+    view = kvi.store_view(g, kv, emb, fs, fl, n_tokens=1)
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvi.kvi_workspace_bytes_shared(R, w.n_facts, k), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ts = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvi.kvi_retrieve_topk_shared(view, R, q, k, ids, sc, ws, status)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    assert int(status.item()) == 0
+    print(json.dumps({"mode": "shared_retrieval", "queries": R, "k": k, "facts": w.n_facts,
+                      "embed_dim": w.embed_dim, "median_us": round(statistics.median(ts), 2),
+                      "tf32_gflop": round(2.0 * R * w.n_facts * w.embed_dim / 1e9, 3)}), flush=True)
 
 
 def run_reference(args):
@@ -560,7 +678,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.shared_retrieval:
+        run_shared_retrieval(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -6,9 +6,10 @@
 // is a dense contraction S = Q E^T, so here it runs on the 5th-generation
 // tensor cores instead of R separate scans of the matrix:
 //
-//   coarse_kernel   one CTA per 128 facts.  A TMA producer warp streams the
-//                   facts' rows and all queries through a ring of 128-byte
-//                   swizzled stages; one thread issues tcgen05.mma (kind::tf32,
+//   coarse_kernel   one CTA per 128 facts.  A TMA producer warp (one box per
+//                   lane) streams the facts' rows and all queries through a
+//                   ring of 128-byte swizzled stages; one thread issues
+//                   tcgen05.mma (kind::tf32,
 //                   M = 128, N = R padded to 16) accumulating in tensor
 //                   memory; four warps compute the row norms from the same
 //                   stages and, at the end, read the accumulator back
@@ -46,6 +47,8 @@ constexpr int kCoarseThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5
 constexpr int kStageBytesA = kTileM * kChunk * 4;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
+constexpr int kBoxRowsA = 32;  // fact rows per TMA box (4 boxes per stage)
+constexpr int kBoxRowsB = 16;  // query rows per TMA box (R padded to 16)
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct CoarseSmemTail {
@@ -165,23 +168,34 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     bool ok = true;
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint32_t bytes = (uint32_t)(kStageBytesA + stage_b);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % S;
-                const int round = kc / S;
-                if (round > 0) {
-                    if (!wait_bar(saddr(&tl.empty[s]), (uint32_t)((round - 1) & 1))) {
-                        record_status(p.status, KVI_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                const uint32_t fb = saddr(&tl.full[s]);
+        // the stage is loaded as boxes of kBoxRowsA fact rows and kBoxRowsB
+        // query rows, one box per lane (a single issuing thread caps the
+        // copy rate far below the SM's share of HBM bandwidth)
+        const uint32_t bytes = (uint32_t)(kStageBytesA + stage_b);
+        const int na = kTileM / kBoxRowsA, nb = p.Rp / kBoxRowsB;
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % S;
+            const int round = kc / S;
+            bool go = true;
+            if (lane == 0 && round > 0) go = wait_bar(saddr(&tl.empty[s]), (uint32_t)((round - 1) & 1));
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) {
+                if (lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const uint32_t fb = saddr(&tl.full[s]);
+            if (lane == 0) {
+                if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
-                tma_2d(saddr(a_st + (size_t)s * kStageBytesA), &tm_emb, kc * kChunk, tile * kTileM, fb);
-                tma_2d(saddr(b_st + (size_t)s * stage_b), &tm_q, kc * kChunk, 0, fb);
+            }
+            __syncwarp();
+            for (int j = lane; j < na + nb; j += 32) {
+                if (j < na)
+                    tma_2d(saddr(a_st + (size_t)s * kStageBytesA + (size_t)j * kBoxRowsA * 128), &tm_emb,
+                           kc * kChunk, tile * kTileM + j * kBoxRowsA, fb);
+                else
+                    tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
+                           kc * kChunk, (j - na) * kBoxRowsB, fb);
             }
         }
     } else if (warp == 1) {
@@ -349,9 +363,9 @@ cudaError_t launch_coarse(const CoarseParams &p0, const float *emb, int64_t n_fa
     while (cols < p.Rp) cols <<= 1;
     p.tmem_cols = cols;
     CUtensorMap te, tq;
-    cudaError_t e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, kTileM);
+    cudaError_t e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, kBoxRowsA);
     if (e != cudaSuccess) return e;
-    e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, (uint32_t)p.Rp);
+    e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, kBoxRowsB);
     if (e != cudaSuccess) return e;
     const size_t smem = coarse_smem_bytes(p.Rp);
     // the opt-in is made once per device, so it covers the largest ring any
