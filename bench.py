@@ -421,6 +421,27 @@ class Bench:
         del pool
         return out
 
+    def host_store(self, k, steps, warmup):
+        """The same step with the K/V store in pinned host memory
+        (KVI_STORE_KV_HOST): the inject kernel reads each piece in place over
+        the host link.  Returns the median step time (s)."""
+        t, kvi = self.torch, self.kvi
+        host = t.empty(self.b.kv.shape, dtype=self.b.kv.dtype, pin_memory=True)
+        host.copy_(self.b.kv)
+        t.cuda.synchronize()
+        st = self.b.stores[0]
+        view = kvi.store_view(self.g, host, st.emb, st.fact_start, st.fact_len,
+                              n_tokens=self.b.kv.shape[2], kv_host=True)
+        saved = self.d_views
+        self.d_views = t.frombuffer(bytearray(kvi.pack_store_views([view])), dtype=t.uint8).cuda()
+        try:
+            ts, _ = self.timed(k, steps, warmup)
+            assert int(self.status.item()) == 0
+        finally:
+            self.d_views = saved
+        del host
+        return statistics.median(ts)
+
     def e2e(self, k, steps, warmup):
         """Same step through the C ABI from pinned host buffers: the query,
         start position and block table go host->device and the ids, scores,
@@ -584,6 +605,11 @@ def run_ours(args):
         var = bench.rope_variants(k, max(10, args.steps), args.warmup)
         out["rope_variants_us_per_request"] = {n: round(v * 1e6, 2) for n, v in var.items()}
         out["shared_store_64_requests"] = bench.shared_store(64, k, 10, args.warmup)
+        hs = bench.host_store(k, 10, args.warmup)
+        hb = statistics.mean(step_tokens) * w.token_bytes
+        out["host_store_kv"] = {"latency_us_per_request": round(hs * 1e6, 2),
+                                "injected_gb_per_s": round(hb / hs / 1e9, 2),
+                                "note": "K/V in pinned host memory, read in place over the host link"}
     if not args.no_e2e:
         e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
         e_max = max_over_ranks(dist, sum(e_times), dev)

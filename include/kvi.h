@@ -97,7 +97,17 @@ typedef struct {
 /* A fact store (Figure 2 caption: retrieval embedding and pre-RoPE K/V under
  * one fact_id; fact_id = index).  The struct itself lives in host memory for
  * the single-request calls and in device memory (an array of R of them) for
- * kvi_retrieve_and_inject; the pointers inside are device pointers. */
+ * kvi_retrieve_and_inject; the pointers inside are device pointers.
+ *
+ * flags & KVI_STORE_KV_HOST: kv lives in host memory that the GPU reads in
+ * place -- pinned host memory (cudaHostAlloc, cudaHostRegister) through
+ * its unified address, or any memory on a system with hardware address
+ * translation.  The paper keeps a store that outgrows HBM in host DRAM
+ * ("a few ms" of extra TTFT); on a Grace host the inject kernel then reads
+ * each piece of K/V over NVLink-C2C directly into the rotating warps
+ * instead of staging it in shared memory.  emb, fact_start and fact_len stay
+ * in device memory. */
+#define KVI_STORE_KV_HOST 1u
 typedef struct {
     kvi_geometry g;
     int64_t n_facts;           /* N */
@@ -106,6 +116,8 @@ typedef struct {
     const float *emb;          /* float32 [N][E] */
     const int64_t *fact_start; /* [N] first store row of each fact */
     const int32_t *fact_len;   /* [N] tokens of each fact, >= 0 */
+    uint32_t flags;            /* KVI_STORE_* */
+    uint32_t reserved;         /* 0 */
 } kvi_store_view;
 
 typedef struct {

@@ -51,10 +51,14 @@ class Geometry(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("embed_dim", ctypes.c_int32)]
 
 
+STORE_KV_HOST = 1
+
+
 class StoreView(ctypes.Structure):
     _fields_ = [("g", Geometry), ("n_facts", ctypes.c_int64), ("n_tokens", ctypes.c_int64),
                 ("kv", ctypes.c_void_p), ("emb", ctypes.c_void_p),
-                ("fact_start", ctypes.c_void_p), ("fact_len", ctypes.c_void_p)]
+                ("fact_start", ctypes.c_void_p), ("fact_len", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class StoreSizes(ctypes.Structure):
@@ -160,12 +164,15 @@ def geometry(layers: int, kv_heads: int, head_dim: int, embed_dim: int) -> Geome
     return Geometry(layers, kv_heads, head_dim, embed_dim)
 
 
-def store_view(g: Geometry, kv, emb, fact_start, fact_len, n_tokens: int | None = None) -> StoreView:
+def store_view(g: Geometry, kv, emb, fact_start, fact_len, n_tokens: int | None = None,
+               kv_host: bool = False) -> StoreView:
     """Describe a store held in torch tensors (kv bf16 [L][2][T][H][D],
-    emb float32 [N][E], fact_start int64 [N], fact_len int32 [N])."""
+    emb float32 [N][E], fact_start int64 [N], fact_len int32 [N]).
+    kv_host: kv is a pinned host tensor the GPU reads in place."""
     n_facts = (emb.shape[0] if emb is not None else fact_len.shape[0])
     T = n_tokens if n_tokens is not None else (kv.shape[2] if kv is not None else 0)
-    return StoreView(g, n_facts, T, _ptr(kv), _ptr(emb), _ptr(fact_start), _ptr(fact_len))
+    return StoreView(g, n_facts, T, _ptr(kv), _ptr(emb), _ptr(fact_start), _ptr(fact_len),
+                     STORE_KV_HOST if kv_host else 0, 0)
 
 
 def pack_store_views(views: Sequence[StoreView]) -> bytes:

@@ -59,11 +59,12 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct PieceDesc {
     uint8_t *dst;
-    uint32_t bytes;  // 0: nothing to do
+    const uint8_t *src;  // host-resident store: read in place; null: staged
+    uint32_t bytes;      // 0: nothing to do
     int32_t pos0;
     int32_t ntok;
     int16_t kv;
-    int16_t stop;    // 1: no more pieces for this consumer
+    int16_t stop;        // 1: no more pieces for this consumer
 };
 
 // Small fused calls (at most kCacheReqs requests, kCacheFacts fact slots and
@@ -78,6 +79,7 @@ struct ReqSlot {
     const void *kv;
     int64_t n_tokens;
     int32_t table_len;
+    uint32_t flags;
 };
 
 struct FactSlot {
@@ -366,6 +368,7 @@ struct Piece {
     int32_t pos0;
     int32_t ntok;
     int32_t kv;
+    bool direct;     // the store is in host memory: consumers read src in place
 };
 
 // What a piece needs to know about its fact and request.
@@ -378,6 +381,7 @@ struct FactRef {
     int64_t n_tokens;
     const int32_t *bt;  // block table (global or shared memory)
     int32_t tlen;
+    uint32_t flags;     // the store's KVI_STORE_* flags
 };
 
 __device__ __forceinline__ FactRef fact_of_split(const InjectParams &p, const int32_t *prefix, int32_t piece)
@@ -394,6 +398,7 @@ __device__ __forceinline__ FactRef fact_of_split(const InjectParams &p, const in
     q.n_tokens = sv.n_tokens;
     q.bt = p.block_tables;
     q.tlen = p.table_len;
+    q.flags = sv.flags;
     return q;
 }
 
@@ -419,6 +424,7 @@ __device__ __forceinline__ FactRef fact_of_fused(const InjectParams &p, const in
     q.n_tokens = sv.n_tokens;
     q.bt = p.block_tables + (int64_t)r * p.max_blocks;
     q.tlen = p.table_lens[r];
+    q.flags = sv.flags;
     return q;
 }
 
@@ -439,6 +445,7 @@ __device__ __forceinline__ FactRef fact_of_cached(const InjectParams &p, const I
     q.n_tokens = rq.n_tokens;
     q.bt = sm.btab + r * p.max_blocks;
     q.tlen = rq.table_len;
+    q.flags = rq.flags;
     return q;
 }
 
@@ -448,7 +455,7 @@ __device__ __forceinline__ FactRef fact_of_cached(const InjectParams &p, const I
 __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjSmem &sm, bool cached,
                                                int64_t it)
 {
-    Piece x{nullptr, nullptr, 0u, 0, 0, 0};
+    Piece x{nullptr, nullptr, 0u, 0, 0, 0, false};
     const int L2 = 2 * p.L;
     int64_t piece;
     int kl;
@@ -495,6 +502,7 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
     x.bytes = (uint32_t)(x.ntok * p.pg.hg * p.D * 2);
     x.pos0 = (int32_t)a;
     x.kv = kv;
+    x.direct = (q.flags & KVI_STORE_KV_HOST) != 0;
     return x;
 }
 
@@ -554,7 +562,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
         for (int i = tid; i < p.R * p.max_blocks; i += kInjThreads) sm.btab[i] = p.block_tables[i];
         for (int r = tid; r < p.R; r += kInjThreads) {
             const kvi_store_view &v = store_of(p, r);
-            sm.req[r] = ReqSlot{v.kv, v.n_tokens, p.table_lens[r]};
+            sm.req[r] = ReqSlot{v.kv, v.n_tokens, p.table_lens[r], v.flags};
         }
         __syncthreads();
     }
@@ -640,9 +648,10 @@ inject_kernel(const __grid_constant__ InjectParams p)
                     record_status(p.status, KVI_ERR_TIMEOUT);
                     ok = false;
                 } else {
-                    sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
+                    sm.desc[s] = PieceDesc{x.dst, x.direct ? x.src : nullptr, x.bytes, x.pos0, x.ntok,
+                                           (int16_t)x.kv, 0};
                     const uint32_t fb = smem_u32(&sm.full[s]);
-                    if (x.bytes) {
+                    if (x.bytes && !x.direct) {
                         // the stage's previous contents were read by the
                         // consumers (generic proxy) before this async write
                         if (round > 0) fence_async_smem();
@@ -681,7 +690,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1), kWaitLimitNs)) {
                 record_status(p.status, KVI_ERR_TIMEOUT);
             } else {
-                sm.desc[s] = PieceDesc{nullptr, 0u, 0, 0, 0, 1};
+                sm.desc[s] = PieceDesc{nullptr, nullptr, 0u, 0, 0, 0, 1};
                 mbar_arrive(smem_u32(&sm.full[s]));
             }
         }
@@ -700,7 +709,8 @@ inject_kernel(const __grid_constant__ InjectParams p)
             }
             const PieceDesc d = sm.desc[s];
             if (d.stop) break;
-            const uint8_t *stg = sm.stage[s];
+            // staged in shared memory, or (host-resident store) read in place
+            const uint8_t *stg = d.src ? d.src : sm.stage[s];
             if (d.bytes) {
                 if (d.kv) copy_piece(stg, d.dst, d.bytes, lane);
                 else rotate_piece(p, stg, d.dst, d.ntok, d.pos0, lane, tc);
