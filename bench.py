@@ -60,6 +60,10 @@ def parse_args(argv=None):
     # profiling case only (not a bench line): a smaller store with the same
     # geometry, so that an ncu capture holds a few GB on the device
     ap.add_argument("--facts", type=int, default=0)
+    # another serving workload (not the bench line): one fused call over all
+    # of its requests per step; prints its own JSON line
+    ap.add_argument("--workload", default="", choices=["", "concurrent_64x5k", "mistral_long_50k",
+                                                        "llama3_70b_capacity"])
     # profiling case only: shared-store retrieval of R queries over the
     # workload's embeddings, with a one-token K/V store (~0.1 GB on the device)
     ap.add_argument("--shared-retrieval", type=int, default=0, metavar="R")
@@ -669,6 +673,84 @@ def run_shared_retrieval(args):
                       "tf32_gflop": round(2.0 * R * w.n_facts * w.embed_dim / 1e9, 3)}), flush=True)
 
 
+def run_workload(args):
+    """The other serving workloads at full size: 64 concurrent requests over
+    their own 5k-fact stores, Mistral-7B geometry with 50k facts placed up to
+    32k, and Llama-3-70B geometry with 256 requests into a ~150 GB pool.  One
+    step = one kvi_retrieve_and_inject call over all requests, L2 flushed
+    between steps.  Prints one JSON line (not the bench line)."""
+    import torch
+    import pre_rope_kv_gb300 as kvi
+    from pre_rope_kv_gb300 import build as kbuild
+    from tests import synth
+    kbuild.build()
+    kvi.load_library()
+    w = synth.WORKLOADS[args.workload]
+    k, R = args.k, w.requests
+    peak, peak_kind = load_peaks()
+    g = kvi.geometry(w.layers, w.kv_heads, w.head_dim, w.embed_dim)
+    if args.workload == "llama3_70b_capacity":
+        # block tables sized to each request's injected tokens, from the
+        # library's own selection, as an engine sizes them
+        b = synth.build_workload(w, k=k, with_pool=False)
+        need = []
+        ws1 = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, k), dtype=torch.uint8, device="cuda")
+        ids1 = torch.empty(k, dtype=torch.int32, device="cuda")
+        sc1 = torch.empty(k, dtype=torch.float32, device="cuda")
+        for r, st in enumerate(b.stores):
+            view = kvi.store_view(g, b.kv, st.emb, st.fact_start, st.fact_len)
+            kvi.kvi_retrieve_topk(view, b.queries[r], k, ids1, sc1, ws1)
+            torch.cuda.synchronize()
+            need.append(int(st.len_np[ids1.cpu().numpy()].sum()))
+        synth.attach_pool(b, tokens_needed=need)
+    else:
+        b = synth.build_workload(w, k=k)
+    views = [kvi.store_view(g, b.kv, st.emb, st.fact_start, st.fact_len) for st in b.stores]
+    d_views = torch.frombuffer(bytearray(kvi.pack_store_views(views)), dtype=torch.uint8).cuda()
+    cache = kvi.paged_cache([b.pool[l] for l in range(w.layers)], w.block_size)
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    pos = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvi.kvi_workspace_bytes(R, w.n_facts, k), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    start = torch.from_numpy(b.start_pos).cuda()
+    bt = torch.from_numpy(b.block_tables).cuda()
+    tl = torch.from_numpy(b.table_lens).cuda()
+    kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, int(b.max_blocks) * w.block_size)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        kvi.kvi_retrieve_and_inject(g, R, d_views, w.n_facts, b.queries, k, start, bt, tl,
+                                    b.max_blocks, cache, w.rope_theta, ids, sc, pos, ws, status)
+
+    ts = []
+    for i in range(args.warmup + args.steps):
+        flush_w.zero_()
+        flush_r.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    got = ids.cpu().numpy()
+    tokens = sum(int(b.stores[r].len_np[got[r]].sum()) for r in range(R))
+    t = statistics.median(ts)
+    inj = tokens * w.token_bytes
+    alg = 2 * inj + R * w.n_facts * w.embed_dim * 4
+    print(json.dumps({
+        "mode": "workload", "workload": args.workload, "requests": R, "k": k,
+        "facts_per_store": w.n_facts, "injected_tokens_per_step": tokens,
+        "ms_per_step": round(t * 1e3, 4), "injected_gb_per_s": round(inj / t / 1e9, 2),
+        "hbm_frac_of_measured_peak": round(alg / t / 1e9 / peak, 4), "peak_gbs": peak,
+        "peak_kind": peak_kind, "steps": args.steps, "warmup": args.warmup,
+        "store": "arena stand-in (distinct fact extents)" if w.store == "arena" else "dense",
+    }), flush=True)
+
+
 def run_reference(args):
     """The oracle arm: the float64 CPU oracle timed on the host cores."""
     rank, world, _ = dist_env()
@@ -706,6 +788,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.shared_retrieval:
         run_shared_retrieval(args)
+    elif args.workload:
+        run_workload(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
