@@ -546,11 +546,9 @@ inject_kernel(const __grid_constant__ InjectParams p)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     InjSmem &sm = *reinterpret_cast<InjSmem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        for (int s = 0; s < kInjRing; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 1);
-        }
+    if (tid < kInjRing) {  // one stage's barriers per thread
+        mbar_init(smem_u32(&sm.full[tid]), 1);
+        mbar_init(smem_u32(&sm.empty[tid]), 1);
         fence_async_smem();
     }
 

@@ -423,23 +423,23 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
     const int E = p.g.embed_dim;
     const uint32_t row_bytes = (uint32_t)E * 4u;
     const int S = min(kRingMaxStages, (int)(kRingBytes / row_bytes));
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[s])) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.empty[s])) : "memory");
-        }
+    if (tid < S) {  // one stage's barriers per thread
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[tid])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.empty[tid])) : "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    __syncthreads();
-    pdl_launch_dependents();
-
     const int64_t total = (int64_t)p.R * p.max_facts;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t g0 = (int64_t)blockIdx.x * per;
     const int64_t n = total > g0 ? min(per, total - g0) : 0;  // rows of this CTA
+    // the store view of this CTA's first request is loaded while the
+    // barriers are set up
     StoreCache sc;
     sc.r = -1;
     sc.ok = false;
+    if (n > 0) sc.get(p, (int32_t)(g0 / p.max_facts));
+    __syncthreads();
+    pdl_launch_dependents();
 
     if (warp == kRingConsumers) {
         // producer warp: every lane issues copies, rows base + lane for
