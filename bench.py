@@ -427,8 +427,8 @@ class Bench:
 
     def host_store(self, k, steps, warmup):
         """The same step with the K/V store in pinned host memory
-        (KVI_STORE_KV_HOST): the inject kernel reads each piece in place over
-        the host link.  Returns the median step time (s)."""
+        (KVI_STORE_KV_HOST): the inject kernel stages each piece over the host
+        link with cp.async.  Returns the median step time (s)."""
         t, kvi = self.torch, self.kvi
         host = t.empty(self.b.kv.shape, dtype=self.b.kv.dtype, pin_memory=True)
         host.copy_(self.b.kv)
@@ -613,7 +613,8 @@ def run_ours(args):
         hb = statistics.mean(step_tokens) * w.token_bytes
         out["host_store_kv"] = {"latency_us_per_request": round(hs * 1e6, 2),
                                 "injected_gb_per_s": round(hb / hs / 1e9, 2),
-                                "note": "K/V in pinned host memory, read in place over the host link"}
+                                "note": "K/V in pinned host memory, staged over the host link "
+                                        "with cp.async"}
     if not args.no_e2e:
         e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
         e_max = max_over_ranks(dist, sum(e_times), dev)

@@ -59,12 +59,11 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct PieceDesc {
     uint8_t *dst;
-    const uint8_t *src;  // host-resident store: read in place; null: staged
-    uint32_t bytes;      // 0: nothing to do
+    uint32_t bytes;  // 0: nothing to do
     int32_t pos0;
     int32_t ntok;
     int16_t kv;
-    int16_t stop;        // 1: no more pieces for this consumer
+    int16_t stop;    // 1: no more pieces for this consumer
 };
 
 // Small fused calls (at most kCacheReqs requests, kCacheFacts fact slots and
@@ -368,7 +367,7 @@ struct Piece {
     int32_t pos0;
     int32_t ntok;
     int32_t kv;
-    bool direct;     // the store is in host memory: consumers read src in place
+    bool direct;     // the store is in host memory: staged by cp.async, not a bulk copy
 };
 
 // What a piece needs to know about its fact and request.
@@ -637,17 +636,19 @@ inject_kernel(const __grid_constant__ InjectParams p)
         bool ok = true;
         for (;;) {
             const int64_t j = local + lane;
+            const int s = (int)(j % kInjRing);
+            Piece x{nullptr, nullptr, 0u, 0, 0, 0, false};
+            bool staged = false;  // this lane's stage is free and described
             if (lane < nb) {
-                const Piece x = resolve_piece(p, sm, cached, first + lane);
-                const int s = (int)(j % kInjRing);
+                x = resolve_piece(p, sm, cached, first + lane);
                 const int64_t round = j / kInjRing;
                 if (round > 0 &&
                     !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1), kWaitLimitNs)) {
                     record_status(p.status, KVI_ERR_TIMEOUT);
                     ok = false;
                 } else {
-                    sm.desc[s] = PieceDesc{x.dst, x.direct ? x.src : nullptr, x.bytes, x.pos0, x.ntok,
-                                           (int16_t)x.kv, 0};
+                    staged = true;
+                    sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
                     const uint32_t fb = smem_u32(&sm.full[s]);
                     if (x.bytes && !x.direct) {
                         // the stage's previous contents were read by the
@@ -655,10 +656,31 @@ inject_kernel(const __grid_constant__ InjectParams p)
                         if (round > 0) fence_async_smem();
                         mbar_expect_tx(fb, x.bytes);
                         bulk_load(smem_u32(sm.stage[s]), x.src, x.bytes, fb);
-                    } else {
+                    } else if (!x.bytes) {
                         mbar_arrive(fb);
                     }
                 }
+            }
+            // pieces of a host-resident store: the whole warp copies each
+            // one into its stage with 16-byte cp.async (no bulk copy from
+            // host memory); every lane's copies are tracked by the stage's
+            // barrier, and one plain arrival completes its expected count
+            uint32_t host = __ballot_sync(0xffffffffu, staged && x.bytes && x.direct);
+            while (host) {
+                const int i = __ffs(host) - 1;
+                host &= host - 1;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(x.src), i));
+                const uint32_t bytes = __shfl_sync(0xffffffffu, x.bytes, i);
+                const int si = __shfl_sync(0xffffffffu, s, i);
+                const uint32_t dst = smem_u32(sm.stage[si]);
+                for (uint32_t o = 16u * lane; o < bytes; o += 512u)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + o), "l"(src + o)
+                                 : "memory");
+                const uint32_t fb = smem_u32(&sm.full[si]);
+                asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(fb) : "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fb);
             }
             local += nb;
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -688,7 +710,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 !mbar_wait(smem_u32(&sm.empty[s]), (uint32_t)((round - 1) & 1), kWaitLimitNs)) {
                 record_status(p.status, KVI_ERR_TIMEOUT);
             } else {
-                sm.desc[s] = PieceDesc{nullptr, nullptr, 0u, 0, 0, 0, 1};
+                sm.desc[s] = PieceDesc{nullptr, 0u, 0, 0, 0, 1};
                 mbar_arrive(smem_u32(&sm.full[s]));
             }
         }
@@ -707,8 +729,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
             }
             const PieceDesc d = sm.desc[s];
             if (d.stop) break;
-            // staged in shared memory, or (host-resident store) read in place
-            const uint8_t *stg = d.src ? d.src : sm.stage[s];
+            const uint8_t *stg = sm.stage[s];
             if (d.bytes) {
                 if (d.kv) copy_piece(stg, d.dst, d.bytes, lane);
                 else rotate_piece(p, stg, d.dst, d.ntok, d.pos0, lane, tc);
