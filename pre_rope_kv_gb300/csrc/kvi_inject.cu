@@ -98,6 +98,9 @@ struct __align__(128) InjSmem {
     FactSlot fact[kCacheFacts];
     int32_t fpc[kCacheFacts];
     int32_t btab[kCacheBlocks];
+    // the pool's per-layer bases: each producer lane looks up its own layer,
+    // which from the kernel parameters would be a divergent constant load
+    uint8_t *lbase[KVI_MAX_LAYERS];
 };
 static_assert(sizeof(InjSmem) <= 227 * 1024, "inject shared memory");
 
@@ -495,7 +498,7 @@ __device__ __forceinline__ Piece resolve_piece(const InjectParams &p, const InjS
     const int64_t row = q.row + (a - q.pos);
     x.src = reinterpret_cast<const uint8_t *>(q.kv) +
             ((((int64_t)l * 2 + kv) * q.n_tokens + row) * HD + hoff) * 2;
-    x.dst = reinterpret_cast<uint8_t *>(p.layer_base[l]) +
+    x.dst = sm.lbase[l] +
             ((((int64_t)kv * p.num_blocks + blk) * B + (au - page * (uint32_t)B)) * HD + hoff) * 2;
     x.ntok = (int32_t)(b - a);
     x.bytes = (uint32_t)(x.ntok * p.pg.hg * p.D * 2);
@@ -550,6 +553,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
         mbar_init(smem_u32(&sm.empty[tid]), 1);
         fence_async_smem();
     }
+    for (int l = tid; l < p.L; l += kInjThreads) sm.lbase[l] = reinterpret_cast<uint8_t *>(p.layer_base[l]);
 
     // small fused calls: the requests' inputs (store views, block tables,
     // table lengths) are staged before the selection ends
