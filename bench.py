@@ -446,6 +446,68 @@ class Bench:
         del host
         return statistics.median(ts)
 
+    def _packed_io(self, k):
+        """One device block for a request's inputs (query | start | block
+        table) and one for its outputs (ids | scores | positions | status),
+        with pinned host twins, so that a step moves one copy each way."""
+        t = self.torch
+        E, tl = self.w.embed_dim, int(self.tables.shape[1])
+        q_off, s_off, bt_off = 0, E * 4, E * 4 + 16
+        in_bytes = bt_off + tl * 4
+        d_in = t.empty(in_bytes, dtype=t.uint8, device="cuda")
+        h_in = t.empty((N_QUERIES, in_bytes), dtype=t.uint8).pin_memory()
+        for j in range(N_QUERIES):
+            h_in[j, q_off:s_off] = t.from_numpy(self.queries[j].cpu().numpy().view(np.uint8))
+            h_in[j, s_off:s_off + 4] = t.from_numpy(self.b.start_pos[:1].astype(np.int32).view(np.uint8))
+            h_in[j, bt_off:] = t.from_numpy(self.tables[j].cpu().numpy().astype(np.int32).view(np.uint8))
+        out_bytes = 12 * k + 4
+        d_out = t.zeros(out_bytes, dtype=t.uint8, device="cuda")
+        h_out = t.empty(out_bytes, dtype=t.uint8).pin_memory()
+        io = dict(d_in=d_in, h_in=h_in, d_out=d_out, h_out=h_out,
+                  q=d_in[q_off:s_off].view(t.float32).view(1, E),
+                  start=d_in[s_off:s_off + 4].view(t.int32),
+                  bt=d_in[bt_off:].view(t.int32).view(1, tl),
+                  ids=d_out[:4 * k].view(t.int32).view(1, k),
+                  scores=d_out[4 * k:8 * k].view(t.float32).view(1, k),
+                  pos=d_out[8 * k:12 * k].view(t.int32).view(1, k),
+                  status=d_out[12 * k:].view(t.int32))
+        return io, in_bytes, out_bytes
+
+    def e2e_plan(self, k, steps, warmup):
+        """The serving loop's way of calling the library: a request is
+        written into a pinned staging block and one kvi_plan_launch runs its
+        host->device copy, the fused call and the device->host copy of its
+        outputs, recorded once as a CUDA graph."""
+        t, kvi = self.torch, self.kvi
+        tl = int(self.tables.shape[1])
+        io, in_bytes, out_bytes = self._packed_io(k)
+        ws = self.buffers(k)["ws"]
+        # the plan records the request's two copies with the fused call:
+        # the loop writes a request into the pinned staging block, launches
+        # once and reads the pinned output block
+        stage = t.empty(in_bytes, dtype=t.uint8).pin_memory()
+        plan = kvi.kvi_plan_create_fused(self.g, 1, self.d_views, self.w.n_facts, io["q"], k, io["start"],
+                                         io["bt"], self.table_len, tl, self.cache,
+                                         kvi.rope(self.w.rope_theta), io["ids"], io["scores"], io["pos"],
+                                         ws, io["status"], io=(stage, io["d_in"], io["d_out"], io["h_out"]))
+        stage_np = stage.numpy()
+        h_in_np = io["h_in"].numpy()
+        times = []
+        for i in range(warmup + steps):
+            self.flush()
+            t.cuda.synchronize()
+            t0 = time.perf_counter()
+            stage_np[:] = h_in_np[i % N_QUERIES]
+            plan.launch(self.stream)
+            t.cuda.synchronize()
+            t1 = time.perf_counter()
+            if i >= warmup:
+                times.append(t1 - t0)
+        status = int(io["h_out"][12 * k:].view(t.int32).item())
+        assert status == 0, f"device status {status}"
+        plan.close()
+        return times, in_bytes, out_bytes
+
     def e2e(self, k, steps, warmup):
         """Same step through the C ABI from pinned host buffers: the query,
         start position and block table go host->device and the ids, scores,
@@ -616,11 +678,20 @@ def run_ours(args):
                                 "note": "K/V in pinned host memory, staged over the host link "
                                         "with cp.async"}
     if not args.no_e2e:
-        e_times, h2d, d2h = bench.e2e(k, args.steps, args.warmup)
+        # the serving loop's path (a recorded plan per request) is the e2e
+        # figure; direct calls through the same C ABI are reported beside it
+        e_times, _, _ = bench.e2e(k, args.steps, args.warmup)
+        p_times, h2d, d2h = bench.e2e_plan(k, args.steps, args.warmup)
         e_max = max_over_ranks(dist, sum(e_times), dev)
-        out["e2e"] = {"value": round(all_bytes / e_max / 1e9, 2), "unit": "GB/s",
+        p_max = max_over_ranks(dist, sum(p_times), dev)
+        out["e2e"] = {"value": round(all_bytes / p_max / 1e9, 2), "unit": "GB/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "latency_us_median": round(statistics.median(e_times) * 1e6, 2)}
+                      "latency_us_median": round(statistics.median(p_times) * 1e6, 2),
+                      "path": "kvi_plan_launch (request copies + fused call, recorded once as a "
+                              "CUDA graph)"}
+        out["e2e_direct"] = {"value": round(all_bytes / e_max / 1e9, 2), "unit": "GB/s",
+                             "latency_us_median": round(statistics.median(e_times) * 1e6, 2),
+                             "path": "kvi_retrieve_and_inject per request"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, secs, toks = cpu_baseline_sample(w, k, 6, w.seed + 99)
         out["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1,

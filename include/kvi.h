@@ -301,6 +301,45 @@ KVI_API kvi_status kvi_retrieve_and_inject_ex(
     float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
     int32_t *d_status, kvi_stream_t stream);
 
+/* Plans: one fused call recorded once into a CUDA graph and replayed.  A
+ * serving loop calls kvi_retrieve_and_inject_ex with the same buffers for
+ * every request and only their contents change (query, start, block table).
+ * A plan records that call once -- its three kernel launches, with their
+ * programmatic dependencies as graph edges -- so that each request costs
+ * one graph launch on the host instead of three kernel launches and the
+ * argument checks.  The arguments are those of kvi_retrieve_and_inject_ex;
+ * the buffers must stay valid, and their contents are read at each
+ * kvi_plan_launch.  *d_status is not reset by a launch (as with direct
+ * calls, the first error stays).  Creating a plan builds the RoPE table
+ * first, records on a private stream and needs no other stream to be idle.
+ * Errors: those of kvi_retrieve_and_inject_ex, KVI_ERR_CUDA. */
+typedef struct kvi_plan_s *kvi_plan;
+KVI_API kvi_status kvi_plan_create_fused(
+    kvi_plan *plan, const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+    int64_t max_facts, const float *d_queries, int32_t k, const int32_t *d_start_pos,
+    const int32_t *d_block_tables, const int32_t *d_table_lens, int32_t max_blocks,
+    const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids, float *d_scores,
+    int32_t *d_pos, void *d_ws, size_t ws_bytes, int32_t *d_status);
+/* kvi_plan_create_fused that also records the request's copies: before the
+ * fused call, in_bytes from pinned host memory h_in to device d_in (the
+ * request's packed inputs, e.g. query | start | block table, which the
+ * d_* arguments point into); after it, out_bytes from device d_out to
+ * pinned host memory h_out (the packed outputs).  A serving loop then
+ * writes a request into h_in, launches the plan once and reads h_out after
+ * the stream is synchronised.  h_in / h_out must be pinned (cudaHostAlloc or
+ * cudaHostRegister); 0 bytes skips that copy. */
+KVI_API kvi_status kvi_plan_create_fused_io(
+    kvi_plan *plan, const kvi_geometry *g, int32_t R, const kvi_store_view *d_stores,
+    int64_t max_facts, const float *d_queries, int32_t k, const int32_t *d_start_pos,
+    const int32_t *d_block_tables, const int32_t *d_table_lens, int32_t max_blocks,
+    const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids, float *d_scores,
+    int32_t *d_pos, void *d_ws, size_t ws_bytes, int32_t *d_status, const void *h_in,
+    void *d_in, size_t in_bytes, const void *d_out, void *h_out, size_t out_bytes);
+/* Replay the plan on `stream` (stream order applies as for a kernel). */
+KVI_API kvi_status kvi_plan_launch(kvi_plan plan, kvi_stream_t stream);
+/* Free the plan (after its last launch has completed). */
+KVI_API kvi_status kvi_plan_destroy(kvi_plan plan);
+
 /* Shared-store retrieval: R queries against ONE store (Section 6.4, where
  * concurrent users query one conversation's memory).  Scoring R queries
  * against the same embeddings is the dense contraction S = Q E^T, which runs

@@ -21,5 +21,5 @@ from ._binding import (  # noqa: F401
     store_view, Rope, rope, kvi_prepare_rope_ex, kvi_inject_paged_ex, kvi_retrieve_and_inject_ex,
     ROPE_PAIR_HALF, ROPE_PAIR_INTERLEAVED, ROPE_SCALE_NONE, ROPE_SCALE_LLAMA3,
     MAX_SHARED_QUERIES, kvi_workspace_bytes_shared, kvi_retrieve_topk_shared,
-    kvi_retrieve_and_inject_shared, STORE_KV_HOST,
+    kvi_retrieve_and_inject_shared, STORE_KV_HOST, Plan, kvi_plan_create_fused,
 )

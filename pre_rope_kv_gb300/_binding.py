@@ -34,7 +34,8 @@ EXPORTED_SYMBOLS = (
     "kvi_place", "kvi_inject_paged", "kvi_retrieve_and_inject", "kvi_trace_stages",
     "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc", "kvi_prepare_rope_ex",
     "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex", "kvi_workspace_bytes_shared",
-    "kvi_retrieve_topk_shared", "kvi_retrieve_and_inject_shared",
+    "kvi_retrieve_topk_shared", "kvi_retrieve_and_inject_shared", "kvi_plan_create_fused",
+    "kvi_plan_launch", "kvi_plan_destroy", "kvi_plan_create_fused_io",
 )
 MAX_SHARED_QUERIES = 256
 NOALLOC_MAX_FACTS = 65536
@@ -114,6 +115,14 @@ def load_library(path: str | None = None):
         "kvi_trace_stages": (S, [P, i32]),
         "kvi_prepare_rope_ex": (S, [ctypes.POINTER(Rope), i32, i32]),
         "kvi_workspace_bytes_shared": (sz, [i32, i64, i32]),
+        "kvi_plan_create_fused": (S, [P, ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P, P, i32,
+                                      ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P, P, P,
+                                      sz, P]),
+        "kvi_plan_create_fused_io": (S, [P, ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P, P,
+                                         i32, ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P,
+                                         P, P, sz, P, P, P, sz, P, P, sz]),
+        "kvi_plan_launch": (S, [P, P]),
+        "kvi_plan_destroy": (S, [P]),
         "kvi_retrieve_topk_shared": (S, [ctypes.POINTER(StoreView), i32, P, i32, P, P, P, sz, P, P]),
         "kvi_retrieve_and_inject_shared": (S, [ctypes.POINTER(StoreView), i32, P, i32, P, P, P, i32,
                                                ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P,
@@ -319,6 +328,51 @@ def kvi_retrieve_and_inject_shared(store: StoreView, R: int, queries, k: int, st
         _ptr(table_lens), int(max_blocks), ctypes.byref(cache.struct), ctypes.byref(spec),
         _ptr(ids), _ptr(scores), _ptr(pos), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(status), _stream(stream)), "kvi_retrieve_and_inject_shared")
+
+
+class Plan:
+    """A fused call recorded once (kvi_plan_create_fused) and replayed with
+    launch(); the tensors it was created with must stay alive."""
+
+    def __init__(self, handle: int, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def launch(self, stream=None) -> None:
+        _check(load_library().kvi_plan_launch(self.handle, _stream(stream)), "kvi_plan_launch")
+
+    def close(self) -> None:
+        if self.handle:
+            _check(load_library().kvi_plan_destroy(self.handle), "kvi_plan_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def kvi_plan_create_fused(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,
+                          start_pos, block_tables, table_lens, max_blocks: int, cache: _Cache,
+                          spec: Rope, ids, scores, pos, ws, status=None, io=None) -> Plan:
+    """io = (h_in, d_in, d_out, h_out): pinned host and device byte tensors
+    whose copies the plan records around the fused call (optional)."""
+    h = ctypes.c_void_p()
+    lib = load_library()
+    common = (ctypes.byref(h), ctypes.byref(g), int(R), _ptr(stores_dev), int(max_facts), _ptr(queries),
+              int(k), _ptr(start_pos), _ptr(block_tables), _ptr(table_lens), int(max_blocks),
+              ctypes.byref(cache.struct), ctypes.byref(spec), _ptr(ids), _ptr(scores), _ptr(pos),
+              _ptr(ws), ws.numel() * ws.element_size(), _ptr(status))
+    if io is None:
+        _check(lib.kvi_plan_create_fused(*common), "kvi_plan_create_fused")
+    else:
+        h_in, d_in, d_out, h_out = io
+        _check(lib.kvi_plan_create_fused_io(*common, _ptr(h_in), _ptr(d_in), d_in.numel(),
+                                            _ptr(d_out), _ptr(h_out), d_out.numel()),
+               "kvi_plan_create_fused_io")
+    return Plan(h.value, (g, stores_dev, queries, start_pos, block_tables, table_lens, cache, spec,
+                          ids, scores, pos, ws, status, io))
 
 
 def kvi_retrieve_and_inject(g: Geometry, R: int, stores_dev, max_facts: int, queries, k: int,

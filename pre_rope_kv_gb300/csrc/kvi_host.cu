@@ -731,6 +731,115 @@ kvi_status kvi_retrieve_and_inject_ex(const kvi_geometry *g, int32_t R, const kv
     return KVI_OK;
 }
 
+}  // extern "C"
+
+struct kvi_plan_s {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+kvi_status kvi_plan_create_fused(kvi_plan *plan, const kvi_geometry *g, int32_t R,
+                                 const kvi_store_view *d_stores, int64_t max_facts,
+                                 const float *d_queries, int32_t k, const int32_t *d_start_pos,
+                                 const int32_t *d_block_tables, const int32_t *d_table_lens,
+                                 int32_t max_blocks, const kvi_paged_cache *cache, const kvi_rope *rope,
+                                 int32_t *d_ids, float *d_scores, int32_t *d_pos, void *d_ws,
+                                 size_t ws_bytes, int32_t *d_status)
+{
+    return kvi_plan_create_fused_io(plan, g, R, d_stores, max_facts, d_queries, k, d_start_pos,
+                                    d_block_tables, d_table_lens, max_blocks, cache, rope, d_ids, d_scores,
+                                    d_pos, d_ws, ws_bytes, d_status, nullptr, nullptr, 0, nullptr, nullptr,
+                                    0);
+}
+
+kvi_status kvi_plan_create_fused_io(kvi_plan *plan, const kvi_geometry *g, int32_t R,
+                                    const kvi_store_view *d_stores, int64_t max_facts,
+                                    const float *d_queries, int32_t k, const int32_t *d_start_pos,
+                                    const int32_t *d_block_tables, const int32_t *d_table_lens,
+                                    int32_t max_blocks, const kvi_paged_cache *cache, const kvi_rope *rope,
+                                    int32_t *d_ids, float *d_scores, int32_t *d_pos, void *d_ws,
+                                    size_t ws_bytes, int32_t *d_status, const void *h_in, void *d_in,
+                                    size_t in_bytes, const void *d_out, void *h_out, size_t out_bytes)
+{
+    if (!plan) return fail(KVI_ERR_INVALID_ARG, "plan is NULL");
+    if ((in_bytes && (!h_in || !d_in)) || (out_bytes && (!d_out || !h_out)))
+        return fail(KVI_ERR_INVALID_ARG, "a request copy needs both of its pointers");
+    *plan = nullptr;
+    if (t_trace_n == 3) return fail(KVI_ERR_INVALID_ARG, "turn tracing off before recording a plan");
+    kvi_status st = check_geometry(g);
+    if (st != KVI_OK) return st;
+    st = check_rope(rope);
+    if (st != KVI_OK) return st;
+    if (!cache || max_blocks < 1) return fail(KVI_ERR_INVALID_ARG, "cache is NULL or max_blocks < 1");
+    // the table is built now: building it is refused while recording
+    {
+        const float4 *table;
+        int32_t positions;
+        st = rope_get(*rope, g->head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), nullptr,
+                      &table, &positions);
+        if (st != KVI_OK) return st;
+    }
+    // kernel attributes are set once per device, outside the recording
+    KVI_CUDA(prepare_retrieval_kernels());
+    KVI_CUDA(prepare_inject_kernel());
+    cudaStream_t s = nullptr;
+    KVI_CUDA(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(s);
+        return fail(KVI_ERR_CUDA, "cudaStreamBeginCapture: %s", cudaGetErrorString(e));
+    }
+    if (in_bytes) {
+        e = cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) st = fail(KVI_ERR_CUDA, "request input copy: %s", cudaGetErrorString(e));
+    }
+    if (st == KVI_OK)
+        st = kvi_retrieve_and_inject_ex(g, R, d_stores, max_facts, d_queries, k, d_start_pos,
+                                        d_block_tables, d_table_lens, max_blocks, cache, rope, d_ids,
+                                        d_scores, d_pos, d_ws, ws_bytes, d_status,
+                                        reinterpret_cast<kvi_stream_t>(s));
+    if (st == KVI_OK && out_bytes) {
+        e = cudaMemcpyAsync(h_out, d_out, out_bytes, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) st = fail(KVI_ERR_CUDA, "request output copy: %s", cudaGetErrorString(e));
+    }
+    e = cudaStreamEndCapture(s, &graph);
+    cudaStreamDestroy(s);
+    if (st != KVI_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    if (e != cudaSuccess) return fail(KVI_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return fail(KVI_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
+    }
+    *plan = new kvi_plan_s{graph, exec};
+    return KVI_OK;
+}
+
+kvi_status kvi_plan_launch(kvi_plan plan, kvi_stream_t stream)
+{
+    if (!plan) return fail(KVI_ERR_INVALID_ARG, "plan is NULL");
+    KVI_CUDA(cudaGraphLaunch(plan->exec, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+kvi_status kvi_plan_destroy(kvi_plan plan)
+{
+    if (!plan) return KVI_OK;
+    const cudaError_t a = cudaGraphExecDestroy(plan->exec);
+    const cudaError_t b = cudaGraphDestroy(plan->graph);
+    delete plan;
+    if (a != cudaSuccess) return fail(KVI_ERR_CUDA, "cudaGraphExecDestroy: %s", cudaGetErrorString(a));
+    if (b != cudaSuccess) return fail(KVI_ERR_CUDA, "cudaGraphDestroy: %s", cudaGetErrorString(b));
+    return KVI_OK;
+}
+
 size_t kvi_workspace_bytes_shared(int32_t R, int64_t n_facts, int32_t k)
 {
     if (R < 1 || R > KVI_MAX_SHARED_QUERIES || n_facts < 1 || n_facts > 0x7fffffff || k < 1 ||

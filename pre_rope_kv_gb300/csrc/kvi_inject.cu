@@ -746,6 +746,8 @@ inject_kernel(const __grid_constant__ InjectParams p)
 
 }  // namespace
 
+cudaError_t prepare_inject_kernel() { return smem_opt_in(inject_kernel, (int)sizeof(InjSmem)); }
+
 cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl)
 {
     DeviceInfo di;

@@ -166,6 +166,11 @@ struct RescoreParams {
 };
 cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s);
 
+// One-time per-device kernel attributes (shared-memory opt-in), made ahead
+// of a stream capture.
+cudaError_t prepare_retrieval_kernels();
+cudaError_t prepare_inject_kernel();
+
 // Launchers (return the CUDA error of the launch).  `pdl` launches the kernel
 // with programmatic stream serialization so that it can start while the
 // previous kernel of the stream drains; the kernel waits for that kernel's

@@ -1275,6 +1275,13 @@ cudaError_t launch_score(const ScoreParams &p, cudaStream_t s)
     return launch_score_nv<0>(p, s);
 }
 
+cudaError_t prepare_retrieval_kernels()
+{
+    cudaError_t e = smem_opt_in(score_ring_kernel, (int)sizeof(ScoreRingSmem));
+    if (e != cudaSuccess) return e;
+    return smem_opt_in(select_kernel, (int)sizeof(SelectSmem));
+}
+
 cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl)
 {
     static_assert(sizeof(SelectSmem) <= 227 * 1024, "select smem");
