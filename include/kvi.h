@@ -75,7 +75,8 @@ typedef enum {
     KVI_ERR_OUT_OF_RANGE = 2, /* fact id, store row, block id or position out of range */
     KVI_ERR_CAPACITY = 3,     /* the facts do not fit the request's block table */
     KVI_ERR_CUDA = 4,         /* a CUDA runtime call failed (see kvi_last_error) */
-    KVI_ERR_TIMEOUT = 5       /* a kernel's bounded wait for its own copies expired */
+    KVI_ERR_TIMEOUT = 5,      /* a kernel's bounded wait for its own copies expired */
+    KVI_ERR_IO = 6            /* a store file could not be written or read, or is not a valid one */
 } kvi_status;
 
 /* Limits of this build. */
@@ -404,6 +405,73 @@ KVI_API kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store,
                                              const float *d_query, int32_t k,
                                              int32_t *d_ids, float *d_scores,
                                              kvi_stream_t stream);
+
+/* Store files.  The paper encodes a user's memory facts offline into a
+ * long-lived store of pre-RoPE K/V and embeddings, which may sit in host
+ * DRAM when it outgrows HBM (the review's Summary: facts are encoded
+ * offline, and CPU offload of the KV store costs a few ms of TTFT).  These
+ * calls persist a store and load it back into HBM or pinned host memory.
+ *
+ * File format, version 1 (all integers little-endian; every section starts
+ * at a multiple of 4096 bytes and the gaps are zero):
+ *   [0, 8)     magic "KVISTORE"
+ *   [8, 12)    uint32 version = 1
+ *   [12, 16)   uint32 header bytes = 128
+ *   [16, 32)   int32 layers, kv_heads, head_dim, embed_dim
+ *   [32, 40)   int64 n_facts N
+ *   [40, 48)   int64 n_tokens T (rows per (layer, K|V) plane)
+ *   [48, 88)   uint64 file offsets of the sections fact_start, fact_len,
+ *              emb, kv, and the file size
+ *   [88, 96)   uint64 extents hash: FNV-1a 64 over the bytes of the
+ *              fact_start section followed by those of the fact_len section
+ *   [96, 104)  uint64 payload hash (below) over the emb section followed by
+ *              the kv section
+ *   [104, 112) uint64 header hash: FNV-1a 64 over bytes [0, 104)
+ *   [112, 128) zero
+ * Sections: fact_start int64 [N]; fact_len int32 [N]; emb float32 [N][E];
+ * kv bf16 [L][2][T][H][D], exactly as in kvi_store_view.
+ * FNV-1a 64: h = 0xcbf29ce484222325; per byte b: h = (h ^ b) * 0x100000001b3
+ * (mod 2^64).  Payload hash: the payload read as little-endian uint64 words
+ * w_0, w_1, ... goes to four lanes (lane j takes the words with index = j
+ * mod 4); lane j starts at 0xcbf29ce484222325 + j and takes each word as
+ * h_j = (h_j ^ w) * 0x100000001b3; the hash is
+ * h_0 ^ rotl(h_1, 16) ^ rotl(h_2, 32) ^ rotl(h_3, 48). */
+typedef struct {
+    kvi_geometry g;
+    int64_t n_facts;  /* N */
+    int64_t n_tokens; /* T */
+    size_t kv_bytes;  /* L * 2 * T * H * D * 2 */
+    size_t emb_bytes; /* N * E * 4 */
+} kvi_store_file_info;
+
+/* Write *store to a new file at path (replaced if it exists).  The store is
+ * written as it is: all n_tokens rows of kv, including rows no fact
+ * references.  kv may be device memory or, with KVI_STORE_KV_HOST, host
+ * memory; emb, fact_start and fact_len are device memory.  Synchronous: the
+ * data is read with blocking copies, so the work that writes the store must
+ * have finished (synchronise its stream first).  Errors:
+ * KVI_ERR_INVALID_ARG (a bad view or geometry), KVI_ERR_IO (the file cannot
+ * be created or written; a partial file is removed), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_store_save(const char *path, const kvi_store_view *store);
+
+/* Read and check the header of a store file (host only, no CUDA call), so
+ * that the caller can size the buffers for kvi_store_load.  Errors:
+ * KVI_ERR_INVALID_ARG (NULL argument), KVI_ERR_IO (the file cannot be read,
+ * is not a version-1 store file, its header hash does not match, or its
+ * size does not match the header). */
+KVI_API kvi_status kvi_store_file_info_read(const char *path, kvi_store_file_info *info);
+
+/* Load the store file at path into caller-owned buffers sized by
+ * kvi_store_file_info_read: kv (kv_bytes; device memory, or pinned host
+ * memory when flags & KVI_STORE_KV_HOST), emb (device, emb_bytes),
+ * fact_start (device, N int64) and fact_len (device, N int32).  The fact
+ * extents are checked (start >= 0, length >= 0, start + length <= T) and
+ * both hashes are verified.  Synchronous.  Errors: KVI_ERR_INVALID_ARG
+ * (NULL or misaligned buffer, unknown flag), KVI_ERR_IO (unreadable file,
+ * bad header, hash mismatch or bad extent; the buffers then hold
+ * unspecified data), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_store_load(const char *path, void *kv, float *emb, int64_t *fact_start,
+                                  int32_t *fact_len, uint32_t flags);
 
 /* Tracing: when n_events == 3, the calling thread's next
  * kvi_retrieve_and_inject calls record events[0] before the first kernel,

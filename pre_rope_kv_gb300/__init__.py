@@ -22,4 +22,5 @@ from ._binding import (  # noqa: F401
     ROPE_PAIR_HALF, ROPE_PAIR_INTERLEAVED, ROPE_SCALE_NONE, ROPE_SCALE_LLAMA3,
     MAX_SHARED_QUERIES, kvi_workspace_bytes_shared, kvi_retrieve_topk_shared,
     kvi_retrieve_and_inject_shared, STORE_KV_HOST, Plan, kvi_plan_create_fused,
+    ERR_IO, StoreFileInfo, kvi_store_save, kvi_store_file_info_read, kvi_store_load, load_store,
 )

@@ -23,6 +23,7 @@ ERR_OUT_OF_RANGE = 2
 ERR_CAPACITY = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
+ERR_IO = 6
 MAX_REQUESTS = 4096
 
 MAX_LAYERS = 128
@@ -35,7 +36,8 @@ EXPORTED_SYMBOLS = (
     "kvi_status_str", "kvi_last_error", "kvi_retrieve_topk_noalloc", "kvi_prepare_rope_ex",
     "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex", "kvi_workspace_bytes_shared",
     "kvi_retrieve_topk_shared", "kvi_retrieve_and_inject_shared", "kvi_plan_create_fused",
-    "kvi_plan_launch", "kvi_plan_destroy", "kvi_plan_create_fused_io",
+    "kvi_plan_launch", "kvi_plan_destroy", "kvi_plan_create_fused_io", "kvi_store_save",
+    "kvi_store_file_info_read", "kvi_store_load",
 )
 MAX_SHARED_QUERIES = 256
 NOALLOC_MAX_FACTS = 65536
@@ -79,6 +81,11 @@ class Rope(ctypes.Structure):
                 ("original_max_positions", ctypes.c_double),
                 ("cos_table", ctypes.c_void_p), ("sin_table", ctypes.c_void_p),
                 ("table_positions", ctypes.c_int32), ("table_id", ctypes.c_int64)]
+
+
+class StoreFileInfo(ctypes.Structure):
+    _fields_ = [("g", Geometry), ("n_facts", ctypes.c_int64), ("n_tokens", ctypes.c_int64),
+                ("kv_bytes", ctypes.c_size_t), ("emb_bytes", ctypes.c_size_t)]
 
 
 class PagedCache(ctypes.Structure):
@@ -133,6 +140,9 @@ def load_library(path: str | None = None):
                                            P, i32, ctypes.POINTER(PagedCache),
                                            ctypes.POINTER(Rope), P, P, P, P, sz, P, P]),
         "kvi_retrieve_topk_noalloc": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P]),
+        "kvi_store_save": (S, [ctypes.c_char_p, ctypes.POINTER(StoreView)]),
+        "kvi_store_file_info_read": (S, [ctypes.c_char_p, ctypes.POINTER(StoreFileInfo)]),
+        "kvi_store_load": (S, [ctypes.c_char_p, P, P, P, P, ctypes.c_uint32]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -385,6 +395,44 @@ def kvi_retrieve_and_inject(g: Geometry, R: int, stores_dev, max_facts: int, que
         ctypes.byref(cache.struct), float(rope_theta), _ptr(ids), _ptr(scores), _ptr(pos),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
         "kvi_retrieve_and_inject")
+
+
+def kvi_store_save(path: str, store: StoreView) -> None:
+    lib = load_library()
+    _check(lib.kvi_store_save(os.fsencode(path), ctypes.byref(store)), "kvi_store_save")
+
+
+def kvi_store_file_info_read(path: str) -> StoreFileInfo:
+    lib = load_library()
+    info = StoreFileInfo()
+    _check(lib.kvi_store_file_info_read(os.fsencode(path), ctypes.byref(info)),
+           "kvi_store_file_info_read")
+    return info
+
+
+def kvi_store_load(path: str, kv, emb, fact_start, fact_len, kv_host: bool = False) -> None:
+    lib = load_library()
+    _check(lib.kvi_store_load(os.fsencode(path), _ptr(kv), _ptr(emb), _ptr(fact_start),
+                              _ptr(fact_len), STORE_KV_HOST if kv_host else 0), "kvi_store_load")
+
+
+def load_store(path: str, kv_host: bool = False):
+    """Allocate torch buffers for the store file at path and load it:
+    returns (Geometry, kv, emb, fact_start, fact_len); kv is a pinned host
+    tensor when kv_host, else on the current CUDA device."""
+    import torch
+    info = kvi_store_file_info_read(path)
+    g = info.g
+    shape = (g.layers, 2, info.n_tokens, g.kv_heads, g.head_dim)
+    if kv_host:
+        kv = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    else:
+        kv = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    emb = torch.empty((info.n_facts, g.embed_dim), dtype=torch.float32, device="cuda")
+    fs = torch.empty(info.n_facts, dtype=torch.int64, device="cuda")
+    fl = torch.empty(info.n_facts, dtype=torch.int32, device="cuda")
+    kvi_store_load(path, kv, emb, fs, fl, kv_host=kv_host)
+    return Geometry(g.layers, g.kv_heads, g.head_dim, g.embed_dim), kv, emb, fs, fl
 
 
 def kvi_trace_stages(events) -> None:

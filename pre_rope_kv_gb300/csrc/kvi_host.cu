@@ -323,6 +323,8 @@ cudaError_t device_info(DeviceInfo *out)
 kvi_status set_error(kvi_status s, const char *msg) { return fail(s, "%s", msg); }
 
 kvi_status check_retrieval_store(const kvi_store_view *s) { return check_store(s, true, false); }
+kvi_status check_full_store(const kvi_store_view *s) { return check_store(s, true, true); }
+kvi_status check_store_geometry(const kvi_geometry *g) { return check_geometry(g); }
 
 cudaError_t smem_opt_in_raw(const void *kernel, int bytes)
 {
@@ -410,6 +412,7 @@ const char *kvi_status_str(kvi_status s)
     case KVI_ERR_CAPACITY: return "facts do not fit the block table";
     case KVI_ERR_CUDA: return "CUDA error";
     case KVI_ERR_TIMEOUT: return "a kernel wait timed out";
+    case KVI_ERR_IO: return "store file error";
     }
     return "unknown status";
 }

@@ -184,6 +184,10 @@ cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl);
 kvi_status set_error(kvi_status s, const char *msg);
 // The store checks kvi_retrieve_topk applies (geometry, n_facts, emb).
 kvi_status check_retrieval_store(const kvi_store_view *s);
+// The checks of a store used for retrieval and injection (emb, kv, extents).
+kvi_status check_full_store(const kvi_store_view *s);
+// The geometry limits of this build (records a message on failure).
+kvi_status check_store_geometry(const kvi_geometry *g);
 
 // Device facts cached per device (SM count).
 struct DeviceInfo {
