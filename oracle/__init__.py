@@ -94,6 +94,11 @@ def _load():
             P, i32, i32, i32, i64, P, P, i64, P, P, i32, P, i32, i32, i32, P, i32, P, P, i64,
             P, P]
         lib.kvo_inject_expected_ex.restype = ctypes.c_int
+        lib.kvo_graph_build.argtypes = [P, i64, i64, i32, P]
+        lib.kvo_graph_build.restype = ctypes.c_int
+        lib.kvo_graph_search.argtypes = [P, P, i64, i64, P, i32, P, i32, i32, i32, i32, i32, P,
+                                         P, P]
+        lib.kvo_graph_search.restype = i32
         _lib = lib
         return lib
 
@@ -309,3 +314,37 @@ def request(q, emb, k, kv_bits, fact_start, fact_len, start, theta, max_tokens):
     if T < 0:
         raise ValueError("oracle request failed")
     return sel, pos, k_out[:T], v_out[:T]
+
+
+def graph_build(emb: np.ndarray, degree: int) -> np.ndarray:
+    """Graph index: each fact's `degree` most similar other facts, exact,
+    in (score desc, id asc) order -> int32 [N][degree]."""
+    emb = _c(emb, np.float32)
+    n, e = emb.shape
+    nbr = np.empty((n, max(degree, 0)), np.int32)
+    rc = _load().kvo_graph_build(_p(emb), n, e, int(degree), _p(nbr))
+    if rc != OK:
+        raise ValueError(f"oracle graph_build: bad argument (n={n}, degree={degree})")
+    return nbr
+
+
+def graph_search(q: np.ndarray, emb: np.ndarray, nbr: np.ndarray, seeds, beam: int, width: int,
+                 max_iters: int, k: int):
+    """Best-first beam search of one query over the graph nbr [N][d] from
+    the given seed ids.  Returns (ids int32 [k], scores float64 [k], count,
+    iterations, facts scored); ids past `count` are -1."""
+    q = _c(q, np.float32)
+    emb = _c(emb, np.float32)
+    nbr = _c(nbr, np.int32)
+    seeds = _c(np.atleast_1d(seeds), np.int32)
+    n, e = emb.shape
+    assert q.shape == (e,) and nbr.shape[0] == n
+    sel = np.empty(max(k, 1), np.int32)
+    sc = np.empty(max(k, 1), np.float64)
+    stats = np.zeros(2, np.int64)
+    cnt = _load().kvo_graph_search(_p(q), _p(emb), n, e, _p(nbr), nbr.shape[1], _p(seeds),
+                                   seeds.shape[0], int(beam), int(width), int(max_iters), int(k),
+                                   _p(sel), _p(sc), _p(stats))
+    if cnt < 0:
+        raise ValueError("oracle graph_search: bad argument")
+    return sel[:k], sc[:k], int(cnt), int(stats[0]), int(stats[1])

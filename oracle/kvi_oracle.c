@@ -421,3 +421,139 @@ void kvo_slots(const int64_t *p, int64_t n, const int32_t *block_table,
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Graph index.  The review's Summary retrieves facts through a GPU ANN index
+ * (Jasper) instead of a scan, and its Axiom & Free-Parameter Ledger fixes
+ * the index at 64 graph neighbours and beam width 64; the reference list
+ * cites CAGRA, a GPU graph index searched best-first from a candidate
+ * buffer.  Readings (the pages give nothing more):
+ *   - the graph links each fact to its `d` most similar other facts, exact,
+ *     under the same (score descending, id ascending) order as the top-k;
+ *   - the search keeps the best `beam` scored facts, expands the best
+ *     `width` not yet expanded per iteration, scores every neighbour at most
+ *     once (visited set) and starts from caller-given seed facts.
+ * ---------------------------------------------------------------------- */
+
+/* Graph build.  nbr[i][0..d) = the d facts j != i with the largest
+ * s_ij = <e_i, e_j> (float64, summed left to right), in (score descending,
+ * id ascending) order.  Requires 1 <= d < n. */
+int kvo_graph_build(const float *emb, int64_t n, int64_t e, int32_t d, int32_t *nbr)
+{
+    if (n < 2 || d < 1 || (int64_t)d >= n) return KVO_BAD_ARG;
+    double *s = (double *)malloc((size_t)n * sizeof *s);
+    kvo_key *keys = (kvo_key *)malloc((size_t)n * sizeof *keys);
+    if (!s || !keys) { free(s); free(keys); return KVO_BAD_ARG; }
+    for (int64_t i = 0; i < n; ++i) {
+        kvo_scores(emb + i * e, emb, n, e, s);
+        int64_t m = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            if (j == i) continue;
+            keys[m].s = s[j];
+            keys[m].id = (int32_t)j;
+            ++m;
+        }
+        qsort(keys, (size_t)m, sizeof *keys, kvo_key_cmp);
+        for (int32_t r = 0; r < d; ++r) nbr[i * d + r] = keys[r].id;
+    }
+    free(s);
+    free(keys);
+    return KVO_OK;
+}
+
+typedef struct { kvo_key key; int expanded; } kvo_cand;
+
+static int kvo_cand_cmp(const void *a, const void *b)
+{
+    return kvo_key_cmp(&((const kvo_cand *)a)->key, &((const kvo_cand *)b)->key);
+}
+
+static double kvo_dot(const float *q, const float *row, int64_t e)
+{
+    double s = 0.0;
+    for (int64_t j = 0; j < e; ++j)
+        s += (double)q[j] * (double)row[j];
+    return s;
+}
+
+/* Graph search for one query q over the graph nbr[n][d].
+ *   1. Each seed not seen before is scored; the beam C is the best `beam`
+ *      of them in (score descending, id ascending) order, all unexpanded.
+ *   2. At most max_iters times: the first `width` unexpanded entries of C
+ *      are the parents (if there are none, stop) and are marked expanded;
+ *      every neighbour of the parents (parents in C order, neighbours in
+ *      list order) not seen before is scored; C becomes the best `beam` of
+ *      C and the new facts.
+ *   3. The result is the first k entries of C.
+ * Every fact is scored at most once, so C never holds an id twice.  Writes
+ * sel[0..k) and score[0..k) (-1 and 0 past the end of a short C) and
+ * stats[0] = iterations run, stats[1] = facts scored.  Returns the number of
+ * results, or -1 for bad arguments (k < 1 or > beam, width outside [1, 1024],
+ * max_iters < 0, a seed or neighbour id outside [0, n)). */
+int32_t kvo_graph_search(const float *q, const float *emb, int64_t n, int64_t e,
+                         const int32_t *nbr, int32_t d, const int32_t *seeds,
+                         int32_t n_seeds, int32_t beam, int32_t width, int32_t max_iters,
+                         int32_t k, int32_t *sel, double *score, int64_t *stats)
+{
+    if (k < 1 || beam < k || width < 1 || width > 1024 || max_iters < 0 || d < 1 || n_seeds < 1 ||
+        n < 1)
+        return -1;
+    unsigned char *seen = (unsigned char *)calloc((size_t)n, 1);
+    const int64_t cap = (int64_t)beam + (int64_t)n_seeds + (int64_t)width * d;
+    kvo_cand *c = (kvo_cand *)malloc((size_t)cap * sizeof *c);
+    if (!seen || !c) { free(seen); free(c); return -1; }
+    int64_t nc = 0, scored = 0, iters = 0;
+    int32_t result = -1;
+    for (int32_t i = 0; i < n_seeds; ++i) {
+        const int32_t f = seeds[i];
+        if (f < 0 || (int64_t)f >= n) goto done;
+        if (seen[f]) continue;
+        seen[f] = 1;
+        c[nc].key.s = kvo_dot(q, emb + (int64_t)f * e, e);
+        c[nc].key.id = f;
+        c[nc].expanded = 0;
+        ++nc;
+        ++scored;
+    }
+    qsort(c, (size_t)nc, sizeof *c, kvo_cand_cmp);
+    if (nc > beam) nc = beam;
+    while (iters < max_iters) {
+        int32_t parents[1024];
+        int32_t np = 0;
+        for (int64_t i = 0; i < nc && np < width && np < 1024; ++i) {
+            if (!c[i].expanded) {
+                c[i].expanded = 1;
+                parents[np++] = c[i].key.id;
+            }
+        }
+        if (np == 0) break;
+        ++iters;
+        int64_t m = nc;
+        for (int32_t pi = 0; pi < np; ++pi) {
+            for (int32_t r = 0; r < d; ++r) {
+                const int32_t f = nbr[(int64_t)parents[pi] * d + r];
+                if (f < 0 || (int64_t)f >= n) goto done;
+                if (seen[f]) continue;
+                seen[f] = 1;
+                c[m].key.s = kvo_dot(q, emb + (int64_t)f * e, e);
+                c[m].key.id = f;
+                c[m].expanded = 0;
+                ++m;
+                ++scored;
+            }
+        }
+        qsort(c, (size_t)m, sizeof *c, kvo_cand_cmp);
+        nc = m < beam ? m : beam;
+    }
+    result = (int32_t)(nc < k ? nc : k);
+    for (int32_t j = 0; j < k; ++j) {
+        sel[j] = j < result ? c[j].key.id : -1;
+        score[j] = j < result ? c[j].key.s : 0.0;
+    }
+    stats[0] = iters;
+    stats[1] = scored;
+done:
+    free(seen);
+    free(c);
+    return result;
+}

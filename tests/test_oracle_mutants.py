@@ -51,7 +51,16 @@ MUTANTS = {
         "if (lambda < orig / high) {", "if (lambda < orig / low) {"),
     "table_rotation_sign": (
         "y[ia] = x[ia] * c[i] - x[ib] * sn[i];", "y[ia] = x[ia] * c[i] + x[ib] * sn[i];"),
+    "graph_keeps_self": ("            if (j == i) continue;\n", "            if (j == i && n < 0) continue;\n"),
+    "search_forgets_visited": ("                if (seen[f]) continue;\n", "                if (seen[f] && n < 0) continue;\n"),
+    "search_expands_the_worst": (
+        "for (int64_t i = 0; i < nc && np < width && np < 1024; ++i) {",
+        "for (int64_t i = nc - 1; i >= 0 && np < width && np < 1024; --i) {"),
+    "search_never_marks_expanded": ("                c[i].expanded = 1;\n", "\n"),
+    "search_seeds_not_cut_to_beam": ("    if (nc > beam) nc = beam;\n", "\n"),
+    "search_beam_one_short": ("nc = m < beam ? m : beam;", "nc = m < beam - 1 ? m : beam - 1;"),
 }
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_graph_pins.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -66,6 +75,6 @@ def test_pins_catch_mutant(name, tmp_path):
                            "-fPIC", "-o", str(lib), str(mut), "-lm"])
     env = dict(os.environ, KVI_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
