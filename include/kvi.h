@@ -406,6 +406,75 @@ KVI_API kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store,
                                              int32_t *d_ids, float *d_scores,
                                              kvi_stream_t stream);
 
+/* Graph index.  The review's Summary retrieves facts at serving time
+ * through a GPU ANN index (Jasper) rather than a scan, and its Axiom &
+ * Free-Parameter Ledger sets the index at 64 graph neighbours and beam width
+ * 64; the reference list cites CAGRA, a GPU graph index searched best-first
+ * from a buffer of candidates.  Readings of this library (the pages give
+ * nothing more):
+ *   - the graph links each fact to its `degree` most similar other facts,
+ *     exactly (the same score and order as kvi_retrieve_topk: score
+ *     descending, ties to the lower id), as int32 graph[N][degree];
+ *   - the search keeps a beam of the best `beam` facts scored so far, each
+ *     marked expanded or not.  It scores the query's seed facts, then, up to
+ *     max_iters times, expands the best `width` unexpanded facts of the beam
+ *     (none left: it stops), scores every neighbour of theirs that it has not
+ *     scored before and keeps the best `beam` of the beam and the new facts.
+ *     No fact is scored twice (an exact visited set).  The result is the
+ *     first k facts of the beam, in rank order;
+ *   - the seeds are the caller's (e.g. drawn at random), so that a search is
+ *     a deterministic function of its inputs.
+ * The search is approximate retrieval: its recall against the exact top-k
+ * depends on the data, the graph and the parameters. */
+#define KVI_MAX_GRAPH_DEGREE 128  /* degree */
+#define KVI_MAX_GRAPH_BEAM 256    /* beam */
+#define KVI_MAX_GRAPH_FRONTIER 512 /* n_seeds, and width * degree */
+
+/* Device workspace of kvi_graph_build for a store of n_facts facts (0 for
+ * arguments outside the limits). */
+KVI_API size_t kvi_graph_build_workspace_bytes(int64_t n_facts, int32_t degree);
+
+/* Build the graph of *store (its embeddings; kv is not read) into d_graph,
+ * int32 [n_facts][degree], with 1 <= degree <= min(KVI_MAX_GRAPH_DEGREE,
+ * n_facts - 1).  Each row's neighbours come from the exact shared-store
+ * retrieval (kvi_retrieve_topk_shared) of its own embedding, degree + 1
+ * facts, without the row's own fact; batches of KVI_MAX_SHARED_QUERIES rows
+ * are enqueued on `stream` one after another.  d_ws: device,
+ * kvi_graph_build_workspace_bytes, 256-byte aligned.  Errors:
+ * KVI_ERR_INVALID_ARG, KVI_ERR_CUDA; device-side errors in *d_status. */
+KVI_API kvi_status kvi_graph_build(const kvi_store_view *store, int32_t degree, int32_t *d_graph,
+                                   void *d_ws, size_t ws_bytes, int32_t *d_status,
+                                   kvi_stream_t stream);
+
+typedef struct {
+    int32_t beam;      /* k <= beam <= KVI_MAX_GRAPH_BEAM */
+    int32_t width;     /* >= 1, width * degree <= KVI_MAX_GRAPH_FRONTIER */
+    int32_t max_iters; /* >= 0 */
+    int32_t n_seeds;   /* 1 .. KVI_MAX_GRAPH_FRONTIER seeds per query */
+} kvi_graph_search_params;
+
+/* Device workspace of kvi_graph_search: one visited bitmap of n_facts bits
+ * per query (0 for arguments outside the limits). */
+KVI_API size_t kvi_graph_search_workspace_bytes(int32_t R, int64_t n_facts);
+
+/* Search the graph d_graph [n_facts][degree] (as kvi_graph_build writes it,
+ * or any graph of valid ids) for R queries d_queries [R][E] from the seeds
+ * d_seeds [R][n_seeds] (fact ids).  Outputs, device: d_ids [R][k] and
+ * d_scores [R][k] in rank order (-1 and NaN past a query's result count);
+ * d_count [R] (may be NULL), the number of results, k unless the beam held
+ * fewer facts; d_stats [R][2] (may be NULL), the iterations run and the
+ * facts scored.  One CTA per query; 1 <= R <= 65535.  d_ws: device,
+ * kvi_graph_search_workspace_bytes, 256-byte aligned.  Errors (host):
+ * KVI_ERR_INVALID_ARG for bad pointers or parameters; a seed or graph id
+ * outside [0, n_facts) is recorded as KVI_ERR_OUT_OF_RANGE in *d_status and
+ * skipped. */
+KVI_API kvi_status kvi_graph_search(const kvi_store_view *store, const int32_t *d_graph,
+                                    int32_t degree, int32_t R, const float *d_queries,
+                                    const int32_t *d_seeds, const kvi_graph_search_params *params,
+                                    int32_t k, int32_t *d_ids, float *d_scores, int32_t *d_count,
+                                    int32_t *d_stats, void *d_ws, size_t ws_bytes,
+                                    int32_t *d_status, kvi_stream_t stream);
+
 /* Store files.  The paper encodes a user's memory facts offline into a
  * long-lived store of pre-RoPE K/V and embeddings, which may sit in host
  * DRAM when it outgrows HBM (the review's Summary: facts are encoded

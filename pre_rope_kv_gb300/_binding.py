@@ -37,8 +37,12 @@ EXPORTED_SYMBOLS = (
     "kvi_inject_paged_ex", "kvi_retrieve_and_inject_ex", "kvi_workspace_bytes_shared",
     "kvi_retrieve_topk_shared", "kvi_retrieve_and_inject_shared", "kvi_plan_create_fused",
     "kvi_plan_launch", "kvi_plan_destroy", "kvi_plan_create_fused_io", "kvi_store_save",
-    "kvi_store_file_info_read", "kvi_store_load",
+    "kvi_store_file_info_read", "kvi_store_load", "kvi_graph_build_workspace_bytes",
+    "kvi_graph_build", "kvi_graph_search_workspace_bytes", "kvi_graph_search",
 )
+MAX_GRAPH_DEGREE = 128
+MAX_GRAPH_BEAM = 256
+MAX_GRAPH_FRONTIER = 512
 MAX_SHARED_QUERIES = 256
 NOALLOC_MAX_FACTS = 65536
 
@@ -86,6 +90,11 @@ class Rope(ctypes.Structure):
 class StoreFileInfo(ctypes.Structure):
     _fields_ = [("g", Geometry), ("n_facts", ctypes.c_int64), ("n_tokens", ctypes.c_int64),
                 ("kv_bytes", ctypes.c_size_t), ("emb_bytes", ctypes.c_size_t)]
+
+
+class GraphSearchParams(ctypes.Structure):
+    _fields_ = [("beam", ctypes.c_int32), ("width", ctypes.c_int32), ("max_iters", ctypes.c_int32),
+                ("n_seeds", ctypes.c_int32)]
 
 
 class PagedCache(ctypes.Structure):
@@ -143,6 +152,11 @@ def load_library(path: str | None = None):
         "kvi_store_save": (S, [ctypes.c_char_p, ctypes.POINTER(StoreView)]),
         "kvi_store_file_info_read": (S, [ctypes.c_char_p, ctypes.POINTER(StoreFileInfo)]),
         "kvi_store_load": (S, [ctypes.c_char_p, P, P, P, P, ctypes.c_uint32]),
+        "kvi_graph_build_workspace_bytes": (sz, [i64, i32]),
+        "kvi_graph_build": (S, [ctypes.POINTER(StoreView), i32, P, P, sz, P, P]),
+        "kvi_graph_search_workspace_bytes": (sz, [i32, i64]),
+        "kvi_graph_search": (S, [ctypes.POINTER(StoreView), P, i32, i32, P, P,
+                                 ctypes.POINTER(GraphSearchParams), i32, P, P, P, P, P, sz, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -433,6 +447,37 @@ def load_store(path: str, kv_host: bool = False):
     fl = torch.empty(info.n_facts, dtype=torch.int32, device="cuda")
     kvi_store_load(path, kv, emb, fs, fl, kv_host=kv_host)
     return Geometry(g.layers, g.kv_heads, g.head_dim, g.embed_dim), kv, emb, fs, fl
+
+
+def kvi_graph_build_workspace_bytes(n_facts: int, degree: int) -> int:
+    return load_library().kvi_graph_build_workspace_bytes(int(n_facts), int(degree))
+
+
+def kvi_graph_build(store: StoreView, degree: int, graph, ws, status=None, stream=None) -> None:
+    lib = load_library()
+    nb = ws.numel() * ws.element_size()
+    _check(lib.kvi_graph_build(ctypes.byref(store), int(degree), _ptr(graph), _ptr(ws), nb,
+                               _ptr(status), _stream(stream)), "kvi_graph_build")
+
+
+def kvi_graph_search_workspace_bytes(R: int, n_facts: int) -> int:
+    return load_library().kvi_graph_search_workspace_bytes(int(R), int(n_facts))
+
+
+def graph_search_params(beam: int = 64, width: int = 1, max_iters: int = 1000,
+                        n_seeds: int = 64) -> GraphSearchParams:
+    return GraphSearchParams(int(beam), int(width), int(max_iters), int(n_seeds))
+
+
+def kvi_graph_search(store: StoreView, graph, degree: int, R: int, queries, seeds,
+                     params: GraphSearchParams, k: int, ids, scores, ws, count=None, stats=None,
+                     status=None, stream=None) -> None:
+    lib = load_library()
+    nb = ws.numel() * ws.element_size()
+    _check(lib.kvi_graph_search(ctypes.byref(store), _ptr(graph), int(degree), int(R),
+                                _ptr(queries), _ptr(seeds), ctypes.byref(params), int(k),
+                                _ptr(ids), _ptr(scores), _ptr(count), _ptr(stats), _ptr(ws), nb,
+                                _ptr(status), _stream(stream)), "kvi_graph_search")
 
 
 def kvi_trace_stages(events) -> None:

@@ -1029,3 +1029,137 @@ kvi_status kvi_retrieve_and_inject_shared(const kvi_store_view *store, int32_t R
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------- graph index
+
+namespace {
+
+struct GraphBuildWs {
+    SharedWs shared;
+    size_t ids, scores, total;
+};
+
+GraphBuildWs graph_build_layout(int64_t n_facts, int32_t degree)
+{
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    GraphBuildWs x{};
+    const int32_t R = (int32_t)std::min<int64_t>(KVI_MAX_SHARED_QUERIES, n_facts);
+    const int32_t k = degree + 1;
+    x.shared = shared_layout(R, n_facts, k);
+    size_t at = up(x.shared.total);
+    x.ids = at;    at = up(at + (size_t)R * k * 4);
+    x.scores = at; at = up(at + (size_t)R * k * 4);
+    x.total = at;
+    return x;
+}
+
+bool graph_build_args_ok(int64_t n_facts, int32_t degree)
+{
+    return n_facts >= 2 && n_facts <= 0x7fffffff && degree >= 1 && degree <= KVI_MAX_GRAPH_DEGREE &&
+           (int64_t)degree < n_facts;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvi_graph_build_workspace_bytes(int64_t n_facts, int32_t degree)
+{
+    if (!graph_build_args_ok(n_facts, degree)) return 0;
+    return graph_build_layout(n_facts, degree).total;
+}
+
+kvi_status kvi_graph_build(const kvi_store_view *store, int32_t degree, int32_t *d_graph, void *d_ws,
+                           size_t ws_bytes, int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_store(store, true, false);
+    if (st != KVI_OK) return st;
+    const int64_t N = store->n_facts;
+    if (!graph_build_args_ok(N, degree))
+        return fail(KVI_ERR_INVALID_ARG, "degree=%d outside [1, min(%d, n_facts - 1 = %lld)]", degree,
+                    KVI_MAX_GRAPH_DEGREE, (long long)(N - 1));
+    if (!d_graph || !aligned(d_graph, 4)) return fail(KVI_ERR_INVALID_ARG, "graph is NULL or misaligned");
+    const GraphBuildWs W = graph_build_layout(N, degree);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < W.total)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", W.total);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(d_ws);
+    int32_t *ids = reinterpret_cast<int32_t *>(ws + W.ids);
+    float *scores = reinterpret_cast<float *>(ws + W.scores);
+    const int32_t k = degree + 1;
+    const int64_t E = store->g.embed_dim;
+    for (int64_t i0 = 0; i0 < N; i0 += KVI_MAX_SHARED_QUERIES) {
+        const int32_t R = (int32_t)std::min<int64_t>(KVI_MAX_SHARED_QUERIES, N - i0);
+        SharedWs L;
+        st = shared_retrieve(store, false, R, store->emb + i0 * E, k, d_ws, W.shared.total, d_status, s, L);
+        if (st != KVI_OK) return st;
+        SelectParams lp = shared_select_params(store, R, k, L, ws, ids, scores);
+        lp.place = 0;
+        lp.status = d_status;
+        KVI_CUDA(launch_select(lp, s, false));
+        GraphRowsParams gp{ids, i0, R, degree, d_graph};
+        KVI_CUDA(launch_graph_rows(gp, s));
+    }
+    return KVI_OK;
+}
+
+size_t kvi_graph_search_workspace_bytes(int32_t R, int64_t n_facts)
+{
+    if (R < 1 || R > 65535 || n_facts < 1 || n_facts > 0x7fffffff) return 0;
+    return (size_t)R * (size_t)((n_facts + 31) / 32) * 4;
+}
+
+kvi_status kvi_graph_search(const kvi_store_view *store, const int32_t *d_graph, int32_t degree, int32_t R,
+                            const float *d_queries, const int32_t *d_seeds,
+                            const kvi_graph_search_params *params, int32_t k, int32_t *d_ids,
+                            float *d_scores, int32_t *d_count, int32_t *d_stats, void *d_ws,
+                            size_t ws_bytes, int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_store(store, true, false);
+    if (st != KVI_OK) return st;
+    if (!d_graph || !aligned(d_graph, 4)) return fail(KVI_ERR_INVALID_ARG, "graph is NULL or misaligned");
+    if (degree < 1 || degree > KVI_MAX_GRAPH_DEGREE)
+        return fail(KVI_ERR_INVALID_ARG, "degree=%d outside [1, %d]", degree, KVI_MAX_GRAPH_DEGREE);
+    if (R < 1 || R > 65535) return fail(KVI_ERR_INVALID_ARG, "R=%d outside [1, 65535]", R);
+    if (!d_queries || !aligned(d_queries, 16))
+        return fail(KVI_ERR_INVALID_ARG, "queries must be a 16-byte aligned device pointer");
+    if (!d_seeds || !params || !d_ids || !d_scores)
+        return fail(KVI_ERR_INVALID_ARG, "seeds, params, ids or scores is NULL");
+    const kvi_graph_search_params P = *params;
+    if (k < 1 || P.beam < k || P.beam > KVI_MAX_GRAPH_BEAM)
+        return fail(KVI_ERR_INVALID_ARG, "need 1 <= k=%d <= beam=%d <= %d", k, P.beam, KVI_MAX_GRAPH_BEAM);
+    if (P.width < 1 || (int64_t)P.width * degree > KVI_MAX_GRAPH_FRONTIER)
+        return fail(KVI_ERR_INVALID_ARG, "width=%d: need 1 <= width * degree <= %d", P.width,
+                    KVI_MAX_GRAPH_FRONTIER);
+    if (P.max_iters < 0 || P.n_seeds < 1 || P.n_seeds > KVI_MAX_GRAPH_FRONTIER)
+        return fail(KVI_ERR_INVALID_ARG, "max_iters=%d < 0 or n_seeds=%d outside [1, %d]", P.max_iters,
+                    P.n_seeds, KVI_MAX_GRAPH_FRONTIER);
+    const size_t need = kvi_graph_search_workspace_bytes(R, store->n_facts);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < need)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", need);
+    GraphSearchParams gp{};
+    gp.emb = store->emb;
+    gp.N = store->n_facts;
+    gp.E = store->g.embed_dim;
+    gp.graph = d_graph;
+    gp.degree = degree;
+    gp.queries = d_queries;
+    gp.seeds = d_seeds;
+    gp.R = R;
+    gp.n_seeds = P.n_seeds;
+    gp.beam = P.beam;
+    gp.width = P.width;
+    gp.max_iters = P.max_iters;
+    gp.k = k;
+    gp.ids = d_ids;
+    gp.scores = d_scores;
+    gp.count = d_count;
+    gp.stats = d_stats;
+    gp.visited = static_cast<uint32_t *>(d_ws);
+    gp.vis_words = (store->n_facts + 31) / 32;
+    gp.status = d_status;
+    KVI_CUDA(launch_graph_search(gp, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+}  // extern "C"

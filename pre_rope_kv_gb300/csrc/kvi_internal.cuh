@@ -166,6 +166,35 @@ struct RescoreParams {
 };
 cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s);
 
+// Graph index: the neighbour rows of a build batch (a row's top degree + 1
+// ids without the row's own fact) and the beam search, one CTA per query.
+struct GraphRowsParams {
+    const int32_t *ids;  // [R][degree + 1] top ids of rows i0 .. i0 + R - 1
+    int64_t i0;
+    int32_t R, degree;
+    int32_t *graph;      // [N][degree]
+};
+cudaError_t launch_graph_rows(const GraphRowsParams &p, cudaStream_t s);
+
+struct GraphSearchParams {
+    const float *emb;       // [N][E]
+    int64_t N;
+    int32_t E;
+    const int32_t *graph;   // [N][degree]
+    int32_t degree;
+    const float *queries;   // [R][E]
+    const int32_t *seeds;   // [R][n_seeds]
+    int32_t R, n_seeds, beam, width, max_iters, k;
+    int32_t *ids;           // [R][k]
+    float *scores;          // [R][k]
+    int32_t *count;         // [R] or null
+    int32_t *stats;         // [R][2] (iterations, facts scored) or null
+    uint32_t *visited;      // [R][vis_words] bitmaps
+    int64_t vis_words;
+    int32_t *status;
+};
+cudaError_t launch_graph_search(const GraphSearchParams &p, cudaStream_t s);
+
 // One-time per-device kernel attributes (shared-memory opt-in), made ahead
 // of a stream capture.
 cudaError_t prepare_retrieval_kernels();

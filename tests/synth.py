@@ -95,6 +95,33 @@ def unit_rows(rng: np.random.Generator, n: int, e: int) -> np.ndarray:
     return x.astype(np.float32)
 
 
+def clustered_rows(rng: np.random.Generator, n: int, e: int, clusters: int,
+                   spread: float = 0.5) -> np.ndarray:
+    """Unit rows around `clusters` random unit centres (centre + spread *
+    Gaussian / sqrt(e), renormalised in float64): embeddings of related facts
+    lie near each other, as text embeddings of one user's memories do."""
+    centres = rng.standard_normal((clusters, e))
+    centres /= np.linalg.norm(centres, axis=1, keepdims=True)
+    which = rng.integers(0, clusters, n)
+    x = centres[which] + spread * rng.standard_normal((n, e)) / np.sqrt(e)
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    return x.astype(np.float32)
+
+
+def near_queries(rng: np.random.Generator, emb: np.ndarray, n: int, noise: float = 0.5) -> np.ndarray:
+    """Unit queries near random stored rows (row + noise * Gaussian / sqrt(e))."""
+    e = emb.shape[1]
+    picks = rng.integers(0, emb.shape[0], n)
+    q = emb[picks].astype(np.float64) + noise * rng.standard_normal((n, e)) / np.sqrt(e)
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    return q.astype(np.float32)
+
+
+def graph_seeds(rng: np.random.Generator, n_facts: int, R: int, n_seeds: int) -> np.ndarray:
+    """Seed fact ids for R graph searches, drawn uniformly (with repeats)."""
+    return rng.integers(0, n_facts, (R, n_seeds)).astype(np.int32)
+
+
 def bf16_normal_bits(rng: np.random.Generator, shape) -> np.ndarray:
     """N(0,1) float32 rounded to bf16 (round to nearest even), as uint16 bits."""
     x = rng.standard_normal(shape).astype(np.float32)

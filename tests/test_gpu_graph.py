@@ -1,0 +1,193 @@
+"""GPU parity of the graph index against the oracle.
+
+kvi_graph_build must write exactly the oracle's graph (each fact's degree
+most similar other facts, ties to the lower id), and kvi_graph_search must
+reproduce the oracle's search step for step on the same graph and seeds:
+the same ids in the same order, the same result count, the same number of
+iterations and of facts scored, and scores within 1e-4 relative + 1e-7 of
+the oracle's float64 values.  A large case (200k facts, 1024-d) checks
+sampled graph rows and sampled queries one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pre_rope_kv_gb300 as kvi
+from tests import kvi_check as kc
+from tests import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    kc.ensure_built()
+
+
+def _view(emb_d):
+    g = kvi.geometry(1, 1, 16, emb_d.shape[1])
+    return g, kvi.store_view(g, None, emb_d, None, None, n_tokens=0)
+
+
+def gpu_graph(emb_np, degree):
+    emb_d = torch.from_numpy(emb_np).cuda()
+    _, view = _view(emb_d)
+    n = emb_np.shape[0]
+    graph = torch.full((n, degree), -7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_build_workspace_bytes(n, degree), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvi.kvi_graph_build(view, degree, graph, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return graph.cpu().numpy(), emb_d
+
+
+def gpu_search(emb_d, graph_np, queries_np, seeds_np, beam, width, max_iters, k):
+    _, view = _view(emb_d)
+    R = queries_np.shape[0]
+    graph = torch.from_numpy(np.ascontiguousarray(graph_np, np.int32)).cuda()
+    q = torch.from_numpy(queries_np).cuda()
+    seeds = torch.from_numpy(np.ascontiguousarray(seeds_np, np.int32)).cuda()
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    cnt = torch.empty(R, dtype=torch.int32, device="cuda")
+    stats = torch.empty((R, 2), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_search_workspace_bytes(R, emb_d.shape[0]), dtype=torch.uint8,
+                     device="cuda")
+    params = kvi.graph_search_params(beam, width, max_iters, seeds_np.shape[1])
+    kvi.kvi_graph_search(view, graph, graph_np.shape[1], R, q, seeds, params, k, ids, sc, ws, cnt,
+                         stats, st)
+    torch.cuda.synchronize()
+    return (ids.cpu().numpy(), sc.cpu().numpy(), cnt.cpu().numpy(), stats.cpu().numpy(),
+            int(st.item()))
+
+
+def check_search(emb_np, graph_np, q_np, seeds_np, out, beam, width, max_iters, k, queries=None):
+    ids, sc, cnt, stats, status = out
+    assert status == 0
+    for r in (range(q_np.shape[0]) if queries is None else queries):
+        o_ids, o_sc, o_cnt, o_it, o_scored = oracle.graph_search(
+            q_np[r], emb_np, graph_np, seeds_np[r], beam, width, max_iters, k)
+        assert cnt[r] == o_cnt, r
+        assert np.array_equal(ids[r], o_ids), (r, ids[r], o_ids)
+        assert (stats[r, 0], stats[r, 1]) == (o_it, o_scored), r
+        m = o_cnt
+        assert np.all(np.abs(sc[r, :m] - o_sc[:m]) <= 1e-4 * np.abs(o_sc[:m]) + 1e-7), r
+        assert np.all(np.isnan(sc[r, m:]))
+
+
+@pytest.mark.parametrize("n,e,degree,seed", [(300, 64, 8, 0), (700, 128, 64, 1), (257, 32, 1, 2)])
+def test_graph_build_matches_the_oracle(n, e, degree, seed):
+    rng = np.random.default_rng(seed)
+    emb = synth.clustered_rows(rng, n, e, clusters=12)
+    g, _ = gpu_graph(emb, degree)
+    assert np.array_equal(g, oracle.graph_build(emb, degree))
+
+
+def test_graph_build_exact_ties_go_to_the_lower_id():
+    # integer-valued embeddings: many exactly equal scores
+    rng = np.random.default_rng(3)
+    emb = rng.integers(-2, 3, (300, 16)).astype(np.float32)
+    emb[50:60] = emb[7]  # duplicates of fact 7
+    g, _ = gpu_graph(emb, 12)
+    assert np.array_equal(g, oracle.graph_build(emb, 12))
+
+
+@pytest.mark.parametrize("beam,width,max_iters,n_seeds,k", [
+    (64, 1, 1000, 16, 10), (64, 1, 1000, 64, 50), (32, 4, 20, 8, 32), (128, 2, 1000, 40, 50),
+    (256, 8, 6, 512, 64)])
+def test_graph_search_matches_the_oracle(beam, width, max_iters, n_seeds, k):
+    rng = np.random.default_rng(10 + beam + width)
+    n, e, degree = 3000, 128, 32 if width <= 4 else 64
+    emb = synth.clustered_rows(rng, n, e, clusters=30)
+    graph = oracle.graph_build(emb, degree)
+    q = synth.near_queries(rng, emb, 12)
+    seeds = synth.graph_seeds(rng, n, 12, n_seeds)
+    emb_d = torch.from_numpy(emb).cuda()
+    out = gpu_search(emb_d, graph, q, seeds, beam, width, max_iters, k)
+    check_search(emb, graph, q, seeds, out, beam, width, max_iters, k)
+
+
+def test_graph_search_edge_cases():
+    rng = np.random.default_rng(20)
+    n, e = 400, 64
+    emb = synth.clustered_rows(rng, n, e, clusters=5)
+    graph = oracle.graph_build(emb, 6)
+    q = synth.near_queries(rng, emb, 4)
+    emb_d = torch.from_numpy(emb).cuda()
+    # no iterations: the best seeds
+    seeds = synth.graph_seeds(rng, n, 4, 9)
+    out = gpu_search(emb_d, graph, q, seeds, 8, 1, 0, 5)
+    check_search(emb, graph, q, seeds, out, 8, 1, 0, 5)
+    # a graph whose component holds fewer facts than k: a short result
+    small = np.array([[(i + 1) % 3 + 0] for i in range(3)] + [[3 + (i + 1) % 5] for i in range(n - 3)],
+                     np.int32)
+    seeds = np.zeros((4, 1), np.int32)  # fact 0: component {0, 1, 2}
+    out = gpu_search(emb_d, small, q, seeds, 8, 1, 100, 5)
+    check_search(emb, small, q, seeds, out, 8, 1, 100, 5)
+    assert list(out[2]) == [3, 3, 3, 3]
+    # repeated seeds are scored once
+    seeds = np.full((4, 6), 17, np.int32)
+    out = gpu_search(emb_d, graph, q, seeds, 8, 1, 3, 4)
+    check_search(emb, graph, q, seeds, out, 8, 1, 3, 4)
+
+
+def test_graph_search_records_a_bad_seed_and_skips_it():
+    rng = np.random.default_rng(21)
+    n, e = 200, 32
+    emb = synth.clustered_rows(rng, n, e, clusters=4)
+    graph = oracle.graph_build(emb, 5)
+    q = synth.near_queries(rng, emb, 2)
+    seeds = np.array([[3, n + 5, 9], [n, 1, 2]], np.int32)
+    emb_d = torch.from_numpy(emb).cuda()
+    ids, sc, cnt, stats, status = gpu_search(emb_d, graph, q, seeds, 8, 1, 50, 4)
+    assert status == kvi.ERR_OUT_OF_RANGE
+    # the remaining seeds give the oracle's search from those seeds
+    for r, good in enumerate([[3, 9], [1, 2]]):
+        o = oracle.graph_search(q[r], emb, graph, good, 8, 1, 50, 4)
+        assert np.array_equal(ids[r], o[0]) and (stats[r, 0], stats[r, 1]) == (o[3], o[4])
+
+
+def test_graph_search_rejects_bad_parameters():
+    rng = np.random.default_rng(22)
+    emb = synth.clustered_rows(rng, 100, 16, clusters=3)
+    emb_d = torch.from_numpy(emb).cuda()
+    graph = torch.zeros((100, 8), dtype=torch.int32, device="cuda")
+    _, view = _view(emb_d)
+    q = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    seeds = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    ids = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+    sc = torch.empty((1, 8), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_search_workspace_bytes(1, 100), dtype=torch.uint8, device="cuda")
+    bad = [dict(beam=4), dict(beam=300), dict(width=0), dict(width=65), dict(max_iters=-1),
+           dict(n_seeds=0), dict(n_seeds=513)]
+    for kw in bad:
+        p = dict(beam=16, width=1, max_iters=5, n_seeds=4)
+        p.update(kw)
+        with pytest.raises(kvi.KviError) as e:
+            kvi.kvi_graph_search(view, graph, 8, 1, q, seeds, kvi.graph_search_params(**p), 8, ids, sc,
+                                 ws)
+        assert e.value.status == kvi.ERR_INVALID_ARG, kw
+    with pytest.raises(kvi.KviError):
+        kvi.kvi_graph_build(view, 100, graph, ws)  # degree >= n_facts
+
+
+def test_graph_large_store_sampled_rows_and_queries():
+    # 200k facts of 1024-d: the build runs 782 shared-store batches; three
+    # rows are checked against the oracle's exact scores over all facts and
+    # four queries against the oracle's search on the GPU's graph
+    rng = np.random.default_rng(30)
+    n, e, degree = 200_000, 1024, 64
+    emb = synth.clustered_rows(rng, n, e, clusters=2000)
+    graph, emb_d = gpu_graph(emb, degree)
+    for i in (0, 123_457, n - 1):
+        s = oracle.scores(emb[i], emb)
+        top = oracle.topk(s, degree + 1)
+        assert list(graph[i]) == [int(j) for j in top if j != i][:degree], i
+    R = 64
+    q = synth.near_queries(rng, emb, R)
+    seeds = synth.graph_seeds(rng, n, R, 64)
+    out = gpu_search(emb_d, graph, q, seeds, 64, 1, 1000, 50)
+    check_search(emb, graph, q, seeds, out, 64, 1, 1000, 50, queries=[0, 17, 40, 63])
