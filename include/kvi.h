@@ -116,7 +116,9 @@ typedef struct {
     const void *kv;            /* bf16 [L][2][n_tokens][H][D] */
     const float *emb;          /* float32 [N][E] */
     const int64_t *fact_start; /* [N] first store row of each fact */
-    const int32_t *fact_len;   /* [N] tokens of each fact, >= 0 */
+    const int32_t *fact_len;   /* [N] tokens of each fact, >= 0; both extents
+                                * are required by every call, since the
+                                * scoring kernels validate each fact's */
     uint32_t flags;            /* KVI_STORE_* */
     uint32_t reserved;         /* 0 */
 } kvi_store_view;

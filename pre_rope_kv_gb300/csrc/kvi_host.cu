@@ -76,10 +76,12 @@ kvi_status check_store(const kvi_store_view *s, bool retrieval, bool inject)
     if (s->n_tokens < 0) return fail(KVI_ERR_INVALID_ARG, "n_tokens < 0");
     if (retrieval && (!s->emb || !aligned(s->emb, 16)))
         return fail(KVI_ERR_INVALID_ARG, "emb must be a 16-byte aligned device pointer");
-    if ((inject || !retrieval) && (!s->fact_len))
-        return fail(KVI_ERR_INVALID_ARG, "fact_len is NULL");
-    if (inject && (!s->kv || !aligned(s->kv, 16) || !s->fact_start))
-        return fail(KVI_ERR_INVALID_ARG, "kv (16-byte aligned) and fact_start are required");
+    // every kernel that scores a fact also validates its extent, so the
+    // extents are required even by retrieval-only calls
+    if (!s->fact_len || !s->fact_start)
+        return fail(KVI_ERR_INVALID_ARG, "fact_start and fact_len are required");
+    if (inject && (!s->kv || !aligned(s->kv, 16)))
+        return fail(KVI_ERR_INVALID_ARG, "kv (16-byte aligned) is required");
     return KVI_OK;
 }
 

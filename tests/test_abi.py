@@ -132,6 +132,28 @@ def test_retrieve_topk_host_validation(lib):
     small = _FakeTensor(n=16)
     assert _err(kvi.kvi_retrieve_topk, _store(), t, 5, t, t, small) == kvi.ERR_INVALID_ARG
     assert "workspace" in kvi.kvi_last_error()
+    # the scoring kernels validate every fact's extent: retrieval needs them
+    for missing in ("fact_start", "fact_len"):
+        assert _err(kvi.kvi_retrieve_topk, _store(**{missing: None}), t, 5, t, t, t) \
+            == kvi.ERR_INVALID_ARG
+        assert "fact_start and fact_len" in kvi.kvi_last_error()
+
+
+def test_graph_host_validation(lib):
+    t = _FakeTensor()
+    assert _err(kvi.kvi_graph_build, _store(fact_len=None), 8, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(kvi.kvi_graph_build, _store(n_facts=8), 8, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(kvi.kvi_graph_build, _store(), 129, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(kvi.kvi_graph_build, _store(), 8, t, _FakeTensor(n=16)) == kvi.ERR_INVALID_ARG
+    assert kvi.kvi_graph_build_workspace_bytes(8, 8) == 0
+    assert kvi.kvi_graph_search_workspace_bytes(0, 100) == 0
+    p = kvi.graph_search_params(16, 1, 10, 4)
+    assert _err(kvi.kvi_graph_search, _store(fact_start=None), t, 8, 1, t, t, p, 8, t, t, t) \
+        == kvi.ERR_INVALID_ARG
+    assert _err(kvi.kvi_graph_search, _store(), t, 8, 1, t, t, kvi.graph_search_params(4, 1, 10, 4),
+                8, t, t, t) == kvi.ERR_INVALID_ARG       # beam < k
+    assert _err(kvi.kvi_graph_search, _store(), t, 8, 1, t, t, kvi.graph_search_params(16, 65, 10, 4),
+                8, t, t, t) == kvi.ERR_INVALID_ARG       # width * degree > 512
 
 
 def test_inject_paged_host_validation(lib):

@@ -25,9 +25,18 @@ def _built():
     kc.ensure_built()
 
 
+_EXTENTS = {}
+
+
 def _view(emb_d):
+    # retrieval validates each fact's extent: empty facts (start 0, length 0)
+    n = emb_d.shape[0]
+    if n not in _EXTENTS:
+        _EXTENTS[n] = (torch.zeros(n, dtype=torch.int64, device="cuda"),
+                       torch.zeros(n, dtype=torch.int32, device="cuda"))
+    fs, fl = _EXTENTS[n]
     g = kvi.geometry(1, 1, 16, emb_d.shape[1])
-    return g, kvi.store_view(g, None, emb_d, None, None, n_tokens=0)
+    return g, kvi.store_view(g, None, emb_d, fs, fl, n_tokens=0)
 
 
 def gpu_graph(emb_np, degree):
