@@ -67,6 +67,9 @@ def parse_args(argv=None):
     # profiling case only: shared-store retrieval of R queries over the
     # workload's embeddings, with a one-token K/V store (~0.1 GB on the device)
     ap.add_argument("--shared-retrieval", type=int, default=0, metavar="R")
+    ap.add_argument("--graph-index", action="store_true",
+                    help="graph index on a clustered store (own JSON line)")
+    ap.add_argument("--graph-facts", type=int, default=1_000_000)
     return ap.parse_args(argv)
 
 
@@ -745,6 +748,115 @@ def run_shared_retrieval(args):
                       "tf32_gflop": round(2.0 * R * w.n_facts * w.embed_dim / 1e9, 3)}), flush=True)
 
 
+def run_graph_index(args):
+    """The graph index (the review's GPU ANN index, 64 neighbours and beam
+    64) on a clustered store of --graph-facts 1024-d embeddings: graph build
+    time, search latency of one query, throughput of 1024 queries in one
+    call, recall@k against the exact top-k of the shared-store path, and the
+    exact scan of one query timed beside it.  L2 is flushed before every
+    timed call.  Prints one JSON line (not the bench line)."""
+    import torch
+    import pre_rope_kv_gb300 as kvi
+    from pre_rope_kv_gb300 import build as kbuild
+    from tests import synth
+    kbuild.build()
+    kvi.load_library()
+    peak, peak_kind = load_peaks()
+    N, E, D, k = args.graph_facts, 1024, 64, args.k
+    beam, width, n_seeds, R = 64, 1, 64, 1024
+    clusters = max(1, N // 500)
+    emb = synth.clustered_rows_device(7, N, E, clusters)
+    fs = torch.zeros(N, dtype=torch.int64, device="cuda")
+    fl = torch.zeros(N, dtype=torch.int32, device="cuda")
+    g = kvi.geometry(1, 1, 16, E)
+    view = kvi.store_view(g, None, emb, fs, fl, n_tokens=0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    graph = torch.empty((N, D), dtype=torch.int32, device="cuda")
+    ws_b = torch.empty(kvi.kvi_graph_build_workspace_bytes(N, D), dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    kvi.kvi_graph_build(view, D, graph, ws_b, status)
+    e1.record()
+    torch.cuda.synchronize()
+    build_s = e0.elapsed_time(e1) / 1e3
+    del ws_b
+
+    q = synth.near_queries_device(8, emb, R)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    seeds = torch.randint(0, N, (R, n_seeds), generator=gen, device="cuda", dtype=torch.int32)
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    stats = torch.empty((R, 2), dtype=torch.int32, device="cuda")
+    ws_s = torch.empty(kvi.kvi_graph_search_workspace_bytes(R, N), dtype=torch.uint8, device="cuda")
+    params = kvi.graph_search_params(beam, width, 10_000, n_seeds)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(ts)
+
+    def search(r):
+        kvi.kvi_graph_search(view, graph, D, r, q[:r], seeds[:r], params, k, ids[:r], sc[:r], ws_s,
+                             None, stats[:r], status)
+
+    one = timed(lambda: search(1), max(10, args.steps))
+    batch = timed(lambda: search(R), 5)
+    st = stats.cpu().numpy().astype(np.float64)
+    got = ids.cpu().numpy()
+    # exact top-k of the first 256 queries (shared-store path) for recall
+    RE = 256
+    ex_ids = torch.empty((RE, k), dtype=torch.int32, device="cuda")
+    ex_sc = torch.empty((RE, k), dtype=torch.float32, device="cuda")
+    ws_e = torch.empty(kvi.kvi_workspace_bytes_shared(RE, N, k), dtype=torch.uint8, device="cuda")
+    kvi.kvi_retrieve_topk_shared(view, RE, q[:RE], k, ex_ids, ex_sc, ws_e, status)
+    torch.cuda.synchronize()
+    ex = ex_ids.cpu().numpy()
+    recall = float(np.mean([len(set(got[r]) & set(ex[r])) / k for r in range(RE)]))
+    shared_s = timed(lambda: kvi.kvi_retrieve_topk_shared(view, RE, q[:RE], k, ex_ids, ex_sc, ws_e,
+                                                          status), 5)
+    del ws_e
+    ws_1 = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
+    scan_s = timed(lambda: kvi.kvi_retrieve_topk(view, q[0], k, ex_ids[0], ex_sc[0], ws_1), 10)
+    assert int(status.item()) == 0
+    # bytes a query reads: the rows it scores, its graph rows, its bitmap
+    per_q = st[:, 1].mean() * E * 4 + st[:, 0].mean() * D * 4 + (N + 7) // 8
+    out = {
+        "mode": "graph_index", "metric": "graph-index queries/s (1024 queries per call)",
+        "value": round(R / batch, 1), "unit": "queries/s", "higher_is_better": True,
+        "config": {"facts": N, "embed_dim": E, "degree": D, "beam": beam, "width": width,
+                   "seeds": n_seeds, "k": k, "clusters": clusters,
+                   "data": "synthetic clustered unit embeddings (centre + 0.5 Gaussian / sqrt(E)); "
+                           "queries near stored facts", "l2": "flushed before every timed call"},
+        "build_s": round(build_s, 3),
+        "latency_us_one_query": round(one * 1e6, 2),
+        "batch_us": round(batch * 1e6, 2),
+        "recall_at_k": round(recall, 4),
+        "iterations_mean": round(float(st[:, 0].mean()), 1),
+        "facts_scored_mean": round(float(st[:, 1].mean()), 1),
+        "bytes_per_query": int(per_q),
+        "roofline": {"kernel": "graph_search_kernel", "bound": "hbm",
+                     "achieved": round(per_q * R / batch / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_q * R / batch / 1e9 / peak, 4), "traffic": None},
+        "peak_kind": peak_kind,
+        "exact": {"scan_one_query_us": round(scan_s * 1e6, 2),
+                  "shared_256_queries_us_per_query": round(shared_s / RE * 1e6, 2)},
+    }
+    print(json.dumps(out), flush=True)
+
+
 def run_workload(args):
     """The other serving workloads at full size: 64 concurrent requests over
     their own 5k-fact stores, Mistral-7B geometry with 50k facts placed up to
@@ -860,6 +972,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.shared_retrieval:
         run_shared_retrieval(args)
+    elif args.graph_index:
+        run_graph_index(args)
     elif args.workload:
         run_workload(args)
     elif args.impl == "reference":

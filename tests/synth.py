@@ -117,6 +117,35 @@ def near_queries(rng: np.random.Generator, emb: np.ndarray, n: int, noise: float
     return q.astype(np.float32)
 
 
+def clustered_rows_device(seed: int, n: int, e: int, clusters: int, spread: float = 0.5,
+                          chunk: int = 1 << 16):
+    """clustered_rows drawn on the device (torch, float32), for stores too
+    large to draw on the host; chunked so that the draw needs little scratch."""
+    torch = _torch()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    centres = torch.randn((clusters, e), generator=gen, device="cuda")
+    centres /= centres.norm(dim=1, keepdim=True)
+    out = torch.empty((n, e), dtype=torch.float32, device="cuda")
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        which = torch.randint(0, clusters, (b - a,), generator=gen, device="cuda")
+        x = centres[which] + (spread / e ** 0.5) * torch.randn((b - a, e), generator=gen, device="cuda")
+        out[a:b] = x / x.norm(dim=1, keepdim=True)
+    return out
+
+
+def near_queries_device(seed: int, emb, n: int, noise: float = 0.5):
+    """near_queries on the device: unit queries near random stored rows."""
+    torch = _torch()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    e = emb.shape[1]
+    picks = torch.randint(0, emb.shape[0], (n,), generator=gen, device="cuda")
+    q = emb[picks] + (noise / e ** 0.5) * torch.randn((n, e), generator=gen, device="cuda")
+    return (q / q.norm(dim=1, keepdim=True)).contiguous()
+
+
 def graph_seeds(rng: np.random.Generator, n_facts: int, R: int, n_seeds: int) -> np.ndarray:
     """Seed fact ids for R graph searches, drawn uniformly (with repeats)."""
     return rng.integers(0, n_facts, (R, n_seeds)).astype(np.int32)
