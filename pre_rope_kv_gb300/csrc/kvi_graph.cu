@@ -13,7 +13,7 @@
 //                        the parents' neighbour ids and test-and-set them in
 //                        the query's visited bitmap (atomicOr, so each fact
 //                        is scored at most once, exactly); each warp scores
-//                        new facts with the same Dot2 keys as the scan; the
+//                        a new fact with the same Dot2 keys as the scan; the
 //                        new facts and the beam are merged by counting
 //                        ranks (ids are distinct, so every rank is unique)
 //                        into the other half of a double buffer.
@@ -76,36 +76,38 @@ __device__ __forceinline__ void visit(SearchSmem &sm, uint32_t *vis, int64_t N, 
     if (fresh) sm.new_id[base + __popc(mask & ((1u << lane) - 1u))] = f;
 }
 
-// Dot2 key of every new fact: each warp scores two rows at a time.
+// Dot2 key of every new fact, one row per warp: each lane loads up to
+// kRowChunk float4 of the row before any arithmetic, so that a 1024-d row
+// costs one round trip to memory (an iteration typically finds fewer new
+// facts than there are warps).
+constexpr int kRowChunk = 8;
+
 __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem &sm, const float *q, int n_new)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float4 *q4 = reinterpret_cast<const float4 *>(q);
     const int E4 = p.E / 4;
-    for (int m0 = 2 * warp; m0 < n_new; m0 += 2 * kSearchWarps) {
-        const bool two = m0 + 1 < n_new;
-        const float4 *a = reinterpret_cast<const float4 *>(p.emb + (int64_t)sm.new_id[m0] * p.E);
-        const float4 *b = reinterpret_cast<const float4 *>(p.emb + (int64_t)sm.new_id[two ? m0 + 1 : m0] * p.E);
-        Dot2x4 da, db;
+    for (int m = warp; m < n_new; m += kSearchWarps) {
+        const float4 *a = reinterpret_cast<const float4 *>(p.emb + (int64_t)sm.new_id[m] * p.E);
+        Dot2x4 da;
         da.zero();
-        db.zero();
-#pragma unroll 4
-        for (int v = lane; v < E4; v += 32) {
-            const float4 qv = __ldg(q4 + v);
-            const float4 ea = ld_stream_f4(a + v);
-            const float4 eb = ld_stream_f4(b + v);
-            da.add(qv, ea);
-            db.add(qv, eb);
+        for (int v0 = 0; v0 < E4; v0 += 32 * kRowChunk) {
+            float4 ra[kRowChunk];
+#pragma unroll
+            for (int u = 0; u < kRowChunk; ++u) {
+                const int v = v0 + lane + 32 * u;
+                if (v < E4) ra[u] = ld_stream_f4(a + v);
+            }
+#pragma unroll
+            for (int u = 0; u < kRowChunk; ++u) {
+                const int v = v0 + lane + 32 * u;
+                if (v < E4) da.add(__ldg(q4 + v), ra[u]);
+            }
         }
-        float sa, ca, sb, cb;
+        float sa, ca;
         da.combine(sa, ca);
-        db.combine(sb, cb);
         warp_reduce_pair(sa, ca);
-        warp_reduce_pair(sb, cb);
-        if (lane == 0) {
-            sm.new_key[m0] = score_key(sa, ca);
-            if (two) sm.new_key[m0 + 1] = score_key(sb, cb);
-        }
+        if (lane == 0) sm.new_key[m] = score_key(sa, ca);
     }
 }
 
