@@ -858,6 +858,14 @@ def run_graph_index(args):
     batch_search = timed(lambda: search(R, seeds), 5)
     st = stats.cpu().numpy().astype(np.float64)
     recall_lm = recall()
+    # the beam trades recall for work: search alone, same landmark seeds
+    sweep = {}
+    for bw in (64, 128, 256):
+        params = kvi.graph_search_params(bw, width, 10_000, n_seeds)
+        bt = timed(lambda: search(R, seeds), 3)
+        sweep[str(bw)] = {"recall_at_k": round(recall(), 4), "batch_us_search_only": round(bt * 1e6, 2),
+                          "queries_per_s": round(R / bt, 1)}
+    params = kvi.graph_search_params(beam, width, 10_000, n_seeds)
     shared_s = timed(lambda: kvi.kvi_retrieve_topk_shared(view, RE, q[:RE], k, ex_ids, ex_sc, ws_e,
                                                           status), 5)
     del ws_e
@@ -884,6 +892,7 @@ def run_graph_index(args):
         "iterations_mean": round(float(st[:, 0].mean()), 1),
         "facts_scored_mean": round(float(st[:, 1].mean()), 1),
         "bytes_per_query": int(per_q),
+        "beam_sweep": sweep,
         "roofline": {"kernel": "graph_search_kernel", "bound": "hbm",
                      "achieved": round(per_q * R / batch_search / 1e9, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(per_q * R / batch_search / 1e9 / peak, 4),

@@ -200,3 +200,42 @@ def test_graph_large_store_sampled_rows_and_queries():
     seeds = synth.graph_seeds(rng, n, R, 64)
     out = gpu_search(emb_d, graph, q, seeds, 64, 1, 1000, 50)
     check_search(emb, graph, q, seeds, out, 64, 1, 1000, 50, queries=[0, 17, 40, 63])
+
+
+def test_graph_retrieval_through_placement_and_injection():
+    # the approximate index serves the whole path: the graph search's ids go
+    # through kvi_place and kvi_inject_paged, and the pool must equal the
+    # oracle's injection of the oracle's search result at its positions
+    w = synth.Workload(name="graph_inject", layers=2, kv_heads=4, head_dim=128, rope_theta=5e5,
+                       block_size=16, n_facts=800, len_lo=1, len_hi=30, len_dist="uniform",
+                       embed_dim=128, requests=1, k=20, start=7, start_hi=0, seed=950, store="dense")
+    b = synth.build_workload(w)
+    st = b.stores[0]
+    emb = st.emb_np
+    graph = oracle.graph_build(emb, 16)
+    rng = np.random.default_rng(951)
+    seeds = synth.graph_seeds(rng, w.n_facts, 1, 16)
+    k = w.k
+    view = kc.views_of(b)[0]
+    ids = torch.empty((1, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((1, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_search_workspace_bytes(1, w.n_facts), dtype=torch.uint8,
+                     device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_graph = torch.from_numpy(graph).cuda()
+    d_seeds = torch.from_numpy(seeds).cuda()
+    kvi.kvi_graph_search(view, d_graph, 16, 1, b.queries, d_seeds, kvi.graph_search_params(32, 1, 500, 16),
+                         k, ids, sc, ws, status=status)
+    pos = torch.empty(k, dtype=torch.int32, device="cuda")
+    start = int(b.start_pos[0])
+    kvi.kvi_place(view, ids[0], k, start, pos, status)
+    tl = int(b.table_lens[0])
+    bt = torch.from_numpy(b.block_tables[0, :tl].copy()).cuda()
+    kvi.kvi_inject_paged(view, ids[0], pos, k, bt, tl, kc.cache_of(b), w.rope_theta, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_ids = oracle.graph_search(b.queries_np[0], emb, graph, seeds[0], 32, 1, 500, k)[0]
+    assert np.array_equal(ids.cpu().numpy()[0], o_ids)
+    o_pos, _ = oracle.place(o_ids, st.len_np, start)
+    assert np.array_equal(pos.cpu().numpy(), o_pos)
+    kc.check_pool_full(b, [(o_ids, o_pos)])
