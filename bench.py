@@ -70,6 +70,7 @@ def parse_args(argv=None):
     ap.add_argument("--graph-index", action="store_true",
                     help="graph index on a clustered store (own JSON line)")
     ap.add_argument("--graph-facts", type=int, default=1_000_000)
+    ap.add_argument("--graph-data", choices=["latent", "clustered"], default="latent")
     return ap.parse_args(argv)
 
 
@@ -765,7 +766,14 @@ def run_graph_index(args):
     N, E, D, k = args.graph_facts, 1024, 64, args.k
     beam, width, n_seeds, R = 64, 1, 64, 1024
     clusters = max(1, N // 500)
-    emb = synth.clustered_rows_device(7, N, E, clusters)
+    if args.graph_data == "latent":
+        emb = synth.latent_rows_device(7, N, E)
+        data = ("synthetic unit embeddings of intrinsic dimension 32 (random 1024 x 32 projection "
+                "of Gaussian points + 0.1 Gaussian / sqrt(E)); queries near stored facts")
+    else:
+        emb = synth.clustered_rows_device(7, N, E, clusters)
+        data = (f"synthetic clustered unit embeddings, {clusters} separated clusters (centre + 0.5 "
+                f"Gaussian / sqrt(E)); queries near stored facts")
     fs = torch.zeros(N, dtype=torch.int64, device="cuda")
     fl = torch.zeros(N, dtype=torch.int32, device="cuda")
     g = kvi.geometry(1, 1, 16, E)
@@ -879,9 +887,8 @@ def run_graph_index(args):
                                           "seeds + search)",
         "value": round(R / batch, 1), "unit": "queries/s", "higher_is_better": True,
         "config": {"facts": N, "embed_dim": E, "degree": D, "beam": beam, "width": width,
-                   "seeds": n_seeds, "landmarks": LM, "k": k, "clusters": clusters,
-                   "data": "synthetic clustered unit embeddings (centre + 0.5 Gaussian / sqrt(E)); "
-                           "queries near stored facts", "l2": "flushed before every timed call"},
+                   "seeds": n_seeds, "landmarks": LM, "k": k, "data": data,
+                   "l2": "flushed before every timed call"},
         "build_s": round(build_s, 3),
         "recall_at_k": round(recall_lm, 4),
         "recall_at_k_random_seeds": round(recall_random, 4),

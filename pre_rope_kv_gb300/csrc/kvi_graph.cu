@@ -88,7 +88,12 @@ __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem
     const float4 *q4 = reinterpret_cast<const float4 *>(q);
     const int E4 = p.E / 4;
     for (int m = warp; m < n_new; m += kSearchWarps) {
-        const float4 *a = reinterpret_cast<const float4 *>(p.emb + (int64_t)sm.new_id[m] * p.E);
+        const int32_t f = sm.new_id[m];
+        const float4 *a = reinterpret_cast<const float4 *>(p.emb + (int64_t)f * p.E);
+        // a scored fact may become a parent: bring its graph row into L2 now,
+        // so that expanding it later costs an L2 hit, not a DRAM round trip
+        if (lane * 32 < p.degree)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.graph + (int64_t)f * p.degree + lane * 32));
         Dot2x4 da;
         da.zero();
         for (int v0 = 0; v0 < E4; v0 += 32 * kRowChunk) {

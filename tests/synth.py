@@ -135,6 +135,25 @@ def clustered_rows_device(seed: int, n: int, e: int, clusters: int, spread: floa
     return out
 
 
+def latent_rows_device(seed: int, n: int, e: int, latent: int = 32, noise: float = 0.1,
+                       chunk: int = 1 << 16):
+    """Unit rows of low intrinsic dimension, drawn on the device: a random
+    e x latent projection of latent-dimensional Gaussian points, plus noise
+    * Gaussian / sqrt(e), renormalised.  Neighbourhoods vary continuously
+    (no isolated clusters), as for text embeddings."""
+    torch = _torch()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    proj = torch.randn((latent, e), generator=gen, device="cuda") / latent ** 0.5
+    out = torch.empty((n, e), dtype=torch.float32, device="cuda")
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        z = torch.randn((b - a, latent), generator=gen, device="cuda")
+        x = z @ proj + (noise / e ** 0.5) * torch.randn((b - a, e), generator=gen, device="cuda")
+        out[a:b] = x / x.norm(dim=1, keepdim=True)
+    return out
+
+
 def near_queries_device(seed: int, emb, n: int, noise: float = 0.5):
     """near_queries on the device: unit queries near random stored rows."""
     torch = _torch()
