@@ -27,8 +27,11 @@
 namespace kvi {
 namespace {
 
-constexpr int kSearchThreads = 256;
-constexpr int kSearchWarps = kSearchThreads / 32;
+// 256 threads per query when many queries share the GPU (4 CTAs per SM);
+// 512 when there are too few queries to fill it, so that one query scores
+// twice as many new facts per memory round trip
+constexpr int kSearchThreadsBatch = 256;
+constexpr int kSearchThreadsAlone = 512;
 
 struct SearchSmem {
     uint64_t key[2][KVI_MAX_GRAPH_BEAM];
@@ -82,8 +85,10 @@ __device__ __forceinline__ void visit(SearchSmem &sm, uint32_t *vis, int64_t N, 
 // facts than there are warps).
 constexpr int kRowChunk = 8;
 
+template <int T>
 __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem &sm, const float *q, int n_new)
 {
+    constexpr int kSearchWarps = T / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float4 *q4 = reinterpret_cast<const float4 *>(q);
     const int E4 = p.E / 4;
@@ -118,10 +123,11 @@ __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem
 
 // Merge the beam (cur, nc entries, sorted) with the new facts into the
 // other buffer, keeping the best `beam`; returns the new count.
+template <int T>
 __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new, int beam)
 {
     const int nxt = cur ^ 1;
-    for (int e = threadIdx.x; e < n_new + nc; e += kSearchThreads) {
+    for (int e = threadIdx.x; e < n_new + nc; e += T) {
         uint64_t k;
         int32_t id;
         uint8_t ex;
@@ -156,29 +162,30 @@ __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new,
     return min(beam, nc + n_new);
 }
 
-__global__ void __launch_bounds__(kSearchThreads) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
+template <int T>
+__global__ void __launch_bounds__(T) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
 {
     __shared__ SearchSmem sm;
     const int r = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *q = p.queries + (int64_t)r * p.E;
     uint32_t *vis = p.visited + (int64_t)r * p.vis_words;
-    for (int64_t w = tid; w < p.vis_words; w += kSearchThreads) vis[w] = 0u;
+    for (int64_t w = tid; w < p.vis_words; w += T) vis[w] = 0u;
     if (tid == 0) sm.n_new = 0;
     __syncthreads();
 
     // seeds
-    for (int t0 = 0; t0 < p.n_seeds; t0 += kSearchThreads) {
+    for (int t0 = 0; t0 < p.n_seeds; t0 += T) {
         const int t = t0 + tid;
         visit(sm, vis, p.N, t < p.n_seeds ? p.seeds[(int64_t)r * p.n_seeds + t] : 0, t < p.n_seeds,
               p.status);
     }
     __syncthreads();
     int n_new = sm.n_new;
-    score_new(p, sm, q, n_new);
+    score_new<T>(p, sm, q, n_new);
     __syncthreads();
     int cur = 0;
-    int nc = merge(sm, cur ^ 1, 0, n_new, p.beam);  // into buffer 0 from an empty beam
+    int nc = merge<T>(sm, cur ^ 1, 0, n_new, p.beam);  // into buffer 0 from an empty beam
     __syncthreads();
 
     int iters = 0;
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kSearchThreads) graph_search_kernel(const __gr
         if (np == 0) break;
         ++iters;
         const int total = np * p.degree;
-        for (int t0 = 0; t0 < total; t0 += kSearchThreads) {
+        for (int t0 = 0; t0 < total; t0 += T) {
             const int t = t0 + tid;
             int32_t f = 0;
             if (t < total) f = __ldg(p.graph + (int64_t)sm.parent[t / p.degree] * p.degree + t % p.degree);
@@ -217,15 +224,15 @@ __global__ void __launch_bounds__(kSearchThreads) graph_search_kernel(const __gr
         __syncthreads();
         n_new = sm.n_new;
         scored += n_new;
-        score_new(p, sm, q, n_new);
+        score_new<T>(p, sm, q, n_new);
         __syncthreads();
-        nc = merge(sm, cur, nc, n_new, p.beam);
+        nc = merge<T>(sm, cur, nc, n_new, p.beam);
         cur ^= 1;
         __syncthreads();
     }
 
     const int cnt = min(nc, p.k);
-    for (int j = tid; j < p.k; j += kSearchThreads) {
+    for (int j = tid; j < p.k; j += T) {
         p.ids[(int64_t)r * p.k + j] = j < cnt ? sm.id[cur][j] : -1;
         p.scores[(int64_t)r * p.k + j] = j < cnt ? key_score(sm.key[cur][j]) : __int_as_float(0x7fc00000);
     }
@@ -248,7 +255,11 @@ cudaError_t launch_graph_rows(const GraphRowsParams &p, cudaStream_t s)
 
 cudaError_t launch_graph_search(const GraphSearchParams &p, cudaStream_t s)
 {
-    graph_search_kernel<<<(unsigned)p.R, kSearchThreads, 0, s>>>(p);
+    DeviceInfo di;
+    const cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    if (p.R <= di.sms) graph_search_kernel<kSearchThreadsAlone><<<(unsigned)p.R, kSearchThreadsAlone, 0, s>>>(p);
+    else graph_search_kernel<kSearchThreadsBatch><<<(unsigned)p.R, kSearchThreadsBatch, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -119,6 +119,19 @@ def test_graph_search_matches_the_oracle(beam, width, max_iters, n_seeds, k):
     check_search(emb, graph, q, seeds, out, beam, width, max_iters, k)
 
 
+def test_graph_search_batch_variant_matches_the_oracle():
+    # more queries than SMs: the 256-thread variant (fewer queries use 512)
+    rng = np.random.default_rng(40)
+    n, e, degree, R = 2000, 64, 32, 160
+    emb = synth.clustered_rows(rng, n, e, clusters=10)
+    graph = oracle.graph_build(emb, degree)
+    q = synth.near_queries(rng, emb, R)
+    seeds = synth.graph_seeds(rng, n, R, 12)
+    emb_d = torch.from_numpy(emb).cuda()
+    out = gpu_search(emb_d, graph, q, seeds, 48, 2, 1000, 40)
+    check_search(emb, graph, q, seeds, out, 48, 2, 1000, 40, queries=range(0, R, 7))
+
+
 def test_graph_search_edge_cases():
     rng = np.random.default_rng(20)
     n, e = 400, 64
