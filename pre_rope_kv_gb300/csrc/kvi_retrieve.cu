@@ -1004,23 +1004,41 @@ select_kernel(const __grid_constant__ SelectParams p)
 // of facts hold a lo whose key's top 16 bits are >= t (so at least k facts
 // have lo >= T = the smallest value with those bits, i.e. T is at most the
 // k-th largest lo, itself at most the k-th largest exact score); every fact
-// with hi >= T is a candidate, and no other fact can be in the top k.
-// Thread t scans a contiguous id range, so a block scan of the counts
-// writes the candidates in id order.
+// with hi >= T is a candidate, and no other fact can be in the top k.  The
+// bound holds for any split of the facts into disjoint groups.  Each warp
+// owns a contiguous segment of ids and its lanes read consecutive facts
+// (coalesced, kCandUnroll loads in flight per lane); a group is 4 lanes'
+// facts.  Candidates are written in id order: a block scan over the warps'
+// counts gives each segment its base, and ballots order each warp's facts.
+constexpr int kCandUnroll = 4;
+
 __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_constant__ CandParams p)
 {
     __shared__ uint32_t gmax[kSelectGroups];
     __shared__ uint32_t wtot[32];
     __shared__ uint32_t t_star;
+    constexpr int kWarps = kSelectThreads / 32;
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *lo = p.lo + (int64_t)r * p.stride;
     const float *hi = p.hi + (int64_t)r * p.stride;
     const int64_t N = p.N;
-    const int64_t per = (N + kSelectThreads - 1) / kSelectThreads;
-    const int64_t i0 = min(N, (int64_t)tid * per), i1 = min(N, i0 + per);
+    // warp segments of whole 32-fact rows
+    const int64_t rows = (N + 31) / 32;
+    const int64_t per = (rows + kWarps - 1) / kWarps;
+    const int64_t s0 = min(N, (int64_t)warp * per * 32), s1 = min(N, s0 + per * 32);
     uint32_t mt = 0;
-    for (int64_t i = i0; i < i1; ++i) mt = max(mt, order32(__ldcg(lo + i)) >> 16);
+    for (int64_t b = s0; b < s1; b += 32 * kCandUnroll) {
+        float v[kCandUnroll];
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u) {
+            const int64_t i = b + 32 * u + lane;
+            v[u] = i < s1 ? __ldcg(lo + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u)
+            if (b + 32 * u + lane < s1) mt = max(mt, order32(v[u]) >> 16);
+    }
     mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
     mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
     if ((lane & 3) == 0) gmax[tid >> 2] = mt;
@@ -1042,14 +1060,46 @@ __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_co
     }
     __syncthreads();
     const uint32_t T = t_star << 16;
+    // this warp's count, then its base among the warps (segments in order)
     uint32_t cnt = 0;
-    for (int64_t i = i0; i < i1; ++i) cnt += order32(__ldcg(hi + i)) >= T ? 1u : 0u;
-    const uint32_t incl = block_incl_scan<uint32_t>(cnt, wtot);
-    uint32_t at = incl - cnt;
+    for (int64_t b = s0; b < s1; b += 32 * kCandUnroll) {
+        float v[kCandUnroll];
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u) {
+            const int64_t i = b + 32 * u + lane;
+            v[u] = i < s1 ? __ldcg(hi + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u)
+            cnt += __popc(__ballot_sync(0xffffffffu, b + 32 * u + lane < s1 && order32(v[u]) >= T));
+    }
+    if (lane == 0) wtot[warp] = cnt;
+    __syncthreads();
+    uint32_t base = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t c = wtot[w];
+        base += w < warp ? c : 0u;
+        total += c;
+    }
     int32_t *cand = p.cand + (int64_t)r * p.stride;
-    for (int64_t i = i0; i < i1; ++i)
-        if (order32(__ldcg(hi + i)) >= T) cand[at++] = (int32_t)i;
-    if (tid == kSelectThreads - 1) p.cand_n[r] = (int32_t)incl;
+    uint32_t at = base;
+    for (int64_t b = s0; b < s1; b += 32 * kCandUnroll) {
+        float v[kCandUnroll];
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u) {
+            const int64_t i = b + 32 * u + lane;
+            v[u] = i < s1 ? __ldcg(hi + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kCandUnroll; ++u) {
+            const int64_t i = b + 32 * u + lane;
+            const bool take = i < s1 && order32(v[u]) >= T;
+            const unsigned m = __ballot_sync(0xffffffffu, take);
+            if (take) cand[at + __popc(m & ((1u << lane) - 1u))] = (int32_t)i;
+            at += __popc(m);
+        }
+    }
+    if (tid == 0) p.cand_n[r] = (int32_t)total;
 }
 
 // Exact keys of the candidates: one warp per candidate, the same Dot2
