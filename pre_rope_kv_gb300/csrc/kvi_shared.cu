@@ -189,17 +189,13 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
             }
             __syncwarp();
-            // each tile walks E from its own starting chunk, so that the
-            // CTAs do not all read the same query columns from the same L2
-            // slices at once (the interval bound holds in any summation order)
-            const int kx = ((kc + tile) % nk) * kChunk;
             for (int j = lane; j < na + nb; j += 32) {
                 if (j < na)
-                    tma_2d(saddr(a_st + (size_t)s * kStageBytesA + (size_t)j * kBoxRowsA * 128), &tm_emb, kx,
-                           tile * kTileM + j * kBoxRowsA, fb);
+                    tma_2d(saddr(a_st + (size_t)s * kStageBytesA + (size_t)j * kBoxRowsA * 128), &tm_emb,
+                           kc * kChunk, tile * kTileM + j * kBoxRowsA, fb);
                 else
-                    tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q, kx,
-                           (j - na) * kBoxRowsB, fb);
+                    tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
+                           kc * kChunk, (j - na) * kBoxRowsB, fb);
             }
         }
     } else if (warp == 1) {
