@@ -477,6 +477,29 @@ KVI_API kvi_status kvi_graph_search(const kvi_store_view *store, const int32_t *
                                     int32_t *d_stats, void *d_ws, size_t ws_bytes,
                                     int32_t *d_status, kvi_stream_t stream);
 
+/* Graph retrieval and injection, fused, for R requests over one store
+ * (the pages' serving path with the ANN index: retrieve, rotate by Chunked
+ * RoPE, scatter into the paged cache).  Each query is searched as by
+ * kvi_graph_search; its final beam, in rank order, is handed to the same
+ * selection, placement and inject kernels as kvi_retrieve_and_inject_shared,
+ * so the first k facts of the beam are injected back to back from
+ * d_start_pos[r] through block table r.  Arguments are those of
+ * kvi_graph_search (no counts or stats) and of
+ * kvi_retrieve_and_inject_shared; 1 <= R <= KVI_MAX_REQUESTS.  If a beam
+ * holds fewer than k facts, the missing ranks come back as id -1 and
+ * KVI_ERR_OUT_OF_RANGE is recorded.  d_ws: device,
+ * kvi_graph_retrieve_and_inject_workspace_bytes, 256-byte aligned.  Errors:
+ * as the two calls named. */
+KVI_API size_t kvi_graph_retrieve_and_inject_workspace_bytes(int32_t R, int64_t n_facts, int32_t beam,
+                                                             int32_t k);
+KVI_API kvi_status kvi_graph_retrieve_and_inject(
+    const kvi_store_view *store, const int32_t *d_graph, int32_t degree, int32_t R,
+    const float *d_queries, const int32_t *d_seeds, const kvi_graph_search_params *params, int32_t k,
+    const int32_t *d_start_pos, const int32_t *d_block_tables, const int32_t *d_table_lens,
+    int32_t max_blocks, const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids,
+    float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes, int32_t *d_status,
+    kvi_stream_t stream);
+
 /* Store files.  The paper encodes a user's memory facts offline into a
  * long-lived store of pre-RoPE K/V and embeddings, which may sit in host
  * DRAM when it outgrows HBM (the review's Summary: facts are encoded

@@ -25,5 +25,6 @@ from ._binding import (  # noqa: F401
     ERR_IO, StoreFileInfo, kvi_store_save, kvi_store_file_info_read, kvi_store_load, load_store,
     MAX_GRAPH_DEGREE, MAX_GRAPH_BEAM, MAX_GRAPH_FRONTIER, GraphSearchParams,
     kvi_graph_build_workspace_bytes, kvi_graph_build, kvi_graph_search_workspace_bytes,
-    kvi_graph_search, graph_search_params,
+    kvi_graph_search, graph_search_params, kvi_graph_retrieve_and_inject_workspace_bytes,
+    kvi_graph_retrieve_and_inject,
 )

@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "kvi_plan_launch", "kvi_plan_destroy", "kvi_plan_create_fused_io", "kvi_store_save",
     "kvi_store_file_info_read", "kvi_store_load", "kvi_graph_build_workspace_bytes",
     "kvi_graph_build", "kvi_graph_search_workspace_bytes", "kvi_graph_search",
+    "kvi_graph_retrieve_and_inject_workspace_bytes", "kvi_graph_retrieve_and_inject",
 )
 MAX_GRAPH_DEGREE = 128
 MAX_GRAPH_BEAM = 256
@@ -157,6 +158,11 @@ def load_library(path: str | None = None):
         "kvi_graph_search_workspace_bytes": (sz, [i32, i64]),
         "kvi_graph_search": (S, [ctypes.POINTER(StoreView), P, i32, i32, P, P,
                                  ctypes.POINTER(GraphSearchParams), i32, P, P, P, P, P, sz, P, P]),
+        "kvi_graph_retrieve_and_inject_workspace_bytes": (sz, [i32, i64, i32, i32]),
+        "kvi_graph_retrieve_and_inject": (S, [ctypes.POINTER(StoreView), P, i32, i32, P, P,
+                                              ctypes.POINTER(GraphSearchParams), i32, P, P, P, i32,
+                                              ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P,
+                                              P, P, sz, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -478,6 +484,25 @@ def kvi_graph_search(store: StoreView, graph, degree: int, R: int, queries, seed
                                 _ptr(queries), _ptr(seeds), ctypes.byref(params), int(k),
                                 _ptr(ids), _ptr(scores), _ptr(count), _ptr(stats), _ptr(ws), nb,
                                 _ptr(status), _stream(stream)), "kvi_graph_search")
+
+
+def kvi_graph_retrieve_and_inject_workspace_bytes(R: int, n_facts: int, beam: int, k: int) -> int:
+    return load_library().kvi_graph_retrieve_and_inject_workspace_bytes(int(R), int(n_facts),
+                                                                        int(beam), int(k))
+
+
+def kvi_graph_retrieve_and_inject(store: StoreView, graph, degree: int, R: int, queries, seeds,
+                                  params: GraphSearchParams, k: int, start_pos, block_tables,
+                                  table_lens, max_blocks: int, cache, rope: Rope, ids, scores, pos,
+                                  ws, status=None, stream=None) -> None:
+    lib = load_library()
+    c = cache.struct if hasattr(cache, "struct") else cache
+    _check(lib.kvi_graph_retrieve_and_inject(
+        ctypes.byref(store), _ptr(graph), int(degree), int(R), _ptr(queries), _ptr(seeds),
+        ctypes.byref(params), int(k), _ptr(start_pos), _ptr(block_tables), _ptr(table_lens),
+        int(max_blocks), ctypes.byref(c), ctypes.byref(rope), _ptr(ids), _ptr(scores), _ptr(pos),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+        "kvi_graph_retrieve_and_inject")
 
 
 def kvi_trace_stages(events) -> None:

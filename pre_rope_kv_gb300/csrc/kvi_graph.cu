@@ -232,9 +232,25 @@ __global__ void __launch_bounds__(T) graph_search_kernel(const __grid_constant__
     }
 
     const int cnt = min(nc, p.k);
-    for (int j = tid; j < p.k; j += T) {
-        p.ids[(int64_t)r * p.k + j] = j < cnt ? sm.id[cur][j] : -1;
-        p.scores[(int64_t)r * p.k + j] = j < cnt ? key_score(sm.key[cur][j]) : __int_as_float(0x7fc00000);
+    if (p.cand_ids) {
+        // the beam, already in rank order, becomes the selector's candidate
+        // list: slot j holds the j-th best fact, its key and its length
+        // (-1 when its extent lies outside the store, as the scan reports)
+        for (int j = tid; j < nc; j += T) {
+            const int32_t f = sm.id[cur][j];
+            const int64_t at = (int64_t)r * p.cand_stride + j;
+            const int64_t s0 = __ldg(p.fact_start + f);
+            const int32_t l0 = __ldg(p.fact_len + f);
+            p.cand_ids[at] = f;
+            p.cand_keys[at] = sm.key[cur][j];
+            p.cand_lens[at] = (l0 >= 0 && s0 >= 0 && s0 + l0 <= p.n_tokens) ? l0 : -1;
+        }
+        if (tid == 0) p.cand_n[r] = nc;
+    } else {
+        for (int j = tid; j < p.k; j += T) {
+            p.ids[(int64_t)r * p.k + j] = j < cnt ? sm.id[cur][j] : -1;
+            p.scores[(int64_t)r * p.k + j] = j < cnt ? key_score(sm.key[cur][j]) : __int_as_float(0x7fc00000);
+        }
     }
     if (tid == 0) {
         if (p.count) p.count[r] = cnt;

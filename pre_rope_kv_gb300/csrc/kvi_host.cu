@@ -1061,6 +1061,76 @@ bool graph_build_args_ok(int64_t n_facts, int32_t degree)
            (int64_t)degree < n_facts;
 }
 
+
+struct GraphFusedWs {
+    SharedWs sel;  // the selector's regions and candidate lists (beam slots)
+    size_t visited, total;
+};
+
+GraphFusedWs graph_fused_layout(int32_t R, int64_t n_facts, int32_t beam, int32_t k)
+{
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    GraphFusedWs x{};
+    x.sel = shared_layout(R, beam, k);
+    x.visited = up(x.sel.total);
+    x.total = up(x.visited + (size_t)R * (size_t)((n_facts + 31) / 32) * 4);
+    return x;
+}
+
+// The argument checks kvi_graph_search and the fused graph call share.
+kvi_status check_graph_search(const kvi_store_view *store, const int32_t *d_graph, int32_t degree,
+                              int32_t R, const float *d_queries, const int32_t *d_seeds,
+                              const kvi_graph_search_params *params, int32_t k, bool inject)
+{
+    kvi_status st = check_store(store, true, inject);
+    if (st != KVI_OK) return st;
+    if (!d_graph || !aligned(d_graph, 4)) return fail(KVI_ERR_INVALID_ARG, "graph is NULL or misaligned");
+    if (degree < 1 || degree > KVI_MAX_GRAPH_DEGREE)
+        return fail(KVI_ERR_INVALID_ARG, "degree=%d outside [1, %d]", degree, KVI_MAX_GRAPH_DEGREE);
+    if (R < 1 || R > 65535) return fail(KVI_ERR_INVALID_ARG, "R=%d outside [1, 65535]", R);
+    if (!d_queries || !aligned(d_queries, 16))
+        return fail(KVI_ERR_INVALID_ARG, "queries must be a 16-byte aligned device pointer");
+    if (!d_seeds || !params) return fail(KVI_ERR_INVALID_ARG, "seeds or params is NULL");
+    const kvi_graph_search_params P = *params;
+    if (k < 1 || P.beam < k || P.beam > KVI_MAX_GRAPH_BEAM)
+        return fail(KVI_ERR_INVALID_ARG, "need 1 <= k=%d <= beam=%d <= %d", k, P.beam, KVI_MAX_GRAPH_BEAM);
+    if (P.width < 1 || (int64_t)P.width * degree > KVI_MAX_GRAPH_FRONTIER)
+        return fail(KVI_ERR_INVALID_ARG, "width=%d: need 1 <= width * degree <= %d", P.width,
+                    KVI_MAX_GRAPH_FRONTIER);
+    if (P.max_iters < 0 || P.n_seeds < 1 || P.n_seeds > KVI_MAX_GRAPH_FRONTIER)
+        return fail(KVI_ERR_INVALID_ARG, "max_iters=%d < 0 or n_seeds=%d outside [1, %d]", P.max_iters,
+                    P.n_seeds, KVI_MAX_GRAPH_FRONTIER);
+    return KVI_OK;
+}
+
+GraphSearchParams graph_params(const kvi_store_view *store, const int32_t *d_graph, int32_t degree, int32_t R,
+                               const float *d_queries, const int32_t *d_seeds,
+                               const kvi_graph_search_params &P, int32_t k, uint32_t *visited,
+                               int32_t *d_status)
+{
+    GraphSearchParams gp{};
+    gp.emb = store->emb;
+    gp.N = store->n_facts;
+    gp.E = store->g.embed_dim;
+    gp.graph = d_graph;
+    gp.degree = degree;
+    gp.queries = d_queries;
+    gp.seeds = d_seeds;
+    gp.R = R;
+    gp.n_seeds = P.n_seeds;
+    gp.beam = P.beam;
+    gp.width = P.width;
+    gp.max_iters = P.max_iters;
+    gp.k = k;
+    gp.visited = visited;
+    gp.vis_words = (store->n_facts + 31) / 32;
+    gp.status = d_status;
+    gp.fact_start = store->fact_start;
+    gp.fact_len = store->fact_len;
+    gp.n_tokens = store->n_tokens;
+    return gp;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1117,50 +1187,126 @@ kvi_status kvi_graph_search(const kvi_store_view *store, const int32_t *d_graph,
                             float *d_scores, int32_t *d_count, int32_t *d_stats, void *d_ws,
                             size_t ws_bytes, int32_t *d_status, kvi_stream_t stream)
 {
-    kvi_status st = check_store(store, true, false);
+    kvi_status st = check_graph_search(store, d_graph, degree, R, d_queries, d_seeds, params, k, false);
     if (st != KVI_OK) return st;
-    if (!d_graph || !aligned(d_graph, 4)) return fail(KVI_ERR_INVALID_ARG, "graph is NULL or misaligned");
-    if (degree < 1 || degree > KVI_MAX_GRAPH_DEGREE)
-        return fail(KVI_ERR_INVALID_ARG, "degree=%d outside [1, %d]", degree, KVI_MAX_GRAPH_DEGREE);
-    if (R < 1 || R > 65535) return fail(KVI_ERR_INVALID_ARG, "R=%d outside [1, 65535]", R);
-    if (!d_queries || !aligned(d_queries, 16))
-        return fail(KVI_ERR_INVALID_ARG, "queries must be a 16-byte aligned device pointer");
-    if (!d_seeds || !params || !d_ids || !d_scores)
-        return fail(KVI_ERR_INVALID_ARG, "seeds, params, ids or scores is NULL");
-    const kvi_graph_search_params P = *params;
-    if (k < 1 || P.beam < k || P.beam > KVI_MAX_GRAPH_BEAM)
-        return fail(KVI_ERR_INVALID_ARG, "need 1 <= k=%d <= beam=%d <= %d", k, P.beam, KVI_MAX_GRAPH_BEAM);
-    if (P.width < 1 || (int64_t)P.width * degree > KVI_MAX_GRAPH_FRONTIER)
-        return fail(KVI_ERR_INVALID_ARG, "width=%d: need 1 <= width * degree <= %d", P.width,
-                    KVI_MAX_GRAPH_FRONTIER);
-    if (P.max_iters < 0 || P.n_seeds < 1 || P.n_seeds > KVI_MAX_GRAPH_FRONTIER)
-        return fail(KVI_ERR_INVALID_ARG, "max_iters=%d < 0 or n_seeds=%d outside [1, %d]", P.max_iters,
-                    P.n_seeds, KVI_MAX_GRAPH_FRONTIER);
+    if (!d_ids || !d_scores) return fail(KVI_ERR_INVALID_ARG, "ids or scores is NULL");
     const size_t need = kvi_graph_search_workspace_bytes(R, store->n_facts);
     if (!d_ws || !aligned(d_ws, 256) || ws_bytes < need)
         return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", need);
-    GraphSearchParams gp{};
-    gp.emb = store->emb;
-    gp.N = store->n_facts;
-    gp.E = store->g.embed_dim;
-    gp.graph = d_graph;
-    gp.degree = degree;
-    gp.queries = d_queries;
-    gp.seeds = d_seeds;
-    gp.R = R;
-    gp.n_seeds = P.n_seeds;
-    gp.beam = P.beam;
-    gp.width = P.width;
-    gp.max_iters = P.max_iters;
-    gp.k = k;
+    GraphSearchParams gp = graph_params(store, d_graph, degree, R, d_queries, d_seeds, *params, k,
+                                        static_cast<uint32_t *>(d_ws), d_status);
     gp.ids = d_ids;
     gp.scores = d_scores;
     gp.count = d_count;
     gp.stats = d_stats;
-    gp.visited = static_cast<uint32_t *>(d_ws);
-    gp.vis_words = (store->n_facts + 31) / 32;
-    gp.status = d_status;
     KVI_CUDA(launch_graph_search(gp, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+}  // extern "C"
+
+
+extern "C" {
+
+size_t kvi_graph_retrieve_and_inject_workspace_bytes(int32_t R, int64_t n_facts, int32_t beam, int32_t k)
+{
+    if (R < 1 || R > KVI_MAX_REQUESTS || n_facts < 1 || n_facts > 0x7fffffff || k < 1 || beam < k ||
+        beam > KVI_MAX_GRAPH_BEAM)
+        return 0;
+    return graph_fused_layout(R, n_facts, beam, k).total;
+}
+
+kvi_status kvi_graph_retrieve_and_inject(const kvi_store_view *store, const int32_t *d_graph, int32_t degree,
+                                         int32_t R, const float *d_queries, const int32_t *d_seeds,
+                                         const kvi_graph_search_params *params, int32_t k,
+                                         const int32_t *d_start_pos, const int32_t *d_block_tables,
+                                         const int32_t *d_table_lens, int32_t max_blocks,
+                                         const kvi_paged_cache *cache, const kvi_rope *rope, int32_t *d_ids,
+                                         float *d_scores, int32_t *d_pos, void *d_ws, size_t ws_bytes,
+                                         int32_t *d_status, kvi_stream_t stream)
+{
+    kvi_status st = check_graph_search(store, d_graph, degree, R, d_queries, d_seeds, params, k, true);
+    if (st != KVI_OK) return st;
+    if (R > KVI_MAX_REQUESTS) return fail(KVI_ERR_INVALID_ARG, "R=%d > %d", R, KVI_MAX_REQUESTS);
+    if (!d_ids || !d_scores || !d_pos) return fail(KVI_ERR_INVALID_ARG, "ids, scores or pos is NULL");
+    if (!d_start_pos || !d_block_tables || !d_table_lens)
+        return fail(KVI_ERR_INVALID_ARG, "start positions, block tables or table lengths is NULL");
+    if (max_blocks < 1) return fail(KVI_ERR_INVALID_ARG, "max_blocks < 1");
+    st = check_cache(cache, store->g);
+    if (st != KVI_OK) return st;
+    if ((int64_t)max_blocks * cache->block_size > 0x7fffffff)
+        return fail(KVI_ERR_INVALID_ARG, "max_blocks * block_size must be < 2^31");
+    st = check_rope(rope);
+    if (st != KVI_OK) return st;
+    const GraphFusedWs W = graph_fused_layout(R, store->n_facts, params->beam, k);
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < W.total)
+        return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", W.total);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float4 *table;
+    int32_t positions;
+    st = rope_get(*rope, store->g.head_dim, clamp_rope((int64_t)max_blocks * cache->block_size), s, &table,
+                  &positions);
+    if (st != KVI_OK) return st;
+    const bool trace = t_trace_n == 3;
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[0], s));
+    char *ws = static_cast<char *>(d_ws);
+    const SharedWs &L = W.sel;
+    GraphSearchParams gp = graph_params(store, d_graph, degree, R, d_queries, d_seeds, *params, k,
+                                        reinterpret_cast<uint32_t *>(ws + W.visited), d_status);
+    gp.cand_ids = reinterpret_cast<int32_t *>(ws + L.cand);
+    gp.cand_keys = reinterpret_cast<uint64_t *>(ws + L.w.keys);
+    gp.cand_lens = reinterpret_cast<int32_t *>(ws + L.w.lens);
+    gp.cand_n = reinterpret_cast<int32_t *>(ws + L.cand_n);
+    gp.cand_stride = L.w.key_stride;
+    KVI_CUDA(launch_graph_search(gp, s));
+
+    const PieceGeom pg = piece_geom(store->g.kv_heads, store->g.head_dim, cache->block_size);
+    SelectParams lp = shared_select_params(store, R, k, L, ws, d_ids, d_scores);
+    lp.place = 1;
+    lp.start_pos = d_start_pos;
+    lp.table_lens = d_table_lens;
+    lp.max_blocks = max_blocks;
+    lp.block_size = cache->block_size;
+    lp.pg = pg;
+    lp.pos = d_pos;
+    lp.slot_len = reinterpret_cast<int32_t *>(ws + L.w.slot_len);
+    lp.pc = reinterpret_cast<int32_t *>(ws + L.w.pc);
+    lp.npc = reinterpret_cast<int32_t *>(ws + L.w.npc);
+    lp.rows = reinterpret_cast<int64_t *>(ws + L.w.rows);
+    lp.work = reinterpret_cast<unsigned long long *>(ws + L.w.work);
+    lp.status = d_status;
+    KVI_CUDA(launch_select(lp, s, false));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
+
+    InjectParams ip{};
+    ip.store.single = *store;
+    ip.store.many = nullptr;
+    ip.L = store->g.layers;
+    ip.H = store->g.kv_heads;
+    ip.D = store->g.head_dim;
+    ip.pg = pg;
+    ip.fused = 1;
+    ip.ids = d_ids;
+    ip.pos = d_pos;
+    ip.R = R;
+    ip.k = k;
+    ip.slot_len = lp.slot_len;
+    ip.pc = lp.pc;
+    ip.npc = lp.npc;
+    ip.rows = lp.rows;
+    ip.work = lp.work;
+    ip.block_tables = d_block_tables;
+    ip.table_lens = d_table_lens;
+    ip.max_blocks = max_blocks;
+    ip.num_blocks = cache->num_blocks;
+    ip.block_size = cache->block_size;
+    ip.rope = table;
+    ip.rope_positions = positions;
+    ip.pairing = rope->pairing;
+    ip.status = d_status;
+    for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
+    KVI_CUDA(launch_inject(ip, s, !trace));
+    if (trace) KVI_CUDA(cudaEventRecord(t_trace[2], s));
     return KVI_OK;
 }
 

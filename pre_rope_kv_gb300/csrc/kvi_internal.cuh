@@ -192,6 +192,16 @@ struct GraphSearchParams {
     uint32_t *visited;      // [R][vis_words] bitmaps
     int64_t vis_words;
     int32_t *status;
+    // fused calls: the final beam as the selector's candidates (slots in
+    // rank order), with exact keys and validated lengths; ids/scores unused
+    int32_t *cand_ids;      // [R][cand_stride] or null
+    uint64_t *cand_keys;
+    int32_t *cand_lens;
+    int32_t *cand_n;        // [R]
+    int64_t cand_stride;
+    const int64_t *fact_start;
+    const int32_t *fact_len;
+    int64_t n_tokens;
 };
 cudaError_t launch_graph_search(const GraphSearchParams &p, cudaStream_t s);
 

@@ -252,3 +252,49 @@ def test_graph_retrieval_through_placement_and_injection():
     o_pos, _ = oracle.place(o_ids, st.len_np, start)
     assert np.array_equal(pos.cpu().numpy(), o_pos)
     kc.check_pool_full(b, [(o_ids, o_pos)])
+
+
+@pytest.mark.parametrize("R,pairing,width", [(5, 0, 1), (3, 1, 2)])
+def test_fused_graph_retrieve_and_inject_full_pool(R, pairing, width):
+    # R requests over one store through kvi_graph_retrieve_and_inject: ids,
+    # scores and positions as the oracle's search and placement give them,
+    # and the whole pool as the oracle's injection of those facts
+    w = synth.Workload(name="graph_fused", layers=2, kv_heads=4, head_dim=64, rope_theta=5e5,
+                       block_size=16, n_facts=900, len_lo=1, len_hi=25, len_dist="uniform",
+                       embed_dim=128, requests=R, k=18, start=5, start_hi=0, seed=960 + R,
+                       store="dense")
+    b = synth.build_workload(w)
+    b.stores = [b.stores[0]] * R  # every request reads request 0's store
+    st = b.stores[0]
+    emb = st.emb_np
+    degree, beam, k = 24, 40, w.k
+    graph = oracle.graph_build(emb, degree)
+    rng = np.random.default_rng(961 + R)
+    seeds = synth.graph_seeds(rng, w.n_facts, R, 10)
+    view = kc.views_of(b)[0]
+    params = kvi.graph_search_params(beam, width, 300, 10)
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    pos = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_retrieve_and_inject_workspace_bytes(R, w.n_facts, beam, k),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvi.kvi_graph_retrieve_and_inject(
+        view, torch.from_numpy(graph).cuda(), degree, R, b.queries, torch.from_numpy(seeds).cuda(),
+        params, k, torch.from_numpy(b.start_pos).cuda(), torch.from_numpy(b.block_tables).cuda(),
+        torch.from_numpy(b.table_lens).cuda(), b.max_blocks, kc.cache_of(b),
+        kvi.rope(w.rope_theta, pairing), ids, sc, pos, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    g_ids, g_sc, g_pos = ids.cpu().numpy(), sc.cpu().numpy(), pos.cpu().numpy()
+    placements = []
+    for r in range(R):
+        o_ids, o_sc, o_cnt, _, _ = oracle.graph_search(b.queries_np[r], emb, graph, seeds[r], beam,
+                                                       width, 300, k)
+        assert o_cnt == k
+        assert np.array_equal(g_ids[r], o_ids), r
+        assert np.all(np.abs(g_sc[r] - o_sc) <= 1e-4 * np.abs(o_sc) + 1e-7), r
+        o_pos, _ = oracle.place(o_ids, st.len_np, int(b.start_pos[r]))
+        assert np.array_equal(g_pos[r], o_pos), r
+        placements.append((o_ids, o_pos))
+    kc.check_pool_full(b, placements, rope=oracle.rope_spec(w.rope_theta, w.head_dim, pairing))
