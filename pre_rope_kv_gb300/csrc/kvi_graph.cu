@@ -162,8 +162,9 @@ __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new,
     return min(beam, nc + n_new);
 }
 
+// 64 registers a thread: 4 CTAs of 256 threads (or 2 of 512) per SM
 template <int T>
-__global__ void __launch_bounds__(T) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
+__global__ void __launch_bounds__(T, 1024 / T) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
 {
     __shared__ SearchSmem sm;
     const int r = blockIdx.x;
