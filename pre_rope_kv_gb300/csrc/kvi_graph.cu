@@ -79,45 +79,60 @@ __device__ __forceinline__ void visit(SearchSmem &sm, uint32_t *vis, int64_t N, 
     if (fresh) sm.new_id[base + __popc(mask & ((1u << lane) - 1u))] = f;
 }
 
-// Dot2 key of every new fact, one row per warp: each lane loads up to
-// kRowChunk float4 of the row before any arithmetic, so that a 1024-d row
-// costs one round trip to memory (an iteration typically finds fewer new
-// facts than there are warps).
+// Dot2 key of every new fact.  A warp scores ROWS rows at a time, and each
+// lane loads up to kRowChunk float4 of each of them before any arithmetic,
+// so that a 1024-d row costs one round trip to memory.  ROWS = 2 when one
+// CTA runs per query and SM (registers to spare), 1 in batches.
 constexpr int kRowChunk = 8;
 
-template <int T>
+template <int T, int ROWS>
 __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem &sm, const float *q, int n_new)
 {
     constexpr int kSearchWarps = T / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float4 *q4 = reinterpret_cast<const float4 *>(q);
     const int E4 = p.E / 4;
-    for (int m = warp; m < n_new; m += kSearchWarps) {
-        const int32_t f = sm.new_id[m];
-        const float4 *a = reinterpret_cast<const float4 *>(p.emb + (int64_t)f * p.E);
-        // a scored fact may become a parent: bring its graph row into L2 now,
-        // so that expanding it later costs an L2 hit, not a DRAM round trip
-        if (lane * 32 < p.degree)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.graph + (int64_t)f * p.degree + lane * 32));
-        Dot2x4 da;
-        da.zero();
+    for (int m0 = ROWS * warp; m0 < n_new; m0 += ROWS * kSearchWarps) {
+        const float4 *row[ROWS];
+#pragma unroll
+        for (int x = 0; x < ROWS; ++x) {
+            const int m = min(m0 + x, n_new - 1);  // a missing second row re-reads the first
+            const int32_t f = sm.new_id[m];
+            row[x] = reinterpret_cast<const float4 *>(p.emb + (int64_t)f * p.E);
+            // a scored fact may become a parent: bring its graph row into
+            // L2 now, so that expanding it later costs an L2 hit
+            if (m == m0 + x && lane * 32 < p.degree)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.graph + (int64_t)f * p.degree + lane * 32));
+        }
+        Dot2x4 acc[ROWS];
+#pragma unroll
+        for (int x = 0; x < ROWS; ++x) acc[x].zero();
         for (int v0 = 0; v0 < E4; v0 += 32 * kRowChunk) {
-            float4 ra[kRowChunk];
+            float4 r[ROWS][kRowChunk];
 #pragma unroll
             for (int u = 0; u < kRowChunk; ++u) {
                 const int v = v0 + lane + 32 * u;
-                if (v < E4) ra[u] = ld_stream_f4(a + v);
+#pragma unroll
+                for (int x = 0; x < ROWS; ++x)
+                    if (v < E4) r[x][u] = ld_stream_f4(row[x] + v);
             }
 #pragma unroll
             for (int u = 0; u < kRowChunk; ++u) {
                 const int v = v0 + lane + 32 * u;
-                if (v < E4) da.add(__ldg(q4 + v), ra[u]);
+                if (v < E4) {
+                    const float4 qv = __ldg(q4 + v);
+#pragma unroll
+                    for (int x = 0; x < ROWS; ++x) acc[x].add(qv, r[x][u]);
+                }
             }
         }
-        float sa, ca;
-        da.combine(sa, ca);
-        warp_reduce_pair(sa, ca);
-        if (lane == 0) sm.new_key[m] = score_key(sa, ca);
+#pragma unroll
+        for (int x = 0; x < ROWS; ++x) {
+            float s, c;
+            acc[x].combine(s, c);
+            warp_reduce_pair(s, c);
+            if (lane == 0 && m0 + x < n_new) sm.new_key[m0 + x] = score_key(s, c);
+        }
     }
 }
 
@@ -162,9 +177,10 @@ __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new,
     return min(beam, nc + n_new);
 }
 
-// 64 registers a thread: 4 CTAs of 256 threads (or 2 of 512) per SM
+// batches: 64 registers a thread, 4 CTAs of 256 threads per SM; alone: one
+// CTA of 512 threads per SM, up to 128 registers
 template <int T>
-__global__ void __launch_bounds__(T, 1024 / T) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
+__global__ void __launch_bounds__(T, T >= 512 ? 1 : 4) graph_search_kernel(const __grid_constant__ GraphSearchParams p)
 {
     __shared__ SearchSmem sm;
     const int r = blockIdx.x;
@@ -183,7 +199,7 @@ __global__ void __launch_bounds__(T, 1024 / T) graph_search_kernel(const __grid_
     }
     __syncthreads();
     int n_new = sm.n_new;
-    score_new<T>(p, sm, q, n_new);
+    score_new<T, (T >= 512 ? 2 : 1)>(p, sm, q, n_new);
     __syncthreads();
     int cur = 0;
     int nc = merge<T>(sm, cur ^ 1, 0, n_new, p.beam);  // into buffer 0 from an empty beam
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(T, 1024 / T) graph_search_kernel(const __grid_
         __syncthreads();
         n_new = sm.n_new;
         scored += n_new;
-        score_new<T>(p, sm, q, n_new);
+        score_new<T, (T >= 512 ? 2 : 1)>(p, sm, q, n_new);
         __syncthreads();
         nc = merge<T>(sm, cur, nc, n_new, p.beam);
         cur ^= 1;
