@@ -938,11 +938,6 @@ select_kernel(const __grid_constant__ SelectParams p)
                             sm.cand_key[at] = kr[m];
                             sm.cand_id[at] = (int32_t)i;
                             sm.cand_len[at] = lr[m];
-                            // placement reads the winners' first rows: start
-                            // the candidates' extents on their way into L2
-                            // while the ranking runs
-                            if (p.place && !p.cand)
-                                asm volatile("prefetch.global.L2 [%0];" ::"l"(st.fact_start + i));
                         }
                         ++at;
                     }
