@@ -6,10 +6,7 @@
 // is a dense contraction S = Q E^T, so here it runs on the 5th-generation
 // tensor cores instead of R separate scans of the matrix:
 //
-//   coarse_kernel   one CTA per 128 facts (a cluster of two, each taking
-//                   half of E, when the tiles do not fill the GPU; the second
-//                   hands its partial sums to the first through distributed
-//                   shared memory).  A TMA producer warp (one box per
+//   coarse_kernel   one CTA per 128 facts.  A TMA producer warp (one box per
 //                   lane) streams the facts' rows and all queries through a
 //                   ring of 128-byte swizzled stages; one thread issues
 //                   tcgen05.mma (kind::tf32,
@@ -117,40 +114,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
-// Sixteen consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&v)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(addr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Every thread of both CTAs of the cluster arrives, then waits.
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// A float into the shared memory of CTA `rank` of this cluster, at the
-// offset of the local address `local`.
-__device__ __forceinline__ void st_remote(const void *local, uint32_t rank, float v)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
 __device__ __forceinline__ float sq_row32(const float *row)
 {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
@@ -179,15 +142,8 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     uint8_t *b_st = base + (size_t)S * kStageBytesA;
     CoarseSmemTail &tl = *reinterpret_cast<CoarseSmemTail *>(b_st + (size_t)S * stage_b);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // K split: the pair of CTAs of a cluster takes the two halves of E for
-    // one tile; rank 1 hands its partial sums to rank 0 at the end
-    const int ks = p.ks;
-    const int tile = blockIdx.x / ks;
-    const int kh = blockIdx.x - tile * ks;
-    const int nk_all = (p.E + kChunk - 1) / kChunk;
-    const int nk_part = (nk_all + ks - 1) / ks;
-    const int kbeg = kh * nk_part;
-    const int nk = min(nk_all - kbeg, nk_part);  // >= 1: a split needs nk_all >= 2
+    const int tile = blockIdx.x;
+    const int nk = (p.E + kChunk - 1) / kChunk;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -210,12 +166,6 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tl.tmem_base;
     bool ok = true;
-    // the epilogue warps' row norms and query norms, and whether the MMAs
-    // finished (thread L of warps 2-5 owns fact row L of the tile)
-    const int q = warp & 3;
-    const int L = 32 * q + lane;
-    float en2 = 0.f, qa = 0.f, qb = 0.f;
-    bool done = false;
 
     if (warp == 0) {
         // the stage is loaded as boxes of kBoxRowsA fact rows and kBoxRowsB
@@ -242,10 +192,10 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
             for (int j = lane; j < na + nb; j += 32) {
                 if (j < na)
                     tma_2d(saddr(a_st + (size_t)s * kStageBytesA + (size_t)j * kBoxRowsA * 128), &tm_emb,
-                           (kbeg + kc) * kChunk, tile * kTileM + j * kBoxRowsA, fb);
+                           kc * kChunk, tile * kTileM + j * kBoxRowsA, fb);
                 else
                     tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
-                           (kbeg + kc) * kChunk, (j - na) * kBoxRowsB, fb);
+                           kc * kChunk, (j - na) * kBoxRowsB, fb);
             }
         }
     } else if (warp == 1) {
@@ -285,6 +235,9 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     } else {
         // warps 2-5: thread L owns tensor-memory lane L = fact row L of the
         // tile (a warp reaches the 32 lanes of its own subpartition, warp % 4)
+        const int q = warp & 3;
+        const int L = 32 * q + lane;
+        float en2 = 0.f, qa = 0.f, qb = 0.f;
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % S;
             const bool got = wait_bar(saddr(&tl.full[s]), (uint32_t)((kc / S) & 1));
@@ -306,69 +259,37 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
         if (L < p.Rp) tl.qn2[L] = qa;
         if (L + 128 < p.Rp) tl.qn2[L + 128] = qb;
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        done = __all_sync(0xffffffffu, ok && wait_bar(saddr(&tl.mma_done), 0));
-        if (!done && lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
-        if (done) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    }
-
-    // the pair's exchange: once both CTAs' MMAs are done (so rank 0's ring
-    // is idle), rank 1 writes its partial scores [Rp][128], row norms and
-    // query norms into rank 0's ring; rank 0 adds them to its own
-    float *xbuf = reinterpret_cast<float *>(base);                 // [Rp][kTileM]
-    float *xen = xbuf + (size_t)p.Rp * kTileM;                      // [kTileM]
-    float *xq = xen + kTileM;                                       // [Rp]
-    float *xok = xq + p.Rp;                                         // [4]: rank 1's warps wrote
-    const bool epi = warp >= 2;
-    bool have = true;  // rank 0: the partner's partial sums for this warp's rows arrived
-    if (ks == 2) {
-        // rank 0 clears the flags while its ring is its own
-        if (epi && kh == 0 && lane == 0) xok[q] = 0.f;
-        cluster_sync_all();
-        if (epi && kh == 1 && done) {
+        const bool done = ok && wait_bar(saddr(&tl.mma_done), 0);
+        if (__all_sync(0xffffffffu, done)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int64_t fact = (int64_t)tile * kTileM + L;
+            const float en = sqrtf(en2);
+            const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
             for (int c0 = 0; c0 < p.Rp; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                    "%15}, [%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                      "=r"(v[14]), "=r"(v[15])
+                    : "r"(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (fact < p.N) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) st_remote(xbuf + (size_t)(c0 + j) * kTileM + L, 0, __uint_as_float(v[j]));
-            }
-            st_remote(xen + L, 0, en2);
-            if (L < p.Rp) st_remote(xq + L, 0, qa);
-            if (L + 128 < p.Rp) st_remote(xq + L + 128, 0, qb);
-            __syncwarp();
-            if (lane == 0) st_remote(xok + q, 0, 1.f);
-        }
-        cluster_sync_all();
-        if (epi && kh == 0) {
-            have = xok[q] == 1.f;
-            if (!have && lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
-        }
-    }
-    if (epi && kh == 0 && done && have) {
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int64_t fact = (int64_t)tile * kTileM + L;
-        const float en = sqrtf(ks == 2 ? en2 + xen[L] : en2);
-        const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
-        for (int c0 = 0; c0 < p.Rp; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-            if (fact < p.N) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = c0 + j;
-                    if (r < p.R) {
-                        float c = __uint_as_float(v[j]);
-                        float qn2 = tl.qn2[r];
-                        if (ks == 2) {
-                            c = __fadd_rn(c, xbuf[(size_t)r * kTileM + L]);
-                            qn2 = __fadd_rn(qn2, xq[r]);
+                    for (int j = 0; j < 16; ++j) {
+                        const int r = c0 + j;
+                        if (r < p.R) {
+                            const float c = __uint_as_float(v[j]);
+                            const float eps = __fmaf_ru(rel * sqrtf(tl.qn2[r]), en * 1.0001f, 7.9e-31f);
+                            p.lo[(int64_t)r * p.stride + fact] = __fsub_rd(c, eps);
+                            p.hi[(int64_t)r * p.stride + fact] = __fadd_ru(c, eps);
                         }
-                        const float eps = __fmaf_ru(rel * sqrtf(qn2), en * 1.0001f, 7.9e-31f);
-                        p.lo[(int64_t)r * p.stride + fact] = __fsub_rd(c, eps);
-                        p.hi[(int64_t)r * p.stride + fact] = __fadd_ru(c, eps);
                     }
                 }
             }
+        } else if (lane == 0) {
+            record_status(p.status, KVI_ERR_TIMEOUT);
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -453,28 +374,8 @@ cudaError_t launch_coarse(const CoarseParams &p0, const float *emb, int64_t n_fa
     for (int rp = 16; rp <= KVI_MAX_SHARED_QUERIES; rp += 16) most = std::max(most, coarse_smem_bytes(rp));
     e = smem_opt_in(coarse_kernel, (int)most);
     if (e != cudaSuccess) return e;
-    // fewer tiles than SMs: split E over a cluster of two CTAs per tile, so
-    // that twice as many SMs stream the embeddings
-    DeviceInfo di;
-    e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    const int64_t tiles = (n_facts + kTileM - 1) / kTileM;
-    const int nk_all = (p.E + kChunk - 1) / kChunk;
-    p.ks = (nk_all >= 2 && tiles < di.sms) ? 2 : 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles * p.ks));
-    cfg.blockDim = dim3(kCoarseThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.ks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, coarse_kernel, te, tq, p);
-    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((n_facts + kTileM - 1) / kTileM);
+    coarse_kernel<<<grid, kCoarseThreads, smem, s>>>(te, tq, p);
     return cudaGetLastError();
 }
 
