@@ -676,6 +676,15 @@ def run_ours(args):
         out["rope_variants_us_per_request"] = {n: round(v * 1e6, 2) for n, v in var.items()}
         out["shared_store_64_requests"] = bench.shared_store(64, k, 10, args.warmup)
         hs = bench.host_store(k, 10, args.warmup)
+        gi = graph_index_measure(100_000, "latent", k, 10, args.warmup, full=False)
+        out["graph_index_100k"] = {
+            "recall_at_k": gi["recall_at_k"], "queries_per_s": gi["value"],
+            "latency_us_one_query": gi["latency_us_one_query"],
+            "exact_shared_us_per_query": gi["exact"]["shared_256_queries_us_per_query"],
+            "exact_scan_one_query_us": gi["exact"]["scan_one_query_us"],
+            "build_s": gi["build_s"], "search_hbm_frac": gi["roofline"]["frac"],
+            "note": "graph index (degree 64, beam 64) on 100k facts of intrinsic dimension 32; "
+                    "1024 queries per call with landmark seeds; bench.py --graph-index for 1M"}
         hb = statistics.mean(step_tokens) * w.token_bytes
         out["host_store_kv"] = {"latency_us_per_request": round(hs * 1e6, 2),
                                 "injected_gb_per_s": round(hb / hs / 1e9, 2),
@@ -750,23 +759,32 @@ def run_shared_retrieval(args):
 
 
 def run_graph_index(args):
+    """The graph index on --graph-facts 1024-d embeddings; prints one JSON
+    line (not the bench line)."""
+    from pre_rope_kv_gb300 import build as kbuild
+    kbuild.build()
+    out = graph_index_measure(args.graph_facts, args.graph_data, args.k, args.steps, args.warmup,
+                              full=True)
+    print(json.dumps(out), flush=True)
+
+
+def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
     """The graph index (the review's GPU ANN index, 64 neighbours and beam
-    64) on a clustered store of --graph-facts 1024-d embeddings: graph build
-    time, search latency of one query, throughput of 1024 queries in one
-    call, recall@k against the exact top-k of the shared-store path, and the
-    exact scan of one query timed beside it.  L2 is flushed before every
-    timed call.  Prints one JSON line (not the bench line)."""
+    64) on N facts of 1024-d embeddings: graph build time, search latency of
+    one query, throughput of 1024 queries in one call, recall@k against the
+    exact top-k of the shared-store path, and the exact paths timed beside
+    it; with `full`, also a beam sweep and one request through
+    retrieve-and-inject (exact and graph) over a 33 GB K/V arena.  L2 is
+    flushed before every timed call."""
     import torch
     import pre_rope_kv_gb300 as kvi
-    from pre_rope_kv_gb300 import build as kbuild
     from tests import synth
-    kbuild.build()
     kvi.load_library()
     peak, peak_kind = load_peaks()
-    N, E, D, k = args.graph_facts, 1024, 64, args.k
+    E, D = 1024, 64
     beam, width, n_seeds, R = 64, 1, 64, 1024
     clusters = max(1, N // 500)
-    if args.graph_data == "latent":
+    if graph_data == "latent":
         emb = synth.latent_rows_device(7, N, E)
         data = ("synthetic unit embeddings of intrinsic dimension 32 (random 1024 x 32 projection "
                 "of Gaussian points + 0.1 Gaussian / sqrt(E)); queries near stored facts")
@@ -812,12 +830,12 @@ def run_graph_index(args):
     ws_s = torch.empty(kvi.kvi_graph_search_workspace_bytes(R, N), dtype=torch.uint8, device="cuda")
     params = kvi.graph_search_params(beam, width, 10_000, n_seeds)
 
-    def timed(fn, steps):
-        for _ in range(args.warmup):
+    def timed(fn, n):
+        for _ in range(warmup):
             flush.zero_()
             fn()
         ts = []
-        for _ in range(steps):
+        for _ in range(n):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
@@ -860,15 +878,15 @@ def run_graph_index(args):
     search(R, rand_seeds)
     torch.cuda.synchronize()
     recall_random = recall()
-    one = timed(lambda: run(1), max(10, args.steps))
-    one_search = timed(lambda: search(1, seeds), max(10, args.steps))
+    one = timed(lambda: run(1), max(10, steps))
+    one_search = timed(lambda: search(1, seeds), max(10, steps))
     batch = timed(lambda: run(R), 5)
     batch_search = timed(lambda: search(R, seeds), 5)
     st = stats.cpu().numpy().astype(np.float64)
     recall_lm = recall()
     # the beam trades recall for work: search alone, same landmark seeds
     sweep = {}
-    for bw in (64, 128, 256):
+    for bw in ((64, 128, 256) if full else ()):
         params = kvi.graph_search_params(bw, width, 10_000, n_seeds)
         bt = timed(lambda: search(R, seeds), 3)
         sweep[str(bw)] = {"recall_at_k": round(recall(), 4), "batch_us_search_only": round(bt * 1e6, 2),
@@ -879,53 +897,55 @@ def run_graph_index(args):
     del ws_e
     ws_1 = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
     scan_s = timed(lambda: kvi.kvi_retrieve_topk(view, q[0], k, ex_ids[0], ex_sc[0], ws_1), 10)
-    # one request through the whole path at this store size: K/V in an arena
-    # (Llama-3-8B geometry, 250k token rows) holding the facts' extents
-    L_, H_, D_, B_ = 32, 8, 128, 16
-    T_ = 250_000
-    gl = torch.Generator(device="cuda")
-    gl.manual_seed(10)
-    fl_a = torch.randint(12, 49, (N,), generator=gl, device="cuda", dtype=torch.int32)
-    fs_a = torch.randint(0, T_ - 48, (N,), generator=gl, device="cuda", dtype=torch.int64)
-    kv = torch.empty((L_, 2, T_, H_, D_), dtype=torch.bfloat16, device="cuda")
-    for l in range(L_):
-        kv[l].normal_(generator=gl)
-    g8 = kvi.geometry(L_, H_, D_, E)
-    fview = kvi.store_view(g8, kv, emb, fs_a, fl_a, n_tokens=T_)
-    lview8 = kvi.store_view(g8, kv, emb[:LM], fs_a[:LM], fl_a[:LM], n_tokens=T_)
-    tl = (64 + k * 48 + B_ - 1) // B_
-    pool = torch.empty((L_, 2, tl, B_, H_, D_), dtype=torch.bfloat16, device="cuda")
-    cache = kvi.paged_cache([pool[l] for l in range(L_)], B_)
-    bt = torch.arange(tl, dtype=torch.int32, device="cuda")[None].contiguous()
-    tls = torch.full((1,), tl, dtype=torch.int32, device="cuda")
-    st64 = torch.full((1,), 64, dtype=torch.int32, device="cuda")
-    fids = torch.empty((1, k), dtype=torch.int32, device="cuda")
-    fsc = torch.empty((1, k), dtype=torch.float32, device="cuda")
-    fpos = torch.empty((1, k), dtype=torch.int32, device="cuda")
-    d_view = torch.frombuffer(bytearray(kvi.pack_store_views([fview])), dtype=torch.uint8).cuda()
-    ws_x = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
-    ws_g = torch.empty(kvi.kvi_graph_retrieve_and_inject_workspace_bytes(1, N, beam, k),
-                       dtype=torch.uint8, device="cuda")
-    params = kvi.graph_search_params(beam, width, 10_000, n_seeds)
+    fused = None
+    if full:
+        # one request through the whole path at this store size: K/V in an arena
+        # (Llama-3-8B geometry, 250k token rows) holding the facts' extents
+        L_, H_, D_, B_ = 32, 8, 128, 16
+        T_ = 250_000
+        gl = torch.Generator(device="cuda")
+        gl.manual_seed(10)
+        fl_a = torch.randint(12, 49, (N,), generator=gl, device="cuda", dtype=torch.int32)
+        fs_a = torch.randint(0, T_ - 48, (N,), generator=gl, device="cuda", dtype=torch.int64)
+        kv = torch.empty((L_, 2, T_, H_, D_), dtype=torch.bfloat16, device="cuda")
+        for l in range(L_):
+            kv[l].normal_(generator=gl)
+        g8 = kvi.geometry(L_, H_, D_, E)
+        fview = kvi.store_view(g8, kv, emb, fs_a, fl_a, n_tokens=T_)
+        lview8 = kvi.store_view(g8, kv, emb[:LM], fs_a[:LM], fl_a[:LM], n_tokens=T_)
+        tl = (64 + k * 48 + B_ - 1) // B_
+        pool = torch.empty((L_, 2, tl, B_, H_, D_), dtype=torch.bfloat16, device="cuda")
+        cache = kvi.paged_cache([pool[l] for l in range(L_)], B_)
+        bt = torch.arange(tl, dtype=torch.int32, device="cuda")[None].contiguous()
+        tls = torch.full((1,), tl, dtype=torch.int32, device="cuda")
+        st64 = torch.full((1,), 64, dtype=torch.int32, device="cuda")
+        fids = torch.empty((1, k), dtype=torch.int32, device="cuda")
+        fsc = torch.empty((1, k), dtype=torch.float32, device="cuda")
+        fpos = torch.empty((1, k), dtype=torch.int32, device="cuda")
+        d_view = torch.frombuffer(bytearray(kvi.pack_store_views([fview])), dtype=torch.uint8).cuda()
+        ws_x = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
+        ws_g = torch.empty(kvi.kvi_graph_retrieve_and_inject_workspace_bytes(1, N, beam, k),
+                           dtype=torch.uint8, device="cuda")
+        params = kvi.graph_search_params(beam, width, 10_000, n_seeds)
 
-    def fused_exact():
-        kvi.kvi_retrieve_and_inject(g8, 1, d_view, N, q[:1], k, st64, bt, tls, tl, cache, 5e5, fids,
-                                    fsc, fpos, ws_x, status)
+        def fused_exact():
+            kvi.kvi_retrieve_and_inject(g8, 1, d_view, N, q[:1], k, st64, bt, tls, tl, cache, 5e5, fids,
+                                        fsc, fpos, ws_x, status)
 
-    def fused_graph():
-        kvi.kvi_retrieve_topk(lview8, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1)
-        kvi.kvi_graph_retrieve_and_inject(fview, graph, D, 1, q[:1], seeds[:1], params, k, st64, bt,
-                                          tls, tl, cache, kvi.rope(5e5), fids, fsc, fpos, ws_g, status)
+        def fused_graph():
+            kvi.kvi_retrieve_topk(lview8, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1)
+            kvi.kvi_graph_retrieve_and_inject(fview, graph, D, 1, q[:1], seeds[:1], params, k, st64, bt,
+                                              tls, tl, cache, kvi.rope(5e5), fids, fsc, fpos, ws_g, status)
 
-    fx = timed(fused_exact, max(10, args.steps))
-    fx_ids = fids.cpu().numpy()[0].copy()
-    fg = timed(fused_graph, max(10, args.steps))
-    fg_ids = fids.cpu().numpy()[0]
-    fused = {"exact_us": round(fx * 1e6, 2), "graph_us": round(fg * 1e6, 2),
-             "recall_of_this_request": round(len(set(fx_ids) & set(fg_ids)) / k, 4),
-             "store": "Llama-3-8B K/V geometry, facts of 12-48 tokens in a 250k-row arena "
-                      "(33 GB), 16-token pages, start 64"}
-    del kv, pool
+        fx = timed(fused_exact, max(10, steps))
+        fx_ids = fids.cpu().numpy()[0].copy()
+        fg = timed(fused_graph, max(10, steps))
+        fg_ids = fids.cpu().numpy()[0]
+        fused = {"exact_us": round(fx * 1e6, 2), "graph_us": round(fg * 1e6, 2),
+                 "recall_of_this_request": round(len(set(fx_ids) & set(fg_ids)) / k, 4),
+                 "store": "Llama-3-8B K/V geometry, facts of 12-48 tokens in a 250k-row arena "
+                          "(33 GB), 16-token pages, start 64"}
+        del kv, pool
     assert int(status.item()) == 0
     # bytes a search reads: the rows it scores, its graph rows, its bitmap
     per_q = st[:, 1].mean() * E * 4 + st[:, 0].mean() * D * 4 + (N + 7) // 8
