@@ -976,7 +976,7 @@ def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
         "exact": {"scan_one_query_us": round(scan_s * 1e6, 2),
                   "shared_256_queries_us_per_query": round(shared_s / RE * 1e6, 2)},
     }
-    print(json.dumps(out), flush=True)
+    return out
 
 
 def run_workload(args):
