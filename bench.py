@@ -1047,14 +1047,26 @@ def run_workload(args):
     t = statistics.median(ts)
     inj = tokens * w.token_bytes
     alg = 2 * inj + R * w.n_facts * w.embed_dim * 4
-    print(json.dumps({
+    out = {
         "mode": "workload", "workload": args.workload, "requests": R, "k": k,
         "facts_per_store": w.n_facts, "injected_tokens_per_step": tokens,
         "ms_per_step": round(t * 1e3, 4), "injected_gb_per_s": round(inj / t / 1e9, 2),
         "hbm_frac_of_measured_peak": round(alg / t / 1e9 / peak, 4), "peak_gbs": peak,
         "peak_kind": peak_kind, "steps": args.steps, "warmup": args.warmup,
         "store": "arena stand-in (distinct fact extents)" if w.store == "arena" else "dense",
-    }), flush=True)
+    }
+    if not args.no_cpu_baseline:
+        # the oracle on a seeded sample of requests of this workload, one
+        # thread; the whole step is extrapolated from the per-request time
+        n_cpu = 4
+        gbs, secs, toks = cpu_baseline_sample(w, k, n_cpu, w.seed + 99)
+        out["cpu_baseline"] = {
+            "value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_cpu} requests of the workload at k={k} ({toks} tokens, {secs:.1f} s)",
+            "per_request_s": round(secs / n_cpu, 4),
+            "extrapolated_step_s": round(secs / n_cpu * R, 2),
+            "extrapolation": f"per-request time x {R} requests (not measured)"}
+    print(json.dumps(out), flush=True)
 
 
 def run_reference(args):
