@@ -993,7 +993,8 @@ def run_workload(args):
     kbuild.build()
     kvi.load_library()
     w = synth.WORKLOADS[args.workload]
-    k, R = args.k, w.requests
+    # the tiny configuration is defined at its own k (5 of 200 facts)
+    k, R = (w.k if args.workload == "tiny" else args.k), w.requests
     peak, peak_kind = load_peaks()
     g = kvi.geometry(w.layers, w.kv_heads, w.head_dim, w.embed_dim)
     if args.workload == "llama3_70b_capacity":
