@@ -567,6 +567,16 @@ KVI_API kvi_status kvi_store_file_info_read(const char *path, kvi_store_file_inf
 KVI_API kvi_status kvi_store_load(const char *path, void *kv, float *emb, int64_t *fact_start,
                                   int32_t *fact_len, uint32_t flags);
 
+/* Diagnostic: one warp waits on a shared-memory barrier that nothing
+ * completes, with the bounded wait every staging kernel of this library
+ * uses; after limit_ns (1 us .. 1 s) of %globaltimer it gives up, records
+ * KVI_ERR_TIMEOUT in *d_status and returns.  *d_elapsed_ns (device, may be
+ * NULL) receives the time the wait took.  Shows that a wait which never
+ * completes ends with a status the host reads, not a hang.  Asynchronous.
+ * Errors: KVI_ERR_INVALID_ARG, KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_selftest_bounded_wait(uint64_t limit_ns, int32_t *d_status,
+                                             int64_t *d_elapsed_ns, kvi_stream_t stream);
+
 /* Tracing: when n_events == 3, the calling thread's next
  * kvi_retrieve_and_inject calls record events[0] before the first kernel,
  * events[1] once retrieval and placement are enqueued and events[2] after

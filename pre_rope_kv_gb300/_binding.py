@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "kvi_store_file_info_read", "kvi_store_load", "kvi_graph_build_workspace_bytes",
     "kvi_graph_build", "kvi_graph_search_workspace_bytes", "kvi_graph_search",
     "kvi_graph_retrieve_and_inject_workspace_bytes", "kvi_graph_retrieve_and_inject",
+    "kvi_selftest_bounded_wait",
 )
 MAX_GRAPH_DEGREE = 128
 MAX_GRAPH_BEAM = 256
@@ -163,6 +164,7 @@ def load_library(path: str | None = None):
                                               ctypes.POINTER(GraphSearchParams), i32, P, P, P, i32,
                                               ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P,
                                               P, P, sz, P, P]),
+        "kvi_selftest_bounded_wait": (S, [ctypes.c_uint64, P, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -503,6 +505,11 @@ def kvi_graph_retrieve_and_inject(store: StoreView, graph, degree: int, R: int, 
         int(max_blocks), ctypes.byref(c), ctypes.byref(rope), _ptr(ids), _ptr(scores), _ptr(pos),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
         "kvi_graph_retrieve_and_inject")
+
+
+def kvi_selftest_bounded_wait(limit_ns: int, status, elapsed_ns=None, stream=None) -> None:
+    _check(load_library().kvi_selftest_bounded_wait(int(limit_ns), _ptr(status), _ptr(elapsed_ns),
+                                                    _stream(stream)), "kvi_selftest_bounded_wait")
 
 
 def kvi_trace_stages(events) -> None:

@@ -19,8 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkvi.so")
 SOURCES = ["kvi_host.cu", "kvi_retrieve.cu", "kvi_inject.cu", "kvi_noalloc.cu", "kvi_shared.cu",
-           "kvi_store_io.cu", "kvi_graph.cu"]
+           "kvi_store_io.cu", "kvi_graph.cu", "kvi_selftest.cu"]
 HEADERS = [os.path.join(CSRC, "kvi_internal.cuh"), os.path.join(CSRC, "kvi_dot2.cuh"),
+           os.path.join(CSRC, "kvi_sync.cuh"),
            os.path.join(INCLUDE, "kvi.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

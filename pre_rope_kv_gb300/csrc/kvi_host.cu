@@ -1311,3 +1311,17 @@ kvi_status kvi_graph_retrieve_and_inject(const kvi_store_view *store, const int3
 }
 
 }  // extern "C"
+
+extern "C" {
+
+kvi_status kvi_selftest_bounded_wait(uint64_t limit_ns, int32_t *d_status, int64_t *d_elapsed_ns,
+                                     kvi_stream_t stream)
+{
+    if (!d_status) return fail(KVI_ERR_INVALID_ARG, "status is NULL");
+    if (limit_ns < 1000 || limit_ns > 1000000000ull)
+        return fail(KVI_ERR_INVALID_ARG, "limit_ns=%llu outside [1e3, 1e9]", (unsigned long long)limit_ns);
+    KVI_CUDA(launch_bounded_wait(limit_ns, d_status, d_elapsed_ns, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+}  // extern "C"

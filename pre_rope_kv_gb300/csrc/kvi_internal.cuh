@@ -205,6 +205,9 @@ struct GraphSearchParams {
 };
 cudaError_t launch_graph_search(const GraphSearchParams &p, cudaStream_t s);
 
+// Diagnostic: a wait on a barrier nothing completes, bounded by limit_ns.
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, int64_t *elapsed_ns, cudaStream_t s);
+
 // One-time per-device kernel attributes (shared-memory opt-in), made ahead
 // of a stream capture.
 cudaError_t prepare_retrieval_kernels();

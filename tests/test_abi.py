@@ -139,6 +139,13 @@ def test_retrieve_topk_host_validation(lib):
         assert "fact_start and fact_len" in kvi.kvi_last_error()
 
 
+def test_selftest_wait_validation(lib):
+    t = _FakeTensor()
+    for bad in (0, 999, 1_000_000_001):
+        assert _err(kvi.kvi_selftest_bounded_wait, bad, t) == kvi.ERR_INVALID_ARG
+    assert lib.kvi_selftest_bounded_wait(1_000_000, None, None, None) == kvi.ERR_INVALID_ARG
+
+
 def test_graph_host_validation(lib):
     t = _FakeTensor()
     assert _err(kvi.kvi_graph_build, _store(fact_len=None), 8, t, t) == kvi.ERR_INVALID_ARG
