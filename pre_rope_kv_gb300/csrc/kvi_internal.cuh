@@ -138,6 +138,7 @@ struct InjectParams {
 struct CoarseParams {
     int32_t N, R, Rp, E;       // facts, queries, queries padded to 16, embedding dim
     int32_t stages, tmem_cols; // set by the launcher
+    int32_t mt;                // accumulators (128-fact tiles) per CTA: 1 or 2
     int64_t stride;            // row stride of lo / hi
     float *lo, *hi;            // [R][stride]
     int32_t *status;

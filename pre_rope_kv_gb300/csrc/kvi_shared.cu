@@ -137,9 +137,12 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     // 1024-byte aligned stages: A (facts) then B (queries), then the tail
     uint8_t *base = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int S = p.stages;
+    // MT accumulators of kTileM facts each share every query chunk
+    const int MT = p.mt;
+    const int stage_a = MT * kStageBytesA;
     const int stage_b = p.Rp * kChunk * 4;
     uint8_t *a_st = base;
-    uint8_t *b_st = base + (size_t)S * kStageBytesA;
+    uint8_t *b_st = base + (size_t)S * stage_a;
     CoarseSmemTail &tl = *reinterpret_cast<CoarseSmemTail *>(b_st + (size_t)S * stage_b);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x;
@@ -165,14 +168,15 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tl.tmem_base;
+    const int cols_acc = p.tmem_cols / MT;  // tensor-memory columns per accumulator
     bool ok = true;
 
     if (warp == 0) {
         // the stage is loaded as boxes of kBoxRowsA fact rows and kBoxRowsB
         // query rows, one box per lane (a single issuing thread caps the
         // copy rate far below the SM's share of HBM bandwidth)
-        const uint32_t bytes = (uint32_t)(kStageBytesA + stage_b);
-        const int na = kTileM / kBoxRowsA, nb = p.Rp / kBoxRowsB;
+        const uint32_t bytes = (uint32_t)(stage_a + stage_b);
+        const int na = MT * kTileM / kBoxRowsA, nb = p.Rp / kBoxRowsB;
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % S;
             const int round = kc / S;
@@ -191,8 +195,8 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
             __syncwarp();
             for (int j = lane; j < na + nb; j += 32) {
                 if (j < na)
-                    tma_2d(saddr(a_st + (size_t)s * kStageBytesA + (size_t)j * kBoxRowsA * 128), &tm_emb,
-                           kc * kChunk, tile * kTileM + j * kBoxRowsA, fb);
+                    tma_2d(saddr(a_st + (size_t)s * stage_a + (size_t)j * kBoxRowsA * 128), &tm_emb,
+                           kc * kChunk, tile * MT * kTileM + j * kBoxRowsA, fb);
                 else
                     tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
                            kc * kChunk, (j - na) * kBoxRowsB, fb);
@@ -209,18 +213,23 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = saddr(a_st + (size_t)s * kStageBytesA);
+                const uint32_t a0 = saddr(a_st + (size_t)s * stage_a);
                 const uint32_t b0 = saddr(b_st + (size_t)s * stage_b);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 8; ++kk) {  // K = 8 tf32 (32 bytes) per MMA
-                    const uint64_t ad = sw128_desc(a0 + 32u * kk);
                     const uint64_t bd = sw128_desc(b0 + 32u * kk);
                     const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
-                    asm volatile(
-                        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
-                        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
-                        : "memory");
+                    // accumulator m: fact rows 128 m .. 128 m + 127 of the
+                    // stage (16 KB further on), columns m * cols_acc on
+                    for (int m = 0; m < MT; ++m) {
+                        const uint64_t ad = sw128_desc(a0 + (uint32_t)(m * kStageBytesA) + 32u * kk);
+                        asm volatile(
+                            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+                                tmem + (uint32_t)(m * cols_acc)),
+                            "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+                            : "memory");
+                    }
                 }
                 // the stage is free once these MMAs have read it
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -237,7 +246,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
         // tile (a warp reaches the 32 lanes of its own subpartition, warp % 4)
         const int q = warp & 3;
         const int L = 32 * q + lane;
-        float en2 = 0.f, qa = 0.f, qb = 0.f;
+        float en2[2] = {0.f, 0.f}, qa = 0.f, qb = 0.f;  // en2[m]: fact row 128 m + L
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % S;
             const bool got = wait_bar(saddr(&tl.full[s]), (uint32_t)((kc / S) & 1));
@@ -249,7 +258,10 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
             // a row's 128 bytes stay within its own 128-byte span under the
             // swizzle (only their 16-byte chunks are permuted), so a sum of
             // squares reads them in place
-            en2 += sq_row32(reinterpret_cast<const float *>(a_st + (size_t)s * kStageBytesA + L * 128));
+            en2[0] += sq_row32(reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + L * 128));
+            if (MT == 2)
+                en2[1] += sq_row32(
+                    reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + kStageBytesA + L * 128));
             if (L < p.Rp) qa += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + L * 128));
             if (L + 128 < p.Rp)
                 qb += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + (L + 128) * 128));
@@ -262,9 +274,10 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
         const bool done = ok && wait_bar(saddr(&tl.mma_done), 0);
         if (__all_sync(0xffffffffu, done)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int64_t fact = (int64_t)tile * kTileM + L;
-            const float en = sqrtf(en2);
             const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
+            for (int m = 0; m < MT; ++m) {
+            const int64_t fact = ((int64_t)tile * MT + m) * kTileM + L;
+            const float en = sqrtf(m == 0 ? en2[0] : en2[1]);
             for (int c0 = 0; c0 < p.Rp; c0 += 16) {
                 uint32_t v[16];
                 asm volatile(
@@ -273,7 +286,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
                       "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
                       "=r"(v[14]), "=r"(v[15])
-                    : "r"(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0));
+                    : "r"(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(m * cols_acc + c0)));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (fact < p.N) {
 #pragma unroll
@@ -287,6 +300,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                         }
                     }
                 }
+            }
             }
         } else if (lane == 0) {
             record_status(p.status, KVI_ERR_TIMEOUT);
@@ -342,39 +356,47 @@ cudaError_t tmap_f32(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t
 
 }  // namespace
 
-int coarse_stages(int Rp)
+int coarse_stages(int Rp, int mt)
 {
-    const int per = kStageBytesA + Rp * kChunk * 4;
+    const int per = mt * kStageBytesA + Rp * kChunk * 4;
     return std::max(2, std::min(kMaxStages, kRingBudget / per));
 }
 
-size_t coarse_smem_bytes(int Rp)
+size_t coarse_smem_bytes(int Rp, int mt)
 {
-    const int S = coarse_stages(Rp);
-    return 1024 + (size_t)S * (kStageBytesA + (size_t)Rp * kChunk * 4) + sizeof(CoarseSmemTail);
+    const int S = coarse_stages(Rp, mt);
+    return 1024 + (size_t)S * (mt * kStageBytesA + (size_t)Rp * kChunk * 4) + sizeof(CoarseSmemTail);
 }
 
 cudaError_t launch_coarse(const CoarseParams &p0, const float *emb, int64_t n_facts, const float *queries,
                           cudaStream_t s)
 {
     CoarseParams p = p0;
-    p.stages = coarse_stages(p.Rp);
+    // two accumulators per CTA (256 facts sharing each query chunk) once the
+    // tiles of 256 still fill the GPU; one otherwise
+    DeviceInfo di;
+    cudaError_t e0 = device_info(&di);
+    if (e0 != cudaSuccess) return e0;
+    const int64_t tiles128 = (n_facts + kTileM - 1) / kTileM;
+    p.mt = tiles128 >= 2 * (int64_t)di.sms ? 2 : 1;
+    p.stages = coarse_stages(p.Rp, p.mt);
     int cols = 32;
     while (cols < p.Rp) cols <<= 1;
-    p.tmem_cols = cols;
+    p.tmem_cols = cols * p.mt;  // <= 512: cols <= 256
     CUtensorMap te, tq;
     cudaError_t e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, kBoxRowsA);
     if (e != cudaSuccess) return e;
     e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, kBoxRowsB);
     if (e != cudaSuccess) return e;
-    const size_t smem = coarse_smem_bytes(p.Rp);
+    const size_t smem = coarse_smem_bytes(p.Rp, p.mt);
     // the opt-in is made once per device, so it covers the largest ring any
     // query count needs
     size_t most = 0;
-    for (int rp = 16; rp <= KVI_MAX_SHARED_QUERIES; rp += 16) most = std::max(most, coarse_smem_bytes(rp));
+    for (int rp = 16; rp <= KVI_MAX_SHARED_QUERIES; rp += 16)
+        most = std::max(most, std::max(coarse_smem_bytes(rp, 1), coarse_smem_bytes(rp, 2)));
     e = smem_opt_in(coarse_kernel, (int)most);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((n_facts + kTileM - 1) / kTileM);
+    const unsigned grid = (unsigned)((n_facts + (int64_t)p.mt * kTileM - 1) / ((int64_t)p.mt * kTileM));
     coarse_kernel<<<grid, kCoarseThreads, smem, s>>>(te, tq, p);
     return cudaGetLastError();
 }

@@ -67,7 +67,9 @@ def check_topk(st, q, k, ids, sc):
 
 
 @pytest.mark.parametrize("N,E,R,k", [(1000, 256, 1, 10), (3000, 1024, 64, 50), (777, 100, 17, 33),
-                                     (5000, 384, 256, 256), (200, 64, 5, 200), (129, 32, 16, 7)])
+                                     (5000, 384, 256, 256), (200, 64, 5, 200), (129, 32, 16, 7),
+                                     # enough tiles for two accumulators (256 facts) per CTA
+                                     (40000, 128, 64, 50), (50001, 96, 3, 20), (39000, 64, 256, 8)])
 def test_shared_topk_matches_oracle(N, E, R, k):
     w, b, st, q = shared_case(R, seed=N + E + R + k, n_facts=N, embed_dim=E)
     ids, sc, status, _ = run_topk(w, b, st, q, k)
@@ -75,10 +77,11 @@ def test_shared_topk_matches_oracle(N, E, R, k):
     check_topk(st, q, k, ids, sc)
 
 
-def test_tensor_core_intervals_contain_exact_scores():
+@pytest.mark.parametrize("N,E,R,k", [(2000, 1024, 48, 30), (40000, 256, 40, 30)])
+def test_tensor_core_intervals_contain_exact_scores(N, E, R, k):
     # white box: the workspace holds the plain regions, then lo and hi
-    # planes [R][key_stride] float32 (256-byte aligned regions)
-    N, E, R, k = 2000, 1024, 48, 30
+    # planes [R][key_stride] float32 (256-byte aligned regions); 40k facts
+    # take the two-accumulator tiles
     w, b, st, q = shared_case(R, seed=711, n_facts=N, embed_dim=E)
     ids, sc, status, ws = run_topk(w, b, st, q, k)
     assert status == 0
