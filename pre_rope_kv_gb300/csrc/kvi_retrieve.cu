@@ -785,7 +785,6 @@ __device__ __noinline__ void select_by_histogram(SelectSmem &sm, const uint64_t 
 // will move -- the best-ranked ones, every layer's K and V rows -- with one
 // 128-byte L2 prefetch each, which warms their address translations.
 constexpr int kWarmFacts = 8;
-constexpr int kStreamUnroll = 8;  // streamed keys in flight per select thread
 constexpr int kSelectGroups = 256;
 
 __device__ __forceinline__ void fact_rows(const SelectParams &p, const SelectSmem &sm,
@@ -884,18 +883,7 @@ select_kernel(const __grid_constant__ SelectParams p)
             for (int m = 0; m < kKeysPerThread; ++m)
                 if (tid + (int64_t)m * kSelectThreads < N) mt = max(mt, (uint32_t)(kr[m] >> 48));
         } else {
-            // streamed keys: kStreamUnroll independent loads in flight per
-            // thread, the ids in ascending order as in every pass below
-            for (uint32_t i0 = tid; i0 < (uint32_t)N; i0 += kSelectThreads * kStreamUnroll) {
-                uint64_t kk[kStreamUnroll];
-#pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u) {
-                    const uint32_t i = i0 + (uint32_t)u * kSelectThreads;  // < 2^32: N < 2^31
-                    kk[u] = i < (uint32_t)N ? __ldcg(keys + i) : 0ull;
-                }
-#pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u) mt = max(mt, (uint32_t)(kk[u] >> 48));
-            }
+            for (int64_t i = tid; i < N; i += kSelectThreads) mt = max(mt, (uint32_t)(__ldcg(keys + i) >> 48));
         }
         // groups of 4 threads (256 groups): group g = threads 4g .. 4g+3
         mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
@@ -928,17 +916,8 @@ select_kernel(const __grid_constant__ SelectParams p)
             for (int m = 0; m < kKeysPerThread; ++m)
                 cnt += (tid + (int64_t)m * kSelectThreads < N && (uint32_t)(kr[m] >> 48) >= lo) ? 1u : 0u;
         } else {
-            for (uint32_t i0 = tid; i0 < (uint32_t)N; i0 += kSelectThreads * kStreamUnroll) {
-                uint64_t kk[kStreamUnroll];
-#pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u) {
-                    const uint32_t i = i0 + (uint32_t)u * kSelectThreads;  // < 2^32: N < 2^31
-                    kk[u] = i < (uint32_t)N ? __ldcg(keys + i) : 0ull;
-                }
-#pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u)
-                    cnt += (i0 + (uint32_t)u * kSelectThreads < (uint32_t)N && (uint32_t)(kk[u] >> 48) >= lo) ? 1u : 0u;
-            }
+            for (int64_t i = tid; i < N; i += kSelectThreads)
+                cnt += ((uint32_t)(__ldcg(keys + i) >> 48) >= lo) ? 1u : 0u;
         }
         uint32_t incl = cnt;
 #pragma unroll
@@ -964,24 +943,15 @@ select_kernel(const __grid_constant__ SelectParams p)
                     }
                 }
             } else {
-                for (uint32_t i0 = tid; i0 < (uint32_t)N; i0 += kSelectThreads * kStreamUnroll) {
-                    uint64_t kk[kStreamUnroll];
-#pragma unroll
-                    for (int u = 0; u < kStreamUnroll; ++u) {
-                        const uint32_t i = i0 + (uint32_t)u * kSelectThreads;  // < 2^32: N < 2^31
-                        kk[u] = i < (uint32_t)N ? __ldcg(keys + i) : 0ull;
-                    }
-#pragma unroll
-                    for (int u = 0; u < kStreamUnroll; ++u) {
-                        const uint32_t i = i0 + (uint32_t)u * kSelectThreads;  // < 2^32: N < 2^31
-                        if (i < (uint32_t)N && (uint32_t)(kk[u] >> 48) >= lo) {
-                            if (at < (uint32_t)kCandCap) {
-                                sm.cand_key[at] = kk[u];
-                                sm.cand_id[at] = (int32_t)i;
-                                sm.cand_len[at] = __ldcg(lens + i);
-                            }
-                            ++at;
+                for (int64_t i = tid; i < N; i += kSelectThreads) {
+                    const uint64_t key = __ldcg(keys + i);
+                    if ((uint32_t)(key >> 48) >= lo) {
+                        if (at < (uint32_t)kCandCap) {
+                            sm.cand_key[at] = key;
+                            sm.cand_id[at] = (int32_t)i;
+                            sm.cand_len[at] = __ldcg(lens + i);
                         }
+                        ++at;
                     }
                 }
             }
