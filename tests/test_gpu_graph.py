@@ -87,7 +87,8 @@ def check_search(emb_np, graph_np, q_np, seeds_np, out, beam, width, max_iters, 
         assert np.all(np.isnan(sc[r, m:]))
 
 
-@pytest.mark.parametrize("n,e,degree,seed", [(300, 64, 8, 0), (700, 128, 64, 1), (257, 32, 1, 2)])
+@pytest.mark.parametrize("n,e,degree,seed", [(300, 64, 8, 0), (700, 128, 64, 1), (257, 32, 1, 2),
+                                            (513, 100, 7, 4), (260, 1028, 128, 5)])
 def test_graph_build_matches_the_oracle(n, e, degree, seed):
     rng = np.random.default_rng(seed)
     emb = synth.clustered_rows(rng, n, e, clusters=12)
@@ -117,6 +118,21 @@ def test_graph_search_matches_the_oracle(beam, width, max_iters, n_seeds, k):
     emb_d = torch.from_numpy(emb).cuda()
     out = gpu_search(emb_d, graph, q, seeds, beam, width, max_iters, k)
     check_search(emb, graph, q, seeds, out, beam, width, max_iters, k)
+
+
+@pytest.mark.parametrize("e", [100, 36, 2052])
+def test_graph_search_odd_widths_match_the_oracle(e):
+    # embedding widths that are not a multiple of a warp's float4 row (a
+    # ragged last chunk, and more than one chunk per lane at 2052)
+    rng = np.random.default_rng(50 + e)
+    n, degree = 1200, 12
+    emb = synth.clustered_rows(rng, n, e, clusters=6)
+    graph = oracle.graph_build(emb, degree)
+    q = synth.near_queries(rng, emb, 6)
+    seeds = synth.graph_seeds(rng, n, 6, 5)
+    emb_d = torch.from_numpy(emb).cuda()
+    out = gpu_search(emb_d, graph, q, seeds, 24, 2, 500, 20)
+    check_search(emb, graph, q, seeds, out, 24, 2, 500, 20)
 
 
 def test_graph_search_batch_variant_matches_the_oracle():
