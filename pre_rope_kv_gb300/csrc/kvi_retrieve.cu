@@ -1106,7 +1106,6 @@ __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_co
 // accumulation, combination and warp reduction as the scoring kernels, so a
 // candidate's key is bit for bit the key the plain path computes for it.
 constexpr int kRescoreWarps = 8;
-constexpr int kRescoreChunk = 8;  // float4 of a row in flight per lane
 constexpr int kRescoreBlocksPerQuery = 16;
 
 __global__ void __launch_bounds__(kRescoreWarps * 32) rescore_kernel(const __grid_constant__ RescoreParams p)
@@ -1126,25 +1125,10 @@ __global__ void __launch_bounds__(kRescoreWarps * 32) rescore_kernel(const __gri
             s0 = __ldg(p.store.fact_start + f);
             l0 = __ldg(p.store.fact_len + f);
         }
-        // the whole row (up to kRescoreChunk float4 per lane) is requested
-        // before any arithmetic; the float4 are added in the same order as
-        // the scan adds them, so the key is the scan's key bit for bit
         Dot2x4 acc;
         acc.zero();
-        const int E4 = E / 4;
-        for (int v0 = 0; v0 < E4; v0 += 32 * kRescoreChunk) {
-            float4 e[kRescoreChunk];
-#pragma unroll
-            for (int u = 0; u < kRescoreChunk; ++u) {
-                const int v = v0 + lane + 32 * u;
-                if (v < E4) e[u] = ld_stream_f4(row + v);
-            }
-#pragma unroll
-            for (int u = 0; u < kRescoreChunk; ++u) {
-                const int v = v0 + lane + 32 * u;
-                if (v < E4) acc.add(__ldg(q4 + v), e[u]);
-            }
-        }
+#pragma unroll 4
+        for (int v = lane; v < E / 4; v += 32) acc.add(__ldg(q4 + v), ld_stream_f4(row + v));
         float s, c;
         acc.combine(s, c);
         warp_reduce_pair(s, c);
