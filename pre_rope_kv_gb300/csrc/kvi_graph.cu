@@ -137,41 +137,56 @@ __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem
 }
 
 // Merge the beam (cur, nc entries, sorted) with the new facts into the
-// other buffer, keeping the best `beam`; returns the new count.
+// other buffer, keeping the best `beam`; returns the new count.  An entry's
+// place is the number of entries better than it: among the new facts (a
+// count, split over a group of G adjacent lanes and summed by shuffles) plus,
+// for a new fact, among the beam (a binary search: the beam is sorted), or
+// for a beam entry, its own index.  Ids are distinct, so places are unique.
 template <int T>
 __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new, int beam)
 {
+    constexpr int G = T >= 512 ? 4 : 2;  // lanes per entry
     const int nxt = cur ^ 1;
-    for (int e = threadIdx.x; e < n_new + nc; e += T) {
-        uint64_t k;
-        int32_t id;
-        uint8_t ex;
-        int pos;
-        if (e < n_new) {
-            k = sm.new_key[e];
-            id = sm.new_id[e];
-            ex = 0;
-            pos = 0;
-            for (int j = 0; j < n_new; ++j) pos += better(sm.new_key[j], sm.new_id[j], k, id) ? 1 : 0;
-            int lo = 0, hi = nc;  // beam entries better than this one: a prefix
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (better(sm.key[cur][mid], sm.id[cur][mid], k, id)) lo = mid + 1;
-                else hi = mid;
+    const int sub = threadIdx.x & (G - 1);
+    const int total = n_new + nc;
+    for (int e0 = 0; e0 < total; e0 += T / G) {
+        const int e = e0 + (int)threadIdx.x / G;  // the same for the G lanes of a group
+        const bool live = e < total;
+        uint64_t k = 0;
+        int32_t id = 0;
+        uint8_t ex = 0;
+        if (live) {
+            if (e < n_new) {
+                k = sm.new_key[e];
+                id = sm.new_id[e];
+            } else {
+                k = sm.key[cur][e - n_new];
+                id = sm.id[cur][e - n_new];
+                ex = sm.expanded[cur][e - n_new];
             }
-            pos += lo;
-        } else {
-            const int i = e - n_new;
-            k = sm.key[cur][i];
-            id = sm.id[cur][i];
-            ex = sm.expanded[cur][i];
-            pos = i;
-            for (int j = 0; j < n_new; ++j) pos += better(sm.new_key[j], sm.new_id[j], k, id) ? 1 : 0;
         }
-        if (pos < beam) {
-            sm.key[nxt][pos] = k;
-            sm.id[nxt][pos] = id;
-            sm.expanded[nxt][pos] = ex;
+        int pos = 0;
+        if (live)
+            for (int j = sub; j < n_new; j += G) pos += better(sm.new_key[j], sm.new_id[j], k, id) ? 1 : 0;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
+        if (live && sub == 0) {
+            if (e < n_new) {
+                int lo = 0, hi = nc;  // beam entries better than this one: a prefix
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (better(sm.key[cur][mid], sm.id[cur][mid], k, id)) lo = mid + 1;
+                    else hi = mid;
+                }
+                pos += lo;
+            } else {
+                pos += e - n_new;
+            }
+            if (pos < beam) {
+                sm.key[nxt][pos] = k;
+                sm.id[nxt][pos] = id;
+                sm.expanded[nxt][pos] = ex;
+            }
         }
     }
     return min(beam, nc + n_new);
