@@ -40,10 +40,7 @@ struct SearchSmem {
     uint64_t new_key[KVI_MAX_GRAPH_FRONTIER];
     int32_t new_id[KVI_MAX_GRAPH_FRONTIER];
     int32_t parent[KVI_MAX_GRAPH_FRONTIER];
-    // per iteration parity: the count of new facts, and (width 1) the best
-    // beam slot left unexpanded by that iteration's merge
-    int32_t n_new[2];
-    int32_t first_open[2];
+    int32_t n_new;
     int32_t n_parent;
 };
 
@@ -60,10 +57,9 @@ __global__ void __launch_bounds__(256) graph_rows_kernel(const __grid_constant__
 }
 
 // Test-and-set `f` in the visited bitmap; the thread that sets the bit adds
-// f to the new list (warp-aggregated slot; *count counts them).  `want`
-// false: no candidate.
-__device__ __forceinline__ void visit(SearchSmem &sm, int32_t *count, uint32_t *vis, int64_t N, int32_t f,
-                                      bool want, int32_t *status)
+// f to the new list (warp-aggregated slot).  `want` false: no candidate.
+__device__ __forceinline__ void visit(SearchSmem &sm, uint32_t *vis, int64_t N, int32_t f, bool want,
+                                      int32_t *status)
 {
     bool fresh = false;
     if (want) {
@@ -78,7 +74,7 @@ __device__ __forceinline__ void visit(SearchSmem &sm, int32_t *count, uint32_t *
     if (!mask) return;
     const int lane = threadIdx.x & 31;
     int base = 0;
-    if (lane == __ffs(mask) - 1) base = atomicAdd(count, __popc(mask));
+    if (lane == __ffs(mask) - 1) base = atomicAdd(&sm.n_new, __popc(mask));
     base = __shfl_sync(0xffffffffu, base, __ffs(mask) - 1);
     if (fresh) sm.new_id[base + __popc(mask & ((1u << lane) - 1u))] = f;
 }
@@ -147,7 +143,7 @@ __device__ __forceinline__ void score_new(const GraphSearchParams &p, SearchSmem
 // for a new fact, among the beam (a binary search: the beam is sorted), or
 // for a beam entry, its own index.  Ids are distinct, so places are unique.
 template <int T>
-__device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new, int beam, int32_t *first_open)
+__device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new, int beam)
 {
     constexpr int G = T >= 512 ? 4 : 2;  // lanes per entry
     const int nxt = cur ^ 1;
@@ -190,7 +186,6 @@ __device__ __forceinline__ int merge(SearchSmem &sm, int cur, int nc, int n_new,
                 sm.key[nxt][pos] = k;
                 sm.id[nxt][pos] = id;
                 sm.expanded[nxt][pos] = ex;
-                if (first_open && !ex) atomicMin(first_open, pos);
             }
         }
     }
@@ -208,90 +203,62 @@ __global__ void __launch_bounds__(T, T >= 512 ? 1 : 4) graph_search_kernel(const
     const float *q = p.queries + (int64_t)r * p.E;
     uint32_t *vis = p.visited + (int64_t)r * p.vis_words;
     for (int64_t w = tid; w < p.vis_words; w += T) vis[w] = 0u;
-    if (tid == 0) {
-        sm.n_new[0] = sm.n_new[1] = 0;
-        sm.first_open[0] = sm.first_open[1] = 0x7fffffff;
-    }
+    if (tid == 0) sm.n_new = 0;
     __syncthreads();
-    // width 1: the merge finds the next parent itself (its lowest unexpanded
-    // slot), so no separate pick or barrier is needed
-    const bool one = p.width == 1;
 
     // seeds
     for (int t0 = 0; t0 < p.n_seeds; t0 += T) {
         const int t = t0 + tid;
-        visit(sm, &sm.n_new[0], vis, p.N, t < p.n_seeds ? p.seeds[(int64_t)r * p.n_seeds + t] : 0,
-              t < p.n_seeds, p.status);
+        visit(sm, vis, p.N, t < p.n_seeds ? p.seeds[(int64_t)r * p.n_seeds + t] : 0, t < p.n_seeds,
+              p.status);
     }
     __syncthreads();
-    int n_new = sm.n_new[0];
+    int n_new = sm.n_new;
     score_new<T, (T >= 512 ? 2 : 1)>(p, sm, q, n_new);
     __syncthreads();
     int cur = 0;
-    // into buffer 0 from an empty beam; iteration 0's parent slot
-    int nc = merge<T>(sm, cur ^ 1, 0, n_new, p.beam, one ? &sm.first_open[0] : nullptr);
+    int nc = merge<T>(sm, cur ^ 1, 0, n_new, p.beam);  // into buffer 0 from an empty beam
     __syncthreads();
 
-    // iteration i: counts its new facts in n_new[(i + 1) & 1], takes its
-    // width-1 parent from first_open[i & 1] and its merge leaves the next one
-    // in first_open[(i + 1) & 1]; thread 0 clears the slots the next
-    // iteration uses once every thread has read their last values
     int iters = 0;
     int scored = n_new;
     while (iters < p.max_iters) {
-        const int par = iters & 1;
-        int np;
-        int32_t parent1 = 0;
-        if (one) {
-            const int pp = sm.first_open[par];
-            if (tid == 0) {
-                sm.first_open[par ^ 1] = 0x7fffffff;
-                sm.n_new[par] = 0;
-                if (pp < nc) sm.expanded[cur][pp] = 1;
-            }
-            np = pp < nc ? 1 : 0;
-            if (np) parent1 = sm.id[cur][pp];
-        } else {
-            if (warp == 0) {
-                // the first `width` unexpanded entries of the beam, in order
-                int n = 0;
-                for (int base = 0; base < nc && n < p.width; base += 32) {
-                    const int i = base + lane;
-                    const bool open = i < nc && !sm.expanded[cur][i];
-                    const unsigned mask = __ballot_sync(0xffffffffu, open);
-                    const int rank = n + __popc(mask & ((1u << lane) - 1u));
-                    if (open && rank < p.width) {
-                        sm.expanded[cur][i] = 1;
-                        sm.parent[rank] = sm.id[cur][i];
-                    }
-                    n = min(p.width, n + __popc(mask));
+        if (warp == 0) {
+            // the first `width` unexpanded entries of the beam, in order
+            int np = 0;
+            for (int base = 0; base < nc && np < p.width; base += 32) {
+                const int i = base + lane;
+                const bool open = i < nc && !sm.expanded[cur][i];
+                const unsigned mask = __ballot_sync(0xffffffffu, open);
+                const int rank = np + __popc(mask & ((1u << lane) - 1u));
+                if (open && rank < p.width) {
+                    sm.expanded[cur][i] = 1;
+                    sm.parent[rank] = sm.id[cur][i];
                 }
-                if (lane == 0) {
-                    sm.n_parent = n;
-                    sm.n_new[par] = 0;
-                }
+                np = min(p.width, np + __popc(mask));
             }
-            __syncthreads();
-            np = sm.n_parent;
+            if (lane == 0) {
+                sm.n_parent = np;
+                sm.n_new = 0;
+            }
         }
+        __syncthreads();
+        const int np = sm.n_parent;
         if (np == 0) break;
         ++iters;
         const int total = np * p.degree;
         for (int t0 = 0; t0 < total; t0 += T) {
             const int t = t0 + tid;
             int32_t f = 0;
-            if (t < total) {
-                const int32_t par_id = one ? parent1 : sm.parent[t / p.degree];
-                f = __ldg(p.graph + (int64_t)par_id * p.degree + t % p.degree);
-            }
-            visit(sm, &sm.n_new[par ^ 1], vis, p.N, f, t < total, p.status);
+            if (t < total) f = __ldg(p.graph + (int64_t)sm.parent[t / p.degree] * p.degree + t % p.degree);
+            visit(sm, vis, p.N, f, t < total, p.status);
         }
         __syncthreads();
-        n_new = sm.n_new[par ^ 1];
+        n_new = sm.n_new;
         scored += n_new;
         score_new<T, (T >= 512 ? 2 : 1)>(p, sm, q, n_new);
         __syncthreads();
-        nc = merge<T>(sm, cur, nc, n_new, p.beam, one ? &sm.first_open[par ^ 1] : nullptr);
+        nc = merge<T>(sm, cur, nc, n_new, p.beam);
         cur ^= 1;
         __syncthreads();
     }
