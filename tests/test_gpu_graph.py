@@ -314,3 +314,43 @@ def test_fused_graph_retrieve_and_inject_full_pool(R, pairing, width):
         assert np.array_equal(g_pos[r], o_pos), r
         placements.append((o_ids, o_pos))
     kc.check_pool_full(b, placements, rope=oracle.rope_spec(w.rope_theta, w.head_dim, pairing))
+
+
+def test_fused_graph_path_with_more_requests_than_sms():
+    # 200 requests over one store: the search runs its batch variant and the
+    # selector and inject kernels place and inject every request's facts
+    R = 200
+    w = synth.Workload(name="graph_many", layers=1, kv_heads=2, head_dim=64, rope_theta=1e4,
+                       block_size=16, n_facts=500, len_lo=1, len_hi=6, len_dist="uniform",
+                       embed_dim=64, requests=R, k=6, start=2, start_hi=0, seed=970, store="dense")
+    b = synth.build_workload(w)
+    b.stores = [b.stores[0]] * R
+    st = b.stores[0]
+    emb = st.emb_np
+    graph = oracle.graph_build(emb, 10)
+    rng = np.random.default_rng(971)
+    seeds = synth.graph_seeds(rng, w.n_facts, R, 6)
+    view = kc.views_of(b)[0]
+    k, beam = w.k, 16
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    pos = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvi.kvi_graph_retrieve_and_inject_workspace_bytes(R, w.n_facts, beam, k),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvi.kvi_graph_retrieve_and_inject(
+        view, torch.from_numpy(graph).cuda(), 10, R, b.queries, torch.from_numpy(seeds).cuda(),
+        kvi.graph_search_params(beam, 1, 200, 6), k, torch.from_numpy(b.start_pos).cuda(),
+        torch.from_numpy(b.block_tables).cuda(), torch.from_numpy(b.table_lens).cuda(), b.max_blocks,
+        kc.cache_of(b), kvi.rope(w.rope_theta), ids, sc, pos, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    g_ids, g_pos = ids.cpu().numpy(), pos.cpu().numpy()
+    placements = []
+    for r in range(R):
+        o_ids = oracle.graph_search(b.queries_np[r], emb, graph, seeds[r], beam, 1, 200, k)[0]
+        assert np.array_equal(g_ids[r], o_ids), r
+        o_pos, _ = oracle.place(o_ids, st.len_np, int(b.start_pos[r]))
+        assert np.array_equal(g_pos[r], o_pos), r
+        placements.append((o_ids, o_pos))
+    kc.check_pool_full(b, placements)

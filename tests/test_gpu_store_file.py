@@ -153,3 +153,27 @@ def test_damaged_payload_and_extents_are_refused(tmp_path):
     open(p, "wb").write(sf.build(f["g"], starts, lens, f["emb"], f["kv"], f["t"]))
     assert _load_status(p, info) == kvi.ERR_IO
     assert "outside the store" in kvi.kvi_last_error()
+
+
+def test_arena_view_round_trips(tmp_path):
+    # extents scattered through more rows than the facts use (an arena
+    # stand-in): the file keeps every row and the extents as they are
+    b = synth.build_workload(W(seed=906, n_facts=60, len_lo=1, len_hi=6))
+    st = b.stores[0]
+    T = 400
+    rng = np.random.default_rng(907)
+    lens = st.len_np.astype(np.int32)
+    starts = np.sort(rng.choice(T - 6, size=60, replace=False)).astype(np.int64)
+    g = kc.geometry_of(b.w)
+    kv = torch.randn((b.w.layers, 2, T, b.w.kv_heads, b.w.head_dim), device="cuda").to(torch.bfloat16)
+    fs = torch.from_numpy(starts).cuda()
+    fl = torch.from_numpy(lens).cuda()
+    view = kvi.store_view(g, kv, st.emb, fs, fl, n_tokens=T)
+    p = os.path.join(str(tmp_path), "arena.kvs")
+    kvi.kvi_store_save(p, view)
+    f = sf.read(p)
+    assert f["t"] == T and f["fact_start"] == starts.astype("<i8").tobytes()
+    g2, kv2, emb2, fs2, fl2 = kvi.load_store(p)
+    torch.cuda.synchronize()
+    assert torch.equal(kv2.view(torch.int16), kv.view(torch.int16))
+    assert torch.equal(fs2, fs) and torch.equal(fl2, fl) and torch.equal(emb2, st.emb)
