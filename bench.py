@@ -386,7 +386,7 @@ class Bench:
 
         def ret_plain():
             for r in range(R):
-                kvi.kvi_retrieve_topk(view, q[r], k, ids[r], sc[r], ws_1, self.stream)
+                kvi.kvi_retrieve_topk(view, q[r], k, ids[r], sc[r], ws_1, self.status, self.stream)
 
         def fused_shared():
             kvi.kvi_retrieve_and_inject_shared(view, R, q, k, start, tables, tls, tl, cache, spec, ids,
@@ -871,7 +871,7 @@ def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
 
     def landmarks(r):
         if r == 1:
-            kvi.kvi_retrieve_topk(lview, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1)
+            kvi.kvi_retrieve_topk(lview, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1, status)
             return
         for a in range(0, r, RS):
             b = min(r, a + RS)
@@ -920,7 +920,7 @@ def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
                                                           status), 5)
     del ws_e
     ws_1 = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
-    scan_s = timed(lambda: kvi.kvi_retrieve_topk(view, q[0], k, ex_ids[0], ex_sc[0], ws_1), 10)
+    scan_s = timed(lambda: kvi.kvi_retrieve_topk(view, q[0], k, ex_ids[0], ex_sc[0], ws_1, status), 10)
     fused = None
     if full:
         # one request through the whole path at this store size: K/V in an arena
@@ -957,7 +957,7 @@ def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
                                         fsc, fpos, ws_x, status)
 
         def fused_graph():
-            kvi.kvi_retrieve_topk(lview8, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1)
+            kvi.kvi_retrieve_topk(lview8, q[0], n_seeds, seeds[0], seed_sc[0], ws_l1, status)
             kvi.kvi_graph_retrieve_and_inject(fview, graph, D, 1, q[:1], seeds[:1], params, k, st64, bt,
                                               tls, tl, cache, kvi.rope(5e5), fids, fsc, fpos, ws_g, status)
 
@@ -1027,13 +1027,15 @@ def run_workload(args):
         b = synth.build_workload(w, k=k, with_pool=False)
         need = []
         ws1 = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, k), dtype=torch.uint8, device="cuda")
+        st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
         ids1 = torch.empty(k, dtype=torch.int32, device="cuda")
         sc1 = torch.empty(k, dtype=torch.float32, device="cuda")
         for r, st in enumerate(b.stores):
             view = kvi.store_view(g, b.kv, st.emb, st.fact_start, st.fact_len)
-            kvi.kvi_retrieve_topk(view, b.queries[r], k, ids1, sc1, ws1)
+            kvi.kvi_retrieve_topk(view, b.queries[r], k, ids1, sc1, ws1, st1)
             torch.cuda.synchronize()
             need.append(int(st.len_np[ids1.cpu().numpy()].sum()))
+        assert int(st1.item()) == 0, f"device status {int(st1.item())}"
         synth.attach_pool(b, tokens_needed=need)
     else:
         b = synth.build_workload(w, k=k)

@@ -158,9 +158,15 @@ KVI_API kvi_status kvi_store_layout(const kvi_geometry *g, const int32_t *fact_l
  * memory owned by the library until process exit.  The inject calls build
  * the table on first use when needed, which blocks the host and is refused
  * (KVI_ERR_INVALID_ARG) while the stream is being captured; call this first
- * to keep them asynchronous.  Errors: KVI_ERR_INVALID_ARG (theta <= 0,
- * head_dim not a multiple of 16, max_position <= 0 or > 2^22),
- * KVI_ERR_CUDA. */
+ * to keep them asynchronous.
+ * Lifetime: no table is freed before the process exits.  When a call needs
+ * more positions than the current table covers, a table with at least twice
+ * the rows replaces it for later calls; the old one stays allocated, so
+ * kernels already enqueued and plans recorded earlier (which hold its
+ * address) keep reading valid memory.  Neither this call nor the growth
+ * synchronises the device.
+ * Errors: KVI_ERR_INVALID_ARG (theta <= 0, head_dim not a multiple of 16,
+ * max_position <= 0 or > 2^22), KVI_ERR_CUDA. */
 KVI_API kvi_status kvi_prepare_rope(double rope_theta, int32_t head_dim,
                             int32_t max_position);
 
@@ -226,11 +232,18 @@ KVI_API size_t kvi_workspace_bytes(int32_t R, int64_t max_facts, int32_t k);
  *   d_ids    [k] int32, rank order      d_scores [k] float32 similarity
  *   d_ws     scratch of >= kvi_workspace_bytes(1, store->n_facts, k) bytes,
  *            256-byte aligned; its contents need no initialisation.
+ *   d_status device int32, required: device-side errors of this call are
+ *            recorded there (first error wins; never cleared by the
+ *            library): KVI_ERR_OUT_OF_RANGE when a selected fact's extent
+ *            (fact_start, fact_len) lies outside the store -- its id is
+ *            still returned -- and KVI_ERR_TIMEOUT when a scoring wait gave
+ *            up (the ids are then not valid).
  * Errors: KVI_ERR_INVALID_ARG (null pointers, k < 1, k > KVI_MAX_K,
  * k > n_facts, bad geometry, workspace too small), KVI_ERR_CUDA. */
 KVI_API kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query,
                              int32_t k, int32_t *d_ids, float *d_scores,
-                             void *d_ws, size_t ws_bytes, kvi_stream_t stream);
+                             void *d_ws, size_t ws_bytes, int32_t *d_status,
+                             kvi_stream_t stream);
 
 /* Place (Figure 2 caption, "positioned by chunked RoPE"; rank-order reading):
  * d_pos[j] = start + sum of fact_len[d_ids[j']] for j' < j.  n <= KVI_MAX_K.
@@ -392,7 +405,10 @@ KVI_API kvi_status kvi_retrieve_and_inject_shared(
  *     process exits.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cached address
+ *     belongs to the device's context as it was then: after
+ *     cudaDeviceReset (or anything else that destroys that context) this
+ *     entry point must not be called again in the process.
  *   - All calls on a device share the one array and it keeps whatever the
  *     last call left; nothing in it has to start at zero.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads, or before the
@@ -406,7 +422,7 @@ KVI_API kvi_status kvi_retrieve_and_inject_shared(
 KVI_API kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store,
                                              const float *d_query, int32_t k,
                                              int32_t *d_ids, float *d_scores,
-                                             kvi_stream_t stream);
+                                             int32_t *d_status, kvi_stream_t stream);
 
 /* Graph index.  The review's Summary retrieves facts at serving time
  * through a GPU ANN index (Jasper) rather than a scan, and its Axiom &

@@ -123,7 +123,7 @@ def load_library(path: str | None = None):
         "kvi_store_layout": (S, [ctypes.POINTER(Geometry), P, i64, P, ctypes.POINTER(StoreSizes)]),
         "kvi_prepare_rope": (S, [f64, i32, i32]),
         "kvi_workspace_bytes": (sz, [i32, i64, i32]),
-        "kvi_retrieve_topk": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P, sz, P]),
+        "kvi_retrieve_topk": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P, sz, P, P]),
         "kvi_place": (S, [ctypes.POINTER(StoreView), P, i32, i32, P, P, P]),
         "kvi_inject_paged": (S, [ctypes.POINTER(StoreView), P, P, i32, P, i32,
                                  ctypes.POINTER(PagedCache), f64, P, P]),
@@ -150,7 +150,7 @@ def load_library(path: str | None = None):
         "kvi_retrieve_and_inject_ex": (S, [ctypes.POINTER(Geometry), i32, P, i64, P, i32, P, P,
                                            P, i32, ctypes.POINTER(PagedCache),
                                            ctypes.POINTER(Rope), P, P, P, P, sz, P, P]),
-        "kvi_retrieve_topk_noalloc": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P]),
+        "kvi_retrieve_topk_noalloc": (S, [ctypes.POINTER(StoreView), P, i32, P, P, P, P]),
         "kvi_store_save": (S, [ctypes.c_char_p, ctypes.POINTER(StoreView)]),
         "kvi_store_file_info_read": (S, [ctypes.c_char_p, ctypes.POINTER(StoreFileInfo)]),
         "kvi_store_load": (S, [ctypes.c_char_p, P, P, P, P, ctypes.c_uint32]),
@@ -294,18 +294,20 @@ def kvi_workspace_bytes(R: int, max_facts: int, k: int) -> int:
     return int(load_library().kvi_workspace_bytes(int(R), int(max_facts), int(k)))
 
 
-def kvi_retrieve_topk(store: StoreView, query, k: int, ids, scores, ws, stream=None) -> None:
+def kvi_retrieve_topk(store: StoreView, query, k: int, ids, scores, ws, status,
+                      stream=None) -> None:
     _check(load_library().kvi_retrieve_topk(
         ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _ptr(ws),
-        ws.numel() * ws.element_size(), _stream(stream)), "kvi_retrieve_topk")
+        ws.numel() * ws.element_size(), _ptr(status), _stream(stream)), "kvi_retrieve_topk")
 
 
-def kvi_retrieve_topk_noalloc(store: StoreView, query, k: int, ids, scores, stream=None) -> None:
+def kvi_retrieve_topk_noalloc(store: StoreView, query, k: int, ids, scores, status,
+                              stream=None) -> None:
     """kvi_retrieve_topk without a workspace: the scratch is a fixed array of
     the library (see include/kvi.h for who needs this and its limits)."""
     _check(load_library().kvi_retrieve_topk_noalloc(
-        ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _stream(stream)),
-        "kvi_retrieve_topk_noalloc")
+        ctypes.byref(store), _ptr(query), int(k), _ptr(ids), _ptr(scores), _ptr(status),
+        _stream(stream)), "kvi_retrieve_topk_noalloc")
 
 
 def kvi_place(store: StoreView, ids, n: int, start: int, pos, status=None, stream=None) -> None:

@@ -107,6 +107,16 @@ std::vector<DeviceInfo> g_dev;  // indexed by device ordinal; sms == 0 = unknown
 
 // One device table per (device, head_dim, frequencies): the pairing does not
 // change the table, only how the kernel applies it.
+//
+// Lifetime: a table is never freed while the library is loaded.  When a
+// call needs more positions than the current table holds, a larger table
+// (at least twice the rows) replaces it for later calls and the old one
+// moves to g_rope_retired.  Kernels already enqueued, and CUDA graphs
+// recorded by kvi_plan_create_fused*, keep the old pointer in their
+// parameters; the old table stays valid and covers the positions they were
+// recorded for, so no replay reads freed memory and no call has to
+// synchronise the device to retire a table.  Doubling bounds the retired
+// tables' total size by the current table's.
 struct RopeEntry {
     int device;
     int32_t head_dim;
@@ -116,6 +126,19 @@ struct RopeEntry {
 };
 std::mutex g_rope_mu;
 std::vector<RopeEntry> g_rope;
+std::vector<float4 *> g_rope_retired;  // superseded tables, kept until exit
+
+// The last table this thread was handed, looked up without the mutex (the
+// pointer stays valid: tables are never freed).
+struct RopeHit {
+    bool valid;
+    int device;
+    int32_t head_dim;
+    kvi_rope key;
+    int32_t positions;
+    const float4 *table;
+};
+thread_local RopeHit t_rope_hit = {false, 0, 0, {}, 0, nullptr};
 
 bool same_table(const kvi_rope &a, const kvi_rope &b)
 {
@@ -242,6 +265,13 @@ kvi_status rope_get(const kvi_rope &spec, int32_t D, int32_t needed, cudaStream_
     KVI_CUDA(cudaGetDevice(&dev));
     const bool given = spec.table_id != 0;
     if (given) needed = spec.table_positions;
+    RopeHit &th = t_rope_hit;
+    if (th.valid && th.device == dev && th.head_dim == D && th.positions >= needed &&
+        same_table(th.key, spec)) {
+        *table = th.table;
+        *positions = th.positions;
+        return KVI_OK;
+    }
     std::lock_guard<std::mutex> lock(g_rope_mu);
     RopeEntry *hit = nullptr;
     for (auto &e : g_rope)
@@ -249,6 +279,7 @@ kvi_status rope_get(const kvi_rope &spec, int32_t D, int32_t needed, cudaStream_
     if (hit && hit->positions >= needed) {
         *table = hit->table;
         *positions = hit->positions;
+        th = RopeHit{true, dev, D, hit->key, hit->positions, hit->table};
         return KVI_OK;
     }
     if (stream) {
@@ -259,7 +290,9 @@ kvi_status rope_get(const kvi_rope &spec, int32_t D, int32_t needed, cudaStream_
                         "RoPE table for theta=%g, D=%d, %d positions is missing during stream "
                         "capture; call kvi_prepare_rope first", spec.theta, D, needed);
     }
-    const int32_t P = given ? needed : std::min(kMaxRopePositions, ((needed + 1023) / 1024) * 1024);
+    int32_t P = given ? needed : std::min(kMaxRopePositions, ((needed + 1023) / 1024) * 1024);
+    if (hit && !given)  // grow geometrically: few retired tables, bounded in size
+        P = std::max(P, (int32_t)std::min<int64_t>(kMaxRopePositions, 2 * (int64_t)hit->positions));
     const int32_t half = D / 2;
     const std::vector<double> omega = given ? std::vector<double>() : rope_omega(spec, D);
     std::vector<float4> host((size_t)P * half);
@@ -279,18 +312,20 @@ kvi_status rope_get(const kvi_rope &spec, int32_t D, int32_t needed, cudaStream_
         return fail(KVI_ERR_CUDA, "RoPE table upload: %s", cudaGetErrorString(ce));
     }
     if (hit) {
-        // The old table may still be read by enqueued kernels.
-        KVI_CUDA(cudaDeviceSynchronize());
-        KVI_CUDA(cudaFree(hit->table));
+        // enqueued kernels and recorded plans may still read the old table:
+        // it is retired, not freed (see RopeEntry)
+        g_rope_retired.push_back(hit->table);
         hit->table = d;
         hit->positions = P;
     } else {
         kvi_rope key = spec;
         key.cos_table = key.sin_table = nullptr;  // the copy is kept, not the caller's arrays
         g_rope.push_back(RopeEntry{dev, D, key, P, d});
+        hit = &g_rope.back();
     }
     *table = d;
     *positions = P;
+    th = RopeHit{true, dev, D, hit->key, P, d};
     return KVI_OK;
 }
 
@@ -488,7 +523,7 @@ kvi_status kvi_trace_stages(const kvi_event_t *events, int32_t n_events)
 
 kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, int32_t k,
                              int32_t *d_ids, float *d_scores, void *d_ws, size_t ws_bytes,
-                             kvi_stream_t stream)
+                             int32_t *d_status, kvi_stream_t stream)
 {
     kvi_status st = check_store(store, true, false);
     if (st != KVI_OK) return st;
@@ -498,6 +533,8 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
         return fail(KVI_ERR_INVALID_ARG, "k=%d outside [1, min(%d, n_facts=%lld)]", k, KVI_MAX_K,
                     (long long)store->n_facts);
     if (!d_ids || !d_scores) return fail(KVI_ERR_INVALID_ARG, "ids or scores is NULL");
+    if (!d_status || !aligned(d_status, 4))
+        return fail(KVI_ERR_INVALID_ARG, "status must be a 4-byte aligned device pointer");
     const WsLayout w = ws_layout(1, store->n_facts, k);
     if (!d_ws || !aligned(d_ws, 256) || ws_bytes < w.total)
         return fail(KVI_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned", w.total);
@@ -515,6 +552,7 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
     sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
     sp.lens = reinterpret_cast<int32_t *>(ws + w.lens);
     sp.key_stride = w.key_stride;
+    sp.status = d_status;
     KVI_CUDA(launch_score(sp, s));
 
     SelectParams lp{};
@@ -529,6 +567,7 @@ kvi_status kvi_retrieve_topk(const kvi_store_view *store, const float *d_query, 
     lp.ids = d_ids;
     lp.scores = d_scores;
     lp.place = 0;
+    lp.status = d_status;
     KVI_CUDA(launch_select(lp, s, true));
     return KVI_OK;
 }

@@ -46,7 +46,9 @@
 //
 // Every wait is bounded (one second of globaltimer); a warp that times out
 // records KVI_ERR_TIMEOUT and stops, and the warps waiting on it stop after
-// their own bounded waits.
+// their own bounded waits.  Before the producer warp exits it waits, again
+// with a bound, for the last copy it issued into every stage, so no copy is
+// still writing into the CTA's shared memory when the CTA ends.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -92,6 +94,7 @@ struct __align__(128) InjSmem {
     uint8_t stage[kInjRing][kPieceMax];
     uint64_t full[kInjRing];
     uint64_t empty[kInjRing];
+    int32_t issued[kInjRing];  // round of the last copy issued into each stage, -1: none
     PieceDesc desc[kInjRing];
     int32_t prefix[kMaxPrefix + 1];
     int32_t part[kInjThreads];
@@ -497,6 +500,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
     if (tid < kInjRing) {  // one stage's barriers per thread
         mbar_init(smem_u32(&sm.full[tid]), 1);
         mbar_init(smem_u32(&sm.empty[tid]), 1);
+        sm.issued[tid] = -1;
         fence_async_smem();
     }
     for (int l = tid; l < p.L; l += kInjThreads) sm.lbase[l] = reinterpret_cast<uint8_t *>(p.layer_base[l]);
@@ -599,6 +603,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 } else {
                     staged = true;
                     sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
+                    if (x.bytes) sm.issued[s] = (int32_t)round;
                     const uint32_t fb = smem_u32(&sm.full[s]);
                     if (x.bytes && !x.direct) {
                         // the stage's previous contents were read by the
@@ -663,6 +668,16 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 sm.desc[s] = PieceDesc{nullptr, 0u, 0, 0, 0, 1};
                 mbar_arrive(smem_u32(&sm.full[s]));
             }
+        }
+        // Leave no copy in flight into this CTA's shared memory: whatever
+        // ended the loop (the last item, or a wait that gave up), each
+        // stage's last issued copy is waited for, with a bound, before the
+        // producer exits.  After a normal end they have all landed already.
+        __syncwarp();
+        if (lane < kInjRing) {
+            const int32_t r = sm.issued[lane];
+            if (r >= 0 && !mbar_wait(smem_u32(&sm.full[lane]), (uint32_t)(r & 1), kWaitLimitNs))
+                record_status(p.status, KVI_ERR_TIMEOUT);
         }
     } else {
         // consumers: this CTA's staged items warp, warp + 12, ... until a stop

@@ -65,7 +65,7 @@ struct ScoreParams {
     uint64_t *keys;
     int32_t *lens;
     int64_t key_stride;
-    int32_t *status;  // may be null (kvi_retrieve_topk has no status word)
+    int32_t *status;  // device status word (first error wins)
 };
 
 struct SelectParams {

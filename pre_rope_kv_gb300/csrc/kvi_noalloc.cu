@@ -16,7 +16,8 @@
 // library holds it (KVI_NOALLOC_SCRATCH_BYTES) until the process exits.  On
 // the host its name is only a stand-in for the device copy, so its device
 // address is looked up with cudaGetSymbolAddress, once per device, on that
-// device's first call.
+// device's first call (the address then stays valid for the life of the
+// device's context; a cudaDeviceReset ends it).
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -75,7 +76,8 @@ kvi_status bad(const char *msg) { return set_error(KVI_ERR_INVALID_ARG, msg); }
 extern "C" {
 
 kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store, const float *d_query, int32_t k,
-                                     int32_t *d_ids, float *d_scores, kvi_stream_t stream)
+                                     int32_t *d_ids, float *d_scores, int32_t *d_status,
+                                     kvi_stream_t stream)
 {
     kvi_status st = check_retrieval_store(store);
     if (st != KVI_OK) return st;
@@ -86,6 +88,8 @@ kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store, const float *d
         return bad("query must be a 16-byte aligned device pointer");
     if (k < 1 || k > KVI_MAX_K || (int64_t)k > store->n_facts) return bad("k outside [1, min(KVI_MAX_K, n_facts)]");
     if (!d_ids || !d_scores) return bad("ids or scores is NULL");
+    if (!d_status || (reinterpret_cast<uintptr_t>(d_status) & 3))
+        return bad("status must be a 4-byte aligned device pointer");
 
     const WsLayout w = ws_layout(1, store->n_facts, k);
     if (w.total > sizeof(g_topk_scratch)) return bad("scratch layout exceeds the fixed array");
@@ -108,6 +112,7 @@ kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store, const float *d
     sp.keys = reinterpret_cast<uint64_t *>(ws + w.keys);
     sp.lens = reinterpret_cast<int32_t *>(ws + w.lens);
     sp.key_stride = w.key_stride;
+    sp.status = d_status;
     cudaError_t e = launch_score(sp, s);
     if (e != cudaSuccess) return cuda_fail("launch_score", e);
     SelectParams lp{};
@@ -122,6 +127,7 @@ kvi_status kvi_retrieve_topk_noalloc(const kvi_store_view *store, const float *d
     lp.ids = d_ids;
     lp.scores = d_scores;
     lp.place = 0;
+    lp.status = d_status;
     e = launch_select(lp, s, true);
     if (e != cudaSuccess) return cuda_fail("launch_select", e);
     return KVI_OK;

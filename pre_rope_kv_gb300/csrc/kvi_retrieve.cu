@@ -244,6 +244,7 @@ struct ScoreRingSmem {
     uint8_t ring[kRingBytes];
     uint64_t full[kRingMaxStages];
     uint64_t empty[kRingMaxStages];
+    int32_t issued[kRingMaxStages];  // round of the last copy into each stage, -1: none
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -315,6 +316,7 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
     if (tid < S) {  // one stage's barriers per thread
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[tid])) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.empty[tid])) : "memory");
+        sm.issued[tid] = -1;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     const int64_t total = (int64_t)p.R * p.max_facts;
@@ -350,6 +352,7 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
                     sc.get(p, cur.r);
                     const uint32_t fb = smem_addr(&sm.full[s]);
                     if (sc.live(cur.i)) {
+                        sm.issued[s] = (int32_t)round;
                         if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
                                      "r"(row_bytes)
@@ -364,7 +367,16 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
                     }
                 }
             }
-            if (!__all_sync(0xffffffffu, ok)) return;
+            if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        // no copy may still be writing into shared memory when the CTA
+        // ends: wait (bounded) for the last copy issued into every stage,
+        // whether the loop finished or a wait gave up
+        __syncwarp();
+        for (int s = lane; s < S; s += 32) {
+            const int32_t r = sm.issued[s];
+            if (r >= 0 && !ring_wait(smem_addr(&sm.full[s]), (uint32_t)r & 1u))
+                record_status(p.status, KVI_ERR_TIMEOUT);
         }
         return;
     }
@@ -990,6 +1002,9 @@ select_kernel(const __grid_constant__ SelectParams p)
         p.ids[(int64_t)r * k + j] = ok ? sm.out_id[j] : -1;
         p.scores[(int64_t)r * k + j] =
             ok ? key_score(sm.out_key[j]) : __int_as_float(0x7fc00000);
+        // retrieval-only calls: a selected fact whose extent the scorer
+        // found outside the store is reported (placement reports it itself)
+        if (!p.place && ok && sm.out_len[j] < 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
     }
     if (p.place) {
         if (tid < 32) place_request(p, sm, r, ok, st, start, tl);

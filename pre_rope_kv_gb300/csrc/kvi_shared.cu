@@ -177,6 +177,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
         // copy rate far below the SM's share of HBM bandwidth)
         const uint32_t bytes = (uint32_t)(stage_a + stage_b);
         const int na = MT * kTileM / kBoxRowsA, nb = p.Rp / kBoxRowsB;
+        int issued = 0;  // chunks whose copies went out
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % S;
             const int round = kc / S;
@@ -201,6 +202,13 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                     tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
                            kc * kChunk, (j - na) * kBoxRowsB, fb);
             }
+            issued = kc + 1;
+        }
+        // no copy may still be writing into shared memory when the CTA
+        // ends: wait (bounded) for the last chunk issued into every stage
+        if (lane < S && lane < issued) {
+            const int r = (issued - 1 - lane) / S;  // round of stage `lane`'s last chunk
+            if (!wait_bar(saddr(&tl.full[lane]), (uint32_t)(r & 1))) record_status(p.status, KVI_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -236,10 +244,13 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                                  saddr(&tl.empty[s]))
                              : "memory");
             }
-            if (ok)
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 saddr(&tl.mma_done))
-                             : "memory");
+            // committed whatever ended the loop, so that the MMAs issued
+            // are known complete before tensor memory is released; after a
+            // timeout the intervals are not valid (the status says so)
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             saddr(&tl.mma_done))
+                         : "memory");
+            if (!wait_bar(saddr(&tl.mma_done), 0)) record_status(p.status, KVI_ERR_TIMEOUT);
         }
     } else {
         // warps 2-5: thread L owns tensor-memory lane L = fact row L of the

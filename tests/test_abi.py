@@ -122,21 +122,36 @@ def _err(fn, *a):
 
 def test_retrieve_topk_host_validation(lib):
     t = _FakeTensor()
-    assert _err(kvi.kvi_retrieve_topk, _store(), t, 0, t, t, t) == kvi.ERR_INVALID_ARG
-    assert _err(kvi.kvi_retrieve_topk, _store(), t, 257, t, t, t) == kvi.ERR_INVALID_ARG
-    assert _err(kvi.kvi_retrieve_topk, _store(n_facts=5), t, 6, t, t, t) == kvi.ERR_INVALID_ARG
-    assert _err(kvi.kvi_retrieve_topk, _store(), _FakeTensor(0x10004), 5, t, t, t) \
+    f = kvi.kvi_retrieve_topk
+    assert _err(f, _store(), t, 0, t, t, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(), t, 257, t, t, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(n_facts=5), t, 6, t, t, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(), _FakeTensor(0x10004), 5, t, t, t, t) \
         == kvi.ERR_INVALID_ARG                                # misaligned query
-    assert _err(kvi.kvi_retrieve_topk, _store(emb=None), t, 5, t, t, t) \
-        == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(emb=None), t, 5, t, t, t, t) == kvi.ERR_INVALID_ARG
     small = _FakeTensor(n=16)
-    assert _err(kvi.kvi_retrieve_topk, _store(), t, 5, t, t, small) == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(), t, 5, t, t, small, t) == kvi.ERR_INVALID_ARG
     assert "workspace" in kvi.kvi_last_error()
     # the scoring kernels validate every fact's extent: retrieval needs them
     for missing in ("fact_start", "fact_len"):
-        assert _err(kvi.kvi_retrieve_topk, _store(**{missing: None}), t, 5, t, t, t) \
-            == kvi.ERR_INVALID_ARG
+        assert _err(f, _store(**{missing: None}), t, 5, t, t, t, t) == kvi.ERR_INVALID_ARG
         assert "fact_start and fact_len" in kvi.kvi_last_error()
+    # device-side errors (a selected fact with a bad extent, a scoring wait
+    # that gave up) can only be reported through a status word: it is required
+    for status in (None, _FakeTensor(0x10002)):
+        assert _err(f, _store(), t, 5, t, t, t, status) == kvi.ERR_INVALID_ARG
+        assert "status" in kvi.kvi_last_error()
+
+
+def test_retrieve_topk_noalloc_host_validation(lib):
+    t = _FakeTensor()
+    f = kvi.kvi_retrieve_topk_noalloc
+    assert _err(f, _store(), t, 0, t, t, t) == kvi.ERR_INVALID_ARG
+    assert _err(f, _store(n_facts=kvi.NOALLOC_MAX_FACTS + 1), t, 5, t, t, t) == kvi.ERR_INVALID_ARG
+    assert "KVI_NOALLOC_MAX_FACTS" in kvi.kvi_last_error()
+    for status in (None, _FakeTensor(0x10002)):
+        assert _err(f, _store(), t, 5, t, t, status) == kvi.ERR_INVALID_ARG
+        assert "status" in kvi.kvi_last_error()
 
 
 def test_selftest_wait_validation(lib):

@@ -44,7 +44,9 @@ def test_a_wait_that_never_completes_times_out_and_the_context_stays_usable(limi
     ids = torch.empty(10, dtype=torch.int32, device="cuda")
     sc = torch.empty(10, dtype=torch.float32, device="cuda")
     ws = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, 10), dtype=torch.uint8, device="cuda")
-    kvi.kvi_retrieve_topk(view, b.queries[0], 10, ids, sc, ws)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvi.kvi_retrieve_topk(view, b.queries[0], 10, ids, sc, ws, st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     want = oracle.topk(oracle.scores(b.queries_np[0], b.stores[0].emb_np), 10)
     assert np.array_equal(ids.cpu().numpy(), want)

@@ -186,8 +186,8 @@ def _split(b, k, ids_override=None, starts=None):
     ids = torch.empty(k, dtype=torch.int32, device="cuda")
     scores = torch.empty(k, dtype=torch.float32, device="cuda")
     ws = torch.empty(kvi.kvi_workspace_bytes(1, N, k), dtype=torch.uint8, device="cuda")
-    kvi.kvi_retrieve_topk(view, b.queries[0], k, ids, scores, ws)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvi.kvi_retrieve_topk(view, b.queries[0], k, ids, scores, ws, status)
     pos = torch.empty(k, dtype=torch.int32, device="cuda")
     kvi.kvi_place(view, ids, k, int(b.start_pos[0]), pos, status)
     inj_ids, inj_pos = ids, pos

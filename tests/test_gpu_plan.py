@@ -112,3 +112,45 @@ def test_plan_with_request_copies():
         kc.check_selection(got_ids, got_sc, got_pos, orc)
         kc.check_pool_full(b, kc.placements_from_oracle(orc))
     plan.close()
+
+
+def test_plan_replays_after_the_rope_table_grows():
+    # A plan keeps the address of the RoPE table it was recorded with.  A
+    # later call that needs more positions replaces the table for later
+    # calls; the plan's table must stay valid and the replay must still
+    # match the oracle (ids, positions and V bit-exact, K within tolerance).
+    w = synth.Workload(name="planrope", layers=2, kv_heads=2, head_dim=64, rope_theta=5e5,
+                       block_size=16, n_facts=500, len_lo=1, len_hi=24, len_dist="uniform",
+                       embed_dim=128, requests=1, k=12, start=5, start_hi=0, seed=970,
+                       store="dense")
+    b = synth.build_workload(w)
+    f = kc.Fused(b)
+    q_dev = b.queries.clone()
+    spec = kvi.rope(w.rope_theta)
+    plan = kvi.kvi_plan_create_fused(f.g, 1, f.d_views, w.n_facts, q_dev, f.k, f.start, f.bt, f.tl,
+                                     b.max_blocks, f.cache, spec, f.ids, f.scores, f.pos, f.ws,
+                                     f.status)
+    rng = np.random.default_rng(971)
+    for grow_to in (b.max_blocks * w.block_size * 8, 1 << 20):
+        kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, grow_to)
+        b.queries_np = synth.query_rows(rng, 1, w.embed_dim)
+        b.queries = torch.from_numpy(b.queries_np).cuda()
+        q_dev.copy_(b.queries)
+        synth.fill_canary(b.pool)
+        f.status.zero_()
+        plan.launch()
+        ids, scores, pos, status = f.results()
+        assert status == 0
+        orc = kc.oracle_select(b)
+        kc.check_selection(ids, scores, pos, orc)
+        kc.check_pool_full(b, kc.placements_from_oracle(orc))
+    # a direct call now uses the grown table and agrees as well
+    synth.fill_canary(b.pool)
+    f.status.zero_()
+    f()
+    ids, scores, pos, status = f.results()
+    assert status == 0
+    orc = kc.oracle_select(b)
+    kc.check_selection(ids, scores, pos, orc)
+    kc.check_pool_full(b, kc.placements_from_oracle(orc))
+    plan.close()

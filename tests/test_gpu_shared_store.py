@@ -129,8 +129,10 @@ def test_same_ids_as_the_plain_path():
         pid = torch.empty(k, dtype=torch.int32, device="cuda")
         psc = torch.empty(k, dtype=torch.float32, device="cuda")
         pws = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, k), dtype=torch.uint8, device="cuda")
-        kvi.kvi_retrieve_topk(view, dq, k, pid, psc, pws)
+        pst = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvi.kvi_retrieve_topk(view, dq, k, pid, psc, pws, pst)
         torch.cuda.synchronize()
+        assert int(pst.item()) == 0
         assert np.array_equal(pid.cpu().numpy(), ids[r])
         np.testing.assert_array_equal(psc.cpu().numpy(), sc[r])
 
