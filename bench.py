@@ -43,7 +43,13 @@ WORKLOAD = "llama3_8b_10k"
 N_QUERIES = 8          # distinct queries / block tables cycled through the steps
 FLUSH_BYTES = 256 << 20  # > 129 MB L2, written then read between timed steps
 SWEEP_KS = (5, 10, 20, 50)
-PROFILE = os.path.join(ROOT, "profiles", "inject_kernel_llama3_8b_10k.md")
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for the fraction beside the measured peak
+# DRAM bytes (read + write) per algorithmic byte of one inject_kernel launch,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# kernel source with this hash; the bench reports roofline.traffic only while
+# the source still matches (otherwise null).  The capture is on a 1000-fact
+# store of the bench geometry and the ratio scales with the injected tokens.
+INJECT_TRAFFIC = {"source_sha16": None, "dram_bytes_per_algorithmic_byte": None}
 
 
 def parse_args(argv=None):
@@ -57,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other serving workloads in the bench line")
     # profiling case only (not a bench line): a smaller store with the same
     # geometry, so that an ncu capture holds a few GB on the device
     ap.add_argument("--facts", type=int, default=0)
@@ -131,24 +139,39 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def profile_traffic():
-    """dram bytes per inject launch from the committed ncu summary, when it
-    was taken on the current kernel source (else None)."""
-    if not os.path.exists(PROFILE):
-        return None
+def inject_traffic(alg_bytes_per_launch: float):
+    """DRAM bytes per inject launch: the ncu-measured ratio above times the
+    launch's algorithmic bytes, while the kernel source is the one captured
+    (else None)."""
     src = os.path.join(ROOT, "pre_rope_kv_gb300", "csrc", "kvi_inject.cu")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    vals = {}
-    for line in open(PROFILE):
-        if ":" in line and line.startswith("- "):
-            key, _, v = line[2:].rpartition(":")  # keys may hold a colon
-            vals[key.strip()] = v.strip().strip("`")
-    if vals.get("kvi_inject.cu sha256[:16]") != digest:
+    if INJECT_TRAFFIC["source_sha16"] != digest or INJECT_TRAFFIC["dram_bytes_per_algorithmic_byte"] is None:
         return None
+    return round(INJECT_TRAFFIC["dram_bytes_per_algorithmic_byte"] * alg_bytes_per_launch)
+
+
+def host_cpu():
+    """The host's core count and CPU model, for the CPU-baseline lines."""
+    model = None
     try:
-        return float(vals["dram bytes per launch (scaled to the bench launch)"])
-    except (KeyError, ValueError):
-        return None
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    return {"host_nproc": os.cpu_count(), "cpu_model": model or platform.processor() or None,
+            "machine": platform.machine()}
 
 
 # ---------------------------------------------------------------- clocks
@@ -354,6 +377,24 @@ class Bench:
             if trace:
                 stages.append((e[0].elapsed_time(e[1]) / 1e3, e[1].elapsed_time(e[2]) / 1e3))
         return times, stages
+
+    def steady(self, k, steps, warmup):
+        """Back-to-back steps with no L2 flush between them, as a serving
+        loop runs them: the lines the inject kernel leaves dirty in L2 are
+        written back inside the following steps.  Queries and block tables
+        cycle as in the timed region (8 x ~200 MB of distinct facts, far
+        more than L2).  Returns the mean device time per step (s)."""
+        t = self.torch
+        for i in range(warmup):
+            self.step(i, k)
+        t.cuda.synchronize()
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            self.step(i, k)
+        e1.record()
+        t.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
 
     def shared_store(self, R, k, steps, warmup):
         """R concurrent requests over this one store (Section 6.4): median
@@ -656,7 +697,7 @@ def run_ours(args):
     ret = [s[0] for s in stages]
     inj_alg = [2 * step_tokens[i] * w.token_bytes for i in range(args.steps)]
     achieved = sum(inj_alg) / sum(inj) / 1e9
-    traffic = profile_traffic()
+    traffic = inject_traffic(statistics.mean(inj_alg))
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -672,7 +713,8 @@ def run_ours(args):
                          "then 256 MB read (leaves L2 clean)",
                    "queries": f"{N_QUERIES} distinct queries and block tables cycled"},
         "hbm_frac_of_measured_peak": round(hbm_frac, 4),
-        "peak_gbs": peak, "peak_kind": peak_kind,
+        "hbm_frac_of_nominal": round(alg / my_time / 1e9 / NOMINAL_HBM_GBS, 4),
+        "peak_gbs": peak, "peak_kind": peak_kind, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "latency_us_per_request": {str(k): round(statistics.median(times) * 1e6, 2)},
         "facts_per_s": round(world * args.steps * k / t_max, 1),
         "stages_us": {"retrieve_place_median": round(statistics.median(ret) * 1e6, 2),
@@ -686,6 +728,18 @@ def run_ours(args):
         "wall_s_timed_region": round(wall, 4),
     }
     if not args.no_sweep:
+        # steady state: the same steps back to back with no flush between them
+        ss = bench.steady(k, max(24, args.steps), args.warmup)
+        ss_tok = statistics.mean(tokens)
+        ss_alg = 2 * ss_tok * w.token_bytes + emb_bytes
+        out["steady_state"] = {
+            "ms_per_step": round(ss * 1e3, 5),
+            "injected_gb_per_s": round(ss_tok * w.token_bytes / ss / 1e9, 2),
+            "hbm_frac_of_measured_peak": round(ss_alg / ss / 1e9 / peak, 4),
+            "hbm_frac_of_nominal": round(ss_alg / ss / 1e9 / NOMINAL_HBM_GBS, 4),
+            "steps": max(24, args.steps),
+            "note": "fused steps back to back, no L2 flush between them (write-back of each "
+                    "step's dirty lines lands in the next steps); queries cycled as above"}
         lat = {}
         for kk in SWEEP_KS:
             ts, _ = bench.timed(kk, max(10, args.steps), args.warmup)
@@ -735,7 +789,25 @@ def run_ours(args):
                                "kind": "oracle",
                                "sample": f"6 requests of the same workload at k={k} ({toks} "
                                          f"tokens, {secs:.1f} s): float64 scoring of all 10k "
-                                         f"facts, top-k, placement, rotation of every token"}
+                                         f"facts, top-k, placement, rotation of every token",
+                               **host_cpu()}
+    if not args.no_workloads:
+        # the other serving workloads at full size, one after another (the
+        # bench store is freed first: the capacity workload takes ~200 GB)
+        del bench
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        wl = {}
+        for name in ("tiny", "concurrent_64x5k", "mistral_long_50k", "llama3_70b_capacity"):
+            ks = SWEEP_KS if name == "concurrent_64x5k" else (None,)
+            wl[name] = measure_workload(name, ks, min(10, args.steps), min(3, args.warmup),
+                                        cpu_requests=0 if (args.no_cpu_baseline or rank) else 2)
+            gc.collect()
+            torch.cuda.empty_cache()
+        out["workloads"] = wl
+        out["gpu_launches_workloads"] = sum(3 * (e["steps"] + e["warmup"]) for v in wl.values()
+                                            for e in v["by_k"].values())
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:
@@ -1003,100 +1075,138 @@ def graph_index_measure(N, graph_data, k, steps, warmup, full=True):
     return out
 
 
-def run_workload(args):
-    """The other serving workloads at full size: the tiny one (200 facts,
+WORKLOAD_TEXT = {
+    "tiny": "2 layers, 2 KV heads, d=64, theta 1e4; 200 facts of 16 tokens, 384-d embeddings; "
+            "1 request, k=5 at positions 0..79, 16-token pages (dense store)",
+    "concurrent_64x5k": "Llama-3-8B KV geometry; 64 requests, each over its own 5k-fact store "
+                        "(12-48 tokens, 1024-d), start 64, 16-token pages, shared pool with "
+                        "shuffled free-list block tables (arena stand-in, 40 GB)",
+    "mistral_long_50k": "Mistral-7B KV geometry (theta 1e6); 50k facts of 8-128 tokens "
+                        "(log-uniform), k=50 at a random base below 32768, 32-token pages "
+                        "(arena stand-in, 48 GB)",
+    "llama3_70b_capacity": "Llama-3-70B KV geometry (80 layers); 256 requests over their own "
+                           "2k-fact stores (12-48 tokens), k=50, start 64, 16-token pages, pool "
+                           "of ~150 GB (arena stand-in, 48 GB)",
+}
+
+
+def measure_workload(name: str, ks, steps: int, warmup: int, cpu_requests: int = 0) -> dict:
+    """One of the serving workloads at full size: the tiny one (200 facts,
     2 layers, k = 5: a latency figure), 64 concurrent requests over their own
     5k-fact stores, Mistral-7B geometry with 50k facts placed up to 32k, and
-    Llama-3-70B geometry with 256 requests into a ~150 GB pool.  One
-    step = one kvi_retrieve_and_inject call over all requests, L2 flushed
-    between steps.  Prints one JSON line (not the bench line)."""
+    Llama-3-70B geometry with 256 requests into a ~150 GB pool.  One step =
+    one kvi_retrieve_and_inject call over all requests, L2 flushed between
+    steps (outside the events).  ks: the k values to time (None: the
+    workload's own k).  cpu_requests > 0 also times the oracle on that many
+    requests (one thread) and extrapolates the step from it."""
     import torch
     import pre_rope_kv_gb300 as kvi
-    from pre_rope_kv_gb300 import build as kbuild
     from tests import synth
-    kbuild.build()
     kvi.load_library()
-    w = synth.WORKLOADS[args.workload]
-    # the tiny configuration is defined at its own k (5 of 200 facts)
-    k, R = (w.k if args.workload == "tiny" else args.k), w.requests
+    w = synth.WORKLOADS[name]
+    ks = [w.k if kk is None else kk for kk in ks]
+    kmax, R = max(ks), w.requests
     peak, peak_kind = load_peaks()
     g = kvi.geometry(w.layers, w.kv_heads, w.head_dim, w.embed_dim)
-    if args.workload == "llama3_70b_capacity":
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if name == "llama3_70b_capacity":
         # block tables sized to each request's injected tokens, from the
         # library's own selection, as an engine sizes them
-        b = synth.build_workload(w, k=k, with_pool=False)
+        b = synth.build_workload(w, k=kmax, with_pool=False)
         need = []
-        ws1 = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, k), dtype=torch.uint8, device="cuda")
-        st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
-        ids1 = torch.empty(k, dtype=torch.int32, device="cuda")
-        sc1 = torch.empty(k, dtype=torch.float32, device="cuda")
+        ws1 = torch.empty(kvi.kvi_workspace_bytes(1, w.n_facts, kmax), dtype=torch.uint8, device="cuda")
+        ids1 = torch.empty(kmax, dtype=torch.int32, device="cuda")
+        sc1 = torch.empty(kmax, dtype=torch.float32, device="cuda")
         for r, st in enumerate(b.stores):
             view = kvi.store_view(g, b.kv, st.emb, st.fact_start, st.fact_len)
-            kvi.kvi_retrieve_topk(view, b.queries[r], k, ids1, sc1, ws1, st1)
+            kvi.kvi_retrieve_topk(view, b.queries[r], kmax, ids1, sc1, ws1, status)
             torch.cuda.synchronize()
             need.append(int(st.len_np[ids1.cpu().numpy()].sum()))
-        assert int(st1.item()) == 0, f"device status {int(st1.item())}"
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
         synth.attach_pool(b, tokens_needed=need)
+        del ws1
     else:
-        b = synth.build_workload(w, k=k)
+        b = synth.build_workload(w, k=kmax)
     views = [kvi.store_view(g, b.kv, st.emb, st.fact_start, st.fact_len) for st in b.stores]
     d_views = torch.frombuffer(bytearray(kvi.pack_store_views(views)), dtype=torch.uint8).cuda()
     cache = kvi.paged_cache([b.pool[l] for l in range(w.layers)], w.block_size)
-    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
-    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
-    pos = torch.empty((R, k), dtype=torch.int32, device="cuda")
-    ws = torch.empty(kvi.kvi_workspace_bytes(R, w.n_facts, k), dtype=torch.uint8, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     start = torch.from_numpy(b.start_pos).cuda()
     bt = torch.from_numpy(b.block_tables).cuda()
     tl = torch.from_numpy(b.table_lens).cuda()
     kvi.kvi_prepare_rope(w.rope_theta, w.head_dim, int(b.max_blocks) * w.block_size)
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    by_k = {}
+    for k in ks:
+        ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+        sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+        pos = torch.empty((R, k), dtype=torch.int32, device="cuda")
+        ws = torch.empty(kvi.kvi_workspace_bytes(R, w.n_facts, k), dtype=torch.uint8, device="cuda")
 
-    def step():
-        kvi.kvi_retrieve_and_inject(g, R, d_views, w.n_facts, b.queries, k, start, bt, tl,
-                                    b.max_blocks, cache, w.rope_theta, ids, sc, pos, ws, status)
+        def step():
+            kvi.kvi_retrieve_and_inject(g, R, d_views, w.n_facts, b.queries, k, start, bt, tl,
+                                        b.max_blocks, cache, w.rope_theta, ids, sc, pos, ws, status)
 
-    ts = []
-    for i in range(args.warmup + args.steps):
-        flush_w.zero_()
-        flush_r.sum()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        step()
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            ts.append(e0.elapsed_time(e1) / 1e3)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    got = ids.cpu().numpy()
-    tokens = sum(int(b.stores[r].len_np[got[r]].sum()) for r in range(R))
-    t = statistics.median(ts)
-    inj = tokens * w.token_bytes
-    alg = 2 * inj + R * w.n_facts * w.embed_dim * 4
-    out = {
-        "mode": "workload", "workload": args.workload, "requests": R, "k": k,
-        "facts_per_store": w.n_facts, "injected_tokens_per_step": tokens,
-        "ms_per_step": round(t * 1e3, 4), "injected_gb_per_s": round(inj / t / 1e9, 2),
-        "hbm_frac_of_measured_peak": round(alg / t / 1e9 / peak, 4), "peak_gbs": peak,
-        "peak_kind": peak_kind, "steps": args.steps, "warmup": args.warmup,
-        "store": "arena stand-in (distinct fact extents)" if w.store == "arena" else "dense",
-    }
-    if args.workload == "tiny":
-        # 80 injected tokens: a latency figure, not a bandwidth one
-        out["latency_us"] = round(t * 1e6, 2)
-    if not args.no_cpu_baseline:
+        ts = []
+        for i in range(warmup + steps):
+            flush_w.zero_()
+            flush_r.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= warmup:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        got = ids.cpu().numpy()
+        tokens = sum(int(b.stores[r].len_np[got[r]].sum()) for r in range(R))
+        t = statistics.median(ts)
+        inj = tokens * w.token_bytes
+        alg = 2 * inj + R * w.n_facts * w.embed_dim * 4
+        e = {"ms_per_step": round(t * 1e3, 4), "injected_tokens_per_step": tokens,
+             "injected_gb_per_s": round(inj / t / 1e9, 2),
+             "hbm_frac_of_measured_peak": round(alg / t / 1e9 / peak, 4),
+             "hbm_frac_of_nominal": round(alg / t / 1e9 / NOMINAL_HBM_GBS, 4),
+             "latency_us_per_request": round(t / R * 1e6, 2),
+             "facts_per_s": round(R * k / t, 1), "steps": steps, "warmup": warmup}
+        by_k[str(k)] = e
+        del ids, sc, pos, ws
+    out = {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "requests": R,
+           "facts_per_store": w.n_facts, "peak_gbs": peak, "peak_kind": peak_kind,
+           "latency_note": ("single request: latency = step time" if R == 1 else
+                            f"batched: latency = step time / {R} requests (amortised)"),
+           "store": ("arena stand-in: distinct fact extents in a shared physical arena, far "
+                     "larger than L2" if w.store == "arena" else "dense CSR store"),
+           "l2": "flushed between steps outside the timed events",
+           "by_k": by_k}
+    if name == "tiny":
+        out["note"] = "80 injected tokens: a latency figure, not a bandwidth one"
+    del b, d_views, cache, flush_w, flush_r
+    if cpu_requests:
         # the oracle on a seeded sample of requests of this workload, one
         # thread; the whole step is extrapolated from the per-request time
-        n_cpu = 4
-        gbs, secs, toks = cpu_baseline_sample(w, k, n_cpu, w.seed + 99)
+        k = max(ks)
+        gbs, secs, toks = cpu_baseline_sample(w, k, cpu_requests, w.seed + 99)
         out["cpu_baseline"] = {
             "value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_cpu} requests of the workload at k={k} ({toks} tokens, {secs:.1f} s)",
-            "per_request_s": round(secs / n_cpu, 4),
-            "extrapolated_step_s": round(secs / n_cpu * R, 2),
+            "sample": f"{cpu_requests} requests of the workload at k={k} ({toks} tokens, "
+                      f"{secs:.1f} s)",
+            "per_request_s": round(secs / cpu_requests, 4),
+            "extrapolated_step_s": round(secs / cpu_requests * R, 2),
             "extrapolation": f"per-request time x {R} requests (not measured)"}
+    return out
+
+
+def run_workload(args):
+    """One serving workload at full size (its own JSON line, not the bench
+    line); --k picks k (the tiny workload runs at its own k = 5)."""
+    from pre_rope_kv_gb300 import build as kbuild
+    kbuild.build()
+    ks = (None,) if args.workload == "tiny" else (args.k,)
+    out = measure_workload(args.workload, ks, args.steps, args.warmup,
+                           cpu_requests=0 if args.no_cpu_baseline else 4)
+    out["mode"] = "workload"
     print(json.dumps(out), flush=True)
 
 
@@ -1126,7 +1236,8 @@ def run_reference(args):
                    "requests_per_step": 1, "k": k},
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"one request per step ({toks_all} tokens over "
-                                   f"{args.steps} steps), single-threaded float64 oracle"},
+                                   f"{args.steps} steps), single-threaded float64 oracle",
+                         **host_cpu()},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

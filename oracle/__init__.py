@@ -94,6 +94,9 @@ def _load():
             P, i32, i32, i32, i64, P, P, i64, P, P, i32, P, i32, i32, i32, P, i32, P, P, i64,
             P, P]
         lib.kvo_inject_expected_ex.restype = ctypes.c_int
+        lib.kvo_check_rows.argtypes = [P, P, i32, i32, i32, i64, i64, i64, P, P, i32, P, P, i64,
+                                       f64, f64, P, P, P]
+        lib.kvo_check_rows.restype = ctypes.c_int
         lib.kvo_graph_build.argtypes = [P, i64, i64, i32, P]
         lib.kvo_graph_build.restype = ctypes.c_int
         lib.kvo_graph_search.argtypes = [P, P, i64, i64, P, i32, P, i32, i32, i32, i32, i32, P,
@@ -314,6 +317,54 @@ def request(q, emb, k, kv_bits, fact_start, fact_len, start, theta, max_tokens):
     if T < 0:
         raise ValueError("oracle request failed")
     return sel, pos, k_out[:T], v_out[:T]
+
+
+def check_rows(src_bits: np.ndarray, got_bits: np.ndarray, pos: np.ndarray, theta: float,
+               k_rel: float, k_abs: float, rope: dict | None = None, threads: int = 1):
+    """Check T injected tokens against the oracle (see kvo_check_rows).
+
+    src_bits, got_bits: uint16 [L][2][T][H][D] -- the store rows each token
+    came from and the pool rows written for it; pos: int64 [T].  The tokens
+    are split over `threads` host threads, each running the single-threaded
+    C routine on its own range (ctypes releases the interpreter lock).
+    Returns (bad K elements, bad V elements, first bad flat index or -1)."""
+    src_bits = _c(src_bits, np.uint16)
+    got_bits = _c(got_bits, np.uint16)
+    pos = _c(pos, np.int64)
+    L, two, T, H, D = src_bits.shape
+    assert two == 2 and got_bits.shape == src_bits.shape and pos.shape == (T,)
+    spec = rope if rope is not None else rope_spec(theta, D)
+    omega, pairing, cos_p, sin_p, n_tab = _rope_args(spec)
+    lib = _load()
+    n = max(1, min(int(threads), T))
+    cuts = [T * i // n for i in range(n + 1)]
+    res = [None] * n
+
+    def run(i):
+        bk, bv, fb = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        rc = lib.kvo_check_rows(_p(src_bits), _p(got_bits), L, H, D, T, cuts[i], cuts[i + 1],
+                                _p(pos), omega, pairing, cos_p, sin_p, n_tab, float(k_rel),
+                                float(k_abs), ctypes.byref(bk), ctypes.byref(bv), ctypes.byref(fb))
+        res[i] = (rc, bk.value, bv.value, fb.value)
+
+    if n == 1:
+        run(0)
+    else:
+        ts = [threading.Thread(target=run, args=(i,)) for i in range(n)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    bad_k = bad_v = 0
+    first = -1
+    for rc, bk, bv, fb in res:
+        if rc != OK:
+            raise ValueError(f"oracle check_rows: status {rc}")
+        bad_k += bk
+        bad_v += bv
+        if first < 0 and fb >= 0:
+            first = fb
+    return bad_k, bad_v, first
 
 
 def graph_build(emb: np.ndarray, degree: int) -> np.ndarray:

@@ -422,6 +422,87 @@ void kvo_slots(const int64_t *p, int64_t n, const int32_t *block_table,
     }
 }
 
+/* Parity check of many injected tokens at once (for pools too large for
+ * kvo_inject_expected; test infrastructure like the rest of this file).
+ *
+ * src and got hold T tokens' rows in the store's layout [L][2][T][H][D]
+ * (bf16 bits): src[.][.][t] the store rows token t was injected from, got
+ * the pool rows the path under test wrote for it; pos[t] its position.
+ * Only tokens t0 <= t < t1 are checked (callers split T over threads).
+ *
+ * Expected values are those of kvo_token_rows_ex: K is src's K rotated to
+ * pos[t] (Section 5.1, Chunked RoPE) -- with the cos and sin of
+ * pos[t] * omega_i, which depend on the position only and are therefore
+ * computed once per token for all of its L * H rows, or with the caller's
+ * table row pos[t] -- and V is src's V bits unchanged.  A K element counts
+ * as bad when |got - y| > k_rel |y| + k_abs (y the float64 expected value);
+ * a V element when its bits differ.  Outputs: bad_k, bad_v, and first_bad =
+ * the flat index into [L][2][T][H][D] of the first bad element met, or -1.
+ * Returns KVO_OK, KVO_OUT_OF_RANGE (a position outside the table) or
+ * KVO_BAD_ARG. */
+int kvo_check_rows(const uint16_t *src, const uint16_t *got, int32_t L, int32_t H,
+                   int32_t D, int64_t T, int64_t t0, int64_t t1, const int64_t *pos,
+                   const double *omega, int32_t pairing, const float *cos_tab,
+                   const float *sin_tab, int64_t tab_positions, double k_rel,
+                   double k_abs, int64_t *bad_k, int64_t *bad_v, int64_t *first_bad)
+{
+    *bad_k = 0;
+    *bad_v = 0;
+    *first_bad = -1;
+    if (t0 < 0 || t1 > T || t0 > t1 || D < 2 || D % 2) return KVO_BAD_ARG;
+    const int32_t half = D / 2;
+    double *c = (double *)malloc((size_t)half * sizeof *c);
+    double *sn = (double *)malloc((size_t)half * sizeof *sn);
+    double *x = (double *)malloc((size_t)D * sizeof *x);
+    double *y = (double *)malloc((size_t)D * sizeof *y);
+    if (!c || !sn || !x || !y) { free(c); free(sn); free(x); free(y); return KVO_BAD_ARG; }
+    int rc = KVO_OK;
+    const int64_t hd = (int64_t)H * D;
+    for (int64_t t = t0; t < t1; ++t) {
+        const int64_t p = pos[t];
+        if (cos_tab) {
+            if (p < 0 || p >= tab_positions) { rc = KVO_OUT_OF_RANGE; break; }
+            for (int32_t i = 0; i < half; ++i) {
+                c[i] = (double)cos_tab[p * half + i];
+                sn[i] = (double)sin_tab[p * half + i];
+            }
+        } else {
+            for (int32_t i = 0; i < half; ++i) {
+                const double ang = (double)p * omega[i];
+                c[i] = cos(ang);
+                sn[i] = sin(ang);
+            }
+        }
+        for (int32_t l = 0; l < L; ++l) {
+            const int64_t kbase = (((int64_t)l * 2 + 0) * T + t) * hd;
+            const int64_t vbase = (((int64_t)l * 2 + 1) * T + t) * hd;
+            for (int32_t h = 0; h < H; ++h) {
+                const int64_t at = kbase + (int64_t)h * D;
+                for (int32_t i = 0; i < D; ++i) x[i] = kvo_bf16_to_double(src[at + i]);
+                kvo_rotate_cs(x, D, c, sn, pairing, y);
+                for (int32_t i = 0; i < D; ++i) {
+                    const double g = kvo_bf16_to_double(got[at + i]);
+                    if (!(fabs(g - y[i]) <= k_rel * fabs(y[i]) + k_abs)) {
+                        if (*first_bad < 0) *first_bad = at + i;
+                        ++*bad_k;
+                    }
+                }
+            }
+            for (int64_t e = 0; e < hd; ++e) {
+                if (got[vbase + e] != src[vbase + e]) {
+                    if (*first_bad < 0) *first_bad = vbase + e;
+                    ++*bad_v;
+                }
+            }
+        }
+    }
+    free(c);
+    free(sn);
+    free(x);
+    free(y);
+    return rc;
+}
+
 /* ------------------------------------------------------------------------
  * Graph index.  The review's Summary retrieves facts through a GPU ANN index
  * (Jasper) instead of a scan, and its Axiom & Free-Parameter Ledger fixes

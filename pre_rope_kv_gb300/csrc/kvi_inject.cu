@@ -94,7 +94,7 @@ struct __align__(128) InjSmem {
     uint8_t stage[kInjRing][kPieceMax];
     uint64_t full[kInjRing];
     uint64_t empty[kInjRing];
-    int32_t issued[kInjRing];  // round of the last copy issued into each stage, -1: none
+    int32_t issued[kInjRing];  // last round whose "full" phase each stage started, -1: none
     PieceDesc desc[kInjRing];
     int32_t prefix[kMaxPrefix + 1];
     int32_t part[kInjThreads];
@@ -603,7 +603,7 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 } else {
                     staged = true;
                     sm.desc[s] = PieceDesc{x.dst, x.bytes, x.pos0, x.ntok, (int16_t)x.kv, 0};
-                    if (x.bytes) sm.issued[s] = (int32_t)round;
+                    sm.issued[s] = (int32_t)round;
                     const uint32_t fb = smem_u32(&sm.full[s]);
                     if (x.bytes && !x.direct) {
                         // the stage's previous contents were read by the
@@ -666,13 +666,17 @@ inject_kernel(const __grid_constant__ InjectParams p)
                 record_status(p.status, KVI_ERR_TIMEOUT);
             } else {
                 sm.desc[s] = PieceDesc{nullptr, 0u, 0, 0, 0, 1};
+                sm.issued[s] = (int32_t)round;
                 mbar_arrive(smem_u32(&sm.full[s]));
             }
         }
         // Leave no copy in flight into this CTA's shared memory: whatever
-        // ended the loop (the last item, or a wait that gave up), each
-        // stage's last issued copy is waited for, with a bound, before the
-        // producer exits.  After a normal end they have all landed already.
+        // ended the loop (the last item, or a wait that gave up), the last
+        // "full" phase the producer started on each stage (a copy, or a
+        // plain arrival that completes at once) is waited for, with a
+        // bound, before the producer exits.  The phase tracked must be the
+        // last one: waiting on an earlier phase's parity after two more
+        // phases began would wait on an incomplete phase of equal parity.
         __syncwarp();
         if (lane < kInjRing) {
             const int32_t r = sm.issued[lane];

@@ -244,7 +244,7 @@ struct ScoreRingSmem {
     uint8_t ring[kRingBytes];
     uint64_t full[kRingMaxStages];
     uint64_t empty[kRingMaxStages];
-    int32_t issued[kRingMaxStages];  // round of the last copy into each stage, -1: none
+    int32_t issued[kRingMaxStages];  // last round whose "full" phase each stage started, -1: none
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -351,8 +351,8 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
                 } else {
                     sc.get(p, cur.r);
                     const uint32_t fb = smem_addr(&sm.full[s]);
+                    sm.issued[s] = (int32_t)round;
                     if (sc.live(cur.i)) {
-                        sm.issued[s] = (int32_t)round;
                         if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
                                      "r"(row_bytes)
@@ -370,8 +370,9 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
             if (!__all_sync(0xffffffffu, ok)) break;
         }
         // no copy may still be writing into shared memory when the CTA
-        // ends: wait (bounded) for the last copy issued into every stage,
-        // whether the loop finished or a wait gave up
+        // ends: wait (bounded) for the last "full" phase started on every
+        // stage (a copy, or an arrival that completes at once), whether the
+        // loop finished or a wait gave up
         __syncwarp();
         for (int s = lane; s < S; s += 32) {
             const int32_t r = sm.issued[s];

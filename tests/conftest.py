@@ -26,3 +26,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Element counts of the exhaustive full-size parity checks."""
+    try:
+        from tests import kvi_check
+    except Exception:
+        return
+    if kvi_check.PARITY_LOG:
+        terminalreporter.section("full-size parity: elements compared")
+        for line in kvi_check.PARITY_LOG:
+            terminalreporter.write_line(line)

@@ -223,6 +223,83 @@ def check_pool_sampled(b: synth.Built, placements, n_samples: int, seed: int = 0
     return pick.shape[0]
 
 
+# Lines of element counts from the exhaustive checks, printed at the end of
+# a pytest session (tests/conftest.py).
+PARITY_LOG: list[str] = []
+
+
+def check_pool_exhaustive(b: synth.Built, placements, rope: dict | None = None,
+                          chunk_bytes: int = 1 << 30, label: str = ""):
+    """Large pools: every injected token's rows (all layers and heads, K and
+    V) compared element by element with the oracle.  Tokens are taken in
+    chunks: the pool rows written for them and the store rows they came
+    from are gathered on the device, copied to pinned host memory, and the
+    oracle's check_rows runs over the chunk on all host cores while the next
+    chunk is gathered.  Returns (tokens, elements compared, host threads)."""
+    import concurrent.futures as cf
+    import os
+    rr, ff, tt, pp = token_list(b, placements)
+    n_tok = rr.shape[0]
+    assert n_tok > 0
+    w = b.w
+    L, H, D, B = w.layers, w.kv_heads, w.head_dim, w.block_size
+    NB = b.num_blocks
+    tok_bytes = L * 2 * H * D * 2
+    per = max(1, chunk_bytes // tok_bytes)
+    slot = np.empty(n_tok, np.int64)
+    row = np.empty(n_tok, np.int64)
+    for r in range(w.requests):
+        m = rr == r
+        if not m.any():
+            continue
+        blk, off = oracle.slots(pp[m], b.block_tables[r, :b.table_lens[r]], B, NB)
+        assert np.all(blk >= 0), f"request {r}: a position outside its block table"
+        slot[m] = blk.astype(np.int64) * B + off
+        row[m] = b.stores[r].start_np[ff[m]] + tt[m]
+    pool_v = b.pool.view(torch.int16).view(L * 2, NB * B, H * D)
+    kv_v = b.kv.view(torch.int16).view(L * 2, b.kv.shape[2], H * D)
+    threads = os.cpu_count() or 1
+    bufs = [(torch.empty((L * 2, per, H * D), dtype=torch.int16).pin_memory(),
+             torch.empty((L * 2, per, H * D), dtype=torch.int16).pin_memory()) for _ in range(2)]
+    slot_d = torch.from_numpy(slot).cuda()
+    row_d = torch.from_numpy(row).cuda()
+
+    def check(i, a, n):
+        src_h, got_h = bufs[i]
+        src = src_h[:, :n].numpy().view(np.uint16).reshape(L, 2, n, H, D)
+        got = got_h[:, :n].numpy().view(np.uint16).reshape(L, 2, n, H, D)
+        bad_k, bad_v, first = oracle.check_rows(src, got, pp[a:a + n], w.rope_theta, K_REL, K_ABS,
+                                                rope, threads=threads)
+        if bad_k or bad_v:
+            l, c, t, h, e = np.unravel_index(first, (L, 2, n, H, D))
+            j = a + t
+            raise AssertionError(
+                f"{bad_k} K and {bad_v} V elements off the oracle; first: request {rr[j]} fact "
+                f"{ff[j]} token {tt[j]} position {pp[j]} layer {l} {'KV'[c]} head {h} elem {e}: "
+                f"gpu bits {got[l, c, t, h, e]:#06x}, store bits {src[l, c, t, h, e]:#06x}")
+
+    with cf.ThreadPoolExecutor(max_workers=1) as ex:
+        pending = None
+        for ci, a in enumerate(range(0, n_tok, per)):
+            n = min(per, n_tok - a)
+            i = ci % 2
+            if pending is not None and pending[1] == i:
+                pending[0].result()  # this buffer pair is free again
+                pending = None
+            src_h, got_h = bufs[i]
+            src_h[:, :n].copy_(kv_v.index_select(1, row_d[a:a + n]))
+            got_h[:, :n].copy_(pool_v.index_select(1, slot_d[a:a + n]))
+            if pending is not None:
+                pending[0].result()
+            pending = (ex.submit(check, i, a, n), i)
+        if pending is not None:
+            pending[0].result()
+    elements = n_tok * L * 2 * H * D
+    PARITY_LOG.append(f"{label or w.name}: {n_tok} tokens, {elements} elements (K and V, all "
+                      f"layers and heads) compared with the oracle on {threads} host threads")
+    return n_tok, elements, threads
+
+
 def check_canaries_by_row(b: synth.Built, placements):
     """Every (block, offset) row the oracle's placement maps a token to is
     written in every layer for K and V; every other row keeps its canary."""

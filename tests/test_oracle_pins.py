@@ -536,3 +536,93 @@ def test_table_rows_in_token_rows():
         np.testing.assert_array_equal(vt, vp)
     with pytest.raises(ValueError):
         oracle.token_rows(kv, 1, 0.0, P, rope)
+
+
+# ------------------------------------------------------- batched row check
+
+def _rne_bf16_bits(y):
+    """float64 -> float32 -> bf16 bits, round to nearest even (numpy)."""
+    u = np.asarray(y, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _check_rows_case(seed, L=3, H=2, D=16, T=7, theta=1e4):
+    rng = np.random.default_rng(seed)
+    src = _rne_bf16_bits(rng.standard_normal((L, 2, T, H, D)))  # bf16 ~N(0,1), as stored
+    pos = rng.integers(0, 40000, size=T).astype(np.int64)
+    pos[0] = 0
+    want_k = np.empty((L, T, H, D))
+    for t in range(T):
+        k, v = oracle.token_rows_from_rows(src[:, 0, t], src[:, 1, t], theta, int(pos[t]))
+        want_k[:, t] = k
+        assert np.array_equal(v, src[:, 1, t])
+    return src, pos, want_k
+
+
+def test_check_rows_agrees_with_token_rows():
+    # the batched check computes each token's cos/sin once; its expected
+    # values must be those of the per-row routine (pinned above): with the
+    # path's result being the RNE bf16 of the expected values, nothing is
+    # off within one bf16 ulp, and with a zero tolerance exactly the
+    # elements that bf16 cannot hold are off
+    src, pos, want_k = _check_rows_case(21)
+    got = src.copy()
+    got[:, 0] = _rne_bf16_bits(want_k)
+    assert oracle.check_rows(src, got, pos, 1e4, 2.0 ** -8, 1e-6) == (0, 0, -1)
+    inexact = int(np.sum(np.vectorize(oracle.bf16_to_double)(got[:, 0]) != want_k))
+    bad_k, bad_v, first = oracle.check_rows(src, got, pos, 1e4, 0.0, 0.0)
+    assert bad_k == inexact and bad_v == 0 and inexact > 0
+    # the threaded split gives the same counts
+    assert oracle.check_rows(src, got, pos, 1e4, 0.0, 0.0, threads=3)[:2] == (bad_k, 0)
+
+
+def test_check_rows_position_zero_is_a_copy():
+    src, pos, _ = _check_rows_case(22)
+    pos[:] = 0
+    assert oracle.check_rows(src, src.copy(), pos, 1e4, 0.0, 0.0) == (0, 0, -1)
+
+
+def test_check_rows_finds_planted_errors():
+    src, pos, want_k = _check_rows_case(23)
+    good = src.copy()
+    good[:, 0] = _rne_bf16_bits(want_k)
+    L, _, T, H, D = src.shape
+    # a K element moved by 4 bf16 ulps (well outside 2^-8 |x|)
+    bad = good.copy()
+    l, t, h, i = 2, 5, 1, 9
+    bad[l, 0, t, h, i] = bad[l, 0, t, h, i] + 4 if want_k[l, t, h, i] != 0 else 0x3F80
+    flat = (((l * 2 + 0) * T + t) * H + h) * D + i
+    assert oracle.check_rows(src, bad, pos, 1e4, 2.0 ** -8, 1e-6) == (1, 0, flat)
+    # one V bit flipped
+    bad = good.copy()
+    bad[0, 1, 3, 0, 2] ^= 1
+    flat = (((0 * 2 + 1) * T + 3) * H + 0) * D + 2
+    assert oracle.check_rows(src, bad, pos, 1e4, 2.0 ** -8, 1e-6) == (0, 1, flat)
+    # a wrong position for one token: its K rows fail (nearly) everywhere
+    wrong = pos.copy()
+    wrong[4] += 1000  # turns even the slowest pair (omega_7 = 10^-3.5) by 0.3 rad
+    bk, bv, _ = oracle.check_rows(src, good, wrong, 1e4, 2.0 ** -8, 1e-6)
+    assert bv == 0 and bk > L * H * D // 2
+    # the wrong pairing fails too
+    spec = oracle.rope_spec(1e4, D, oracle.PAIR_INTERLEAVED)
+    bk, _, _ = oracle.check_rows(src, good, pos, 1e4, 2.0 ** -8, 1e-6, rope=spec)
+    assert bk > (T - 1) * L * H * D // 2
+
+
+def test_check_rows_with_a_table():
+    # a caller's cos/sin table is read at each token's position
+    src, pos, _ = _check_rows_case(24, T=5)
+    D = src.shape[4]
+    P = int(pos.max()) + 1
+    ang = np.arange(P)[:, None] * oracle.rope_omega(1e4, D)[None, :]
+    spec = oracle.rope_spec(1e4, D, cos_table=np.cos(ang).astype(np.float32),
+                            sin_table=np.sin(ang).astype(np.float32))
+    got = src.copy()
+    for t in range(src.shape[2]):
+        k, _ = oracle.token_rows_from_rows(src[:, 0, t], src[:, 1, t], 1e4, int(pos[t]), rope=spec)
+        got[:, 0, t] = _rne_bf16_bits(k)
+    assert oracle.check_rows(src, got, pos, 1e4, 2.0 ** -8, 1e-6, rope=spec) == (0, 0, -1)
+    short = oracle.rope_spec(1e4, D, cos_table=np.ones((1, D // 2), np.float32),
+                             sin_table=np.zeros((1, D // 2), np.float32))
+    with pytest.raises(ValueError):
+        oracle.check_rows(src, got, pos, 1e4, 2.0 ** -8, 1e-6, rope=short)
