@@ -487,6 +487,9 @@ struct SelectSmem {
     int32_t out_len[KVI_MAX_K];
     int32_t out_pc[KVI_MAX_K];
     uint32_t warp_tot[32];
+    int64_t out_s0[KVI_MAX_K];  // placement: first store row of each selected fact
+    int64_t wsum[32];   // placement: lengths per warp
+    int32_t wpc[32];    // placement: inject pieces per warp
     uint32_t n_sure, n_cand, bucket, above, digit, above2, pop;
 };
 
@@ -616,87 +619,6 @@ __device__ __noinline__ void select_crowded(SelectSmem &sm, const uint64_t *keys
     __syncthreads();
 }
 
-// Placement of one request by warp 0: rank order, back to back from the
-// request's start; each fact is cut into the inject kernel's pieces.
-__device__ __forceinline__ void place_request(const SelectParams &p, SelectSmem &sm, int r, bool ok,
-                              const kvi_store_view &st, int64_t start, int32_t tl)
-{
-    const int lane = threadIdx.x;
-    const int32_t k = p.k;
-    if (!ok && lane == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
-    constexpr int kPer = (KVI_MAX_K + 31) / 32;
-    const int per = (k + 31) / 32;
-    const int j0 = lane * per;
-    int64_t len_run = 0;
-    int32_t lens_l[kPer];
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-        const int j = j0 + m;
-        int32_t len = 0;
-        if (m < per && j < k && ok) {
-            const int32_t f = sm.out_id[j];
-            len = sm.out_len[j];
-            if (f < 0 || (int64_t)f >= st.n_facts || len < 0) {
-                record_status(p.status, KVI_ERR_OUT_OF_RANGE);
-                len = 0;
-            }
-        }
-        lens_l[m] = len;
-        len_run += len;
-    }
-    int64_t incl = len_run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-    int fit = ok ? 1 : 0;
-    if (tl < 0 || tl > p.max_blocks) {
-        if (lane == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
-        fit = 0;
-    } else if (start < 0 || start + total > (int64_t)tl * p.block_size) {
-        if (lane == 0 && ok) record_status(p.status, KVI_ERR_CAPACITY);
-        fit = 0;
-    }
-    int64_t run = start + incl - len_run;
-    int64_t pieces = 0;
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-        const int j = j0 + m;
-        if (m >= per || j >= k) break;
-        const int32_t len = lens_l[m];
-        int32_t pc = 0;
-        if (fit && len > 0) {  // positions fit 31 bits once the request fits its table
-            const uint32_t ct = (uint32_t)p.pg.ct;
-            const uint32_t first = (uint32_t)run / ct, last = (uint32_t)(run + len - 1) / ct;
-            pc = (int32_t)((last - first + 1) * (uint32_t)p.pg.units);
-        }
-        p.pos[(int64_t)r * k + j] = (int32_t)run;
-        p.slot_len[(int64_t)r * k + j] = len;
-        sm.out_pc[j] = pc;
-        pieces += pc;
-        run += len;
-    }
-    int64_t pincl = pieces;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t t = __shfl_up_sync(0xffffffffu, pincl, o);
-        if (lane >= o) pincl += t;
-    }
-    int64_t prun = pincl - pieces;
-    for (int m = 0; m < per; ++m) {
-        const int j = j0 + m;
-        if (j >= k) break;
-        p.pc[(int64_t)r * (k + 1) + j] = (int32_t)prun;
-        prun += sm.out_pc[j];
-    }
-    if (lane == 31) {
-        p.pc[(int64_t)r * (k + 1) + k] = (int32_t)pincl;
-        p.npc[r] = (int32_t)pincl;
-    }
-}
-
 // Selection by histogram (the general path): a shared-memory histogram of
 // the keys' float32 parts finds the bucket that holds the k-th key; buckets
 // above it are taken whole and the k-th bucket's keys are ranked exactly or,
@@ -792,40 +714,151 @@ __device__ __noinline__ void select_by_histogram(SelectSmem &sm, const uint64_t 
     __syncthreads();
 }
 
-// Warps 1.. of the selecting CTA, while warp 0 places the request: write
-// the first store row of every selected fact for the inject kernel (so that
-// it needs no dependent load of fact_start), and touch the first facts it
-// will move -- the best-ranked ones, every layer's K and V rows -- with one
-// 128-byte L2 prefetch each, which warms their address translations.
 constexpr int kWarmFacts = 8;
 constexpr int kSelectGroups = 256;
 
-__device__ __forceinline__ void fact_rows(const SelectParams &p, const SelectSmem &sm,
-                                          const kvi_store_view &st, int r, int32_t k)
+// t* = the largest t such that at least k of the 256 values v (8 per lane of
+// the calling warp) are >= t, for 1 <= k <= 256.  The smallest value always
+// qualifies and max + 1 never does, so a 4-ary search between the two
+// (three independent warp counts per round) finds t* in log4 of the range
+// of values rounds.
+__device__ __forceinline__ uint32_t kth_largest_bound(const uint32_t (&v)[kSelectGroups / 32], uint32_t k)
 {
-    const int t = threadIdx.x - 32;
-    const int L = p.g.layers;
-    const int64_t row_bytes = (int64_t)p.g.kv_heads * p.g.head_dim * 2;
-    // lengths are -1 unless the scoring kernel found the extent inside the
-    // store; only such facts have a row (the others inject nothing)
-    for (int j = t; j < k; j += kSelectThreads - 32) {
-        const int32_t f = sm.out_id[j];
-        int64_t s0 = 0;
-        if (sm.out_len[j] > 0 && f >= 0 && (int64_t)f < st.n_facts) s0 = __ldg(st.fact_start + f);
-        p.rows[(int64_t)r * k + j] = s0;
+    uint32_t vmin = v[0], vmax = v[0];
+#pragma unroll
+    for (int i = 1; i < kSelectGroups / 32; ++i) {
+        vmin = min(vmin, v[i]);
+        vmax = max(vmax, v[i]);
     }
-    const int nf = min(k, kWarmFacts);
-    for (int e = t; e < nf * 2 * L; e += kSelectThreads - 32) {
-        const int j = e / (2 * L);
-        const int plane = e - j * 2 * L;  // layer * 2 + (K|V)
-        const int32_t len = sm.out_len[j];
-        const int32_t f = sm.out_id[j];
-        if (len <= 0 || f < 0 || (int64_t)f >= st.n_facts) continue;
-        const int64_t s0 = __ldg(st.fact_start + f);
-        if (s0 < 0 || s0 + len > st.n_tokens) continue;
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(st.kv) +
-                             ((int64_t)plane * st.n_tokens + s0) * row_bytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 128;" ::"l"(src) : "memory");
+    uint32_t lo = __reduce_min_sync(0xffffffffu, vmin);
+    uint32_t hi = __reduce_max_sync(0xffffffffu, vmax) + 1u;
+    while (hi - lo > 1) {
+        const uint32_t d = hi - lo;
+        const uint32_t m1 = lo + d / 4, m2 = lo + d / 2, m3 = lo + (3 * d) / 4;
+        uint32_t a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+        for (int i = 0; i < kSelectGroups / 32; ++i) {
+            a1 += v[i] >= m1 ? 1u : 0u;
+            a2 += v[i] >= m2 ? 1u : 0u;
+            a3 += v[i] >= m3 ? 1u : 0u;
+        }
+        const uint32_t c1 = __reduce_add_sync(0xffffffffu, a1);
+        const uint32_t c2 = __reduce_add_sync(0xffffffffu, a2);
+        const uint32_t c3 = __reduce_add_sync(0xffffffffu, a3);
+        // count(>= lo) >= k > count(>= hi) stays true; equal midpoints
+        // give equal counts, so each branch shrinks the range
+        if (c3 >= k) lo = m3;
+        else if (c2 >= k) { lo = m2; hi = m3; }
+        else if (c1 >= k) { lo = m1; hi = m2; }
+        else hi = m1;
+    }
+    return lo;
+}
+
+// Placement of one request (Figure 2 caption, "positioned by chunked RoPE";
+// rank order, back to back from the request's start), one thread per
+// selected fact j < k: its length, the exclusive prefix of the lengths (its
+// position) and of its inject pieces, by warp scans and one table of warp
+// totals.  Also writes each fact's first store row for the inject kernel
+// (so that it needs no dependent load of fact_start) and, from the spare
+// warps, touches the first facts it will move -- every layer's K and V rows
+// of the best-ranked kWarmFacts facts, which the inject kernel's first items
+// cover -- with one 128-byte L2 prefetch each, which warms their address
+// translations (device-resident stores only; prefetching whole runs from one
+// SM is far too slow: its bulk-copy unit moves them one after another).  All
+// threads of the CTA call this.
+__device__ __forceinline__ void place_parallel(const SelectParams &p, SelectSmem &sm, int r, bool ok,
+                                               const kvi_store_view &st, int64_t start, int32_t tl)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t k = p.k;
+    const int kw = (k + 31) / 32;  // warps holding a fact
+    const int j = tid;
+    int32_t len = 0;
+    int32_t f = -1;
+    int64_t s0 = 0;
+    if (j < k && ok) {
+        f = sm.out_id[j];
+        len = sm.out_len[j];
+        if (f < 0 || (int64_t)f >= st.n_facts || len < 0) {
+            record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+            len = 0;
+        }
+        // lengths are -1 unless the scoring kernel found the extent inside
+        // the store; only facts with a row inject anything
+        if (len > 0) s0 = __ldg(st.fact_start + f);
+    }
+    if (!ok && tid == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+    int64_t incl = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (warp < kw && lane == 31) sm.wsum[warp] = incl;
+    __syncthreads();
+    int64_t before = 0, total = 0;
+    for (int w = 0; w < kw; ++w) {
+        const int64_t t = sm.wsum[w];
+        before += w < warp ? t : 0;
+        total += t;
+    }
+    int fit = ok ? 1 : 0;
+    if (tl < 0 || tl > p.max_blocks) {
+        if (tid == 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
+        fit = 0;
+    } else if (start < 0 || start + total > (int64_t)tl * p.block_size) {
+        if (tid == 0 && ok) record_status(p.status, KVI_ERR_CAPACITY);
+        fit = 0;
+    }
+    const int64_t run = start + before + incl - len;  // this fact's first position
+    int32_t pc = 0;
+    if (j < k) {
+        if (fit && len > 0) {  // positions fit 31 bits once the request fits its table
+            const uint32_t ct = (uint32_t)p.pg.ct;
+            const uint32_t first = (uint32_t)run / ct, last = (uint32_t)(run + len - 1) / ct;
+            pc = (int32_t)((last - first + 1) * (uint32_t)p.pg.units);
+        }
+        p.pos[(int64_t)r * k + j] = (int32_t)run;
+        p.slot_len[(int64_t)r * k + j] = len;
+        if (ok) p.rows[(int64_t)r * k + j] = s0;
+        sm.out_s0[j] = s0;
+    }
+    int32_t pin = pc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, pin, o);
+        if (lane >= o) pin += t;
+    }
+    if (warp < kw && lane == 31) sm.wpc[warp] = pin;
+    __syncthreads();
+    int32_t pbefore = 0, ptotal = 0;
+    for (int w = 0; w < kw; ++w) {
+        const int32_t t = sm.wpc[w];
+        pbefore += w < warp ? t : 0;
+        ptotal += t;
+    }
+    if (j < k) p.pc[(int64_t)r * (k + 1) + j] = pbefore + pin - pc;
+    if (tid == 0) {
+        p.pc[(int64_t)r * (k + 1) + k] = ptotal;
+        p.npc[r] = ptotal;
+    }
+    // warm the first facts' translations (warps past the ones holding
+    // facts; the rows were stored in shared memory before the last barrier)
+    if (ok && warp >= kw && !(st.flags & KVI_STORE_KV_HOST)) {
+        const int L = p.g.layers;
+        const int64_t row_bytes = (int64_t)p.g.kv_heads * p.g.head_dim * 2;
+        const int nf = min(k, kWarmFacts);
+        for (int e = tid - 32 * kw; e < nf * 2 * L; e += kSelectThreads - 32 * kw) {
+            const int jj = e / (2 * L);
+            const int plane = e - jj * 2 * L;  // layer * 2 + (K|V)
+            const int32_t ln = sm.out_len[jj];
+            const int64_t a0 = sm.out_s0[jj];
+            if (ln <= 0 || a0 < 0 || a0 + ln > st.n_tokens) continue;
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(st.kv) +
+                                 ((int64_t)plane * st.n_tokens + a0) * row_bytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], 128;" ::"l"(src) : "memory");
+        }
     }
 }
 
@@ -837,16 +870,6 @@ select_kernel(const __grid_constant__ SelectParams p)
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t k = p.k;
-
-    for (int b = tid; b < kHistBins; b += kSelectThreads) sm.hist[b] = 0;
-    for (int e = tid; e < KVI_MAX_K; e += kSelectThreads) {
-        sm.sure_key[e] = 0;
-        sm.sure_id[e] = -1;
-        sm.sure_len[e] = -1;
-        sm.out_key[e] = 0;
-        sm.out_id[e] = -1;
-        sm.out_len[e] = -1;
-    }
     if (tid == 0) {
         sm.n_sure = 0;
         sm.n_cand = 0;
@@ -854,8 +877,8 @@ select_kernel(const __grid_constant__ SelectParams p)
 
     // the request's own inputs (its store view, start and table length) can
     // be read before the scoring kernel ends: only keys and lengths are its
-    const int64_t start = (p.place && tid < 32) ? (int64_t)p.start_pos[r] : 0;
-    const int32_t tl = (p.place && tid < 32) ? p.table_lens[r] : 0;
+    const int64_t start = p.place ? (int64_t)p.start_pos[r] : 0;
+    const int32_t tl = p.place ? p.table_lens[r] : 0;
     const kvi_store_view st = load_store(p.store, r);
     const bool ok = !p.store.many || store_ok(st, p.g, p.max_facts, k);
     pdl_wait();  // keys and lengths of the scoring kernel
@@ -883,18 +906,17 @@ select_kernel(const __grid_constant__ SelectParams p)
     // the largest t such that at least k groups hold a key with h >= t: then
     // at least k keys have h >= t*, and any key with h < t* has k keys above
     // it, so the top k all have h >= t*.  The groups' largest h go to shared
-    // memory and one warp finds t* by a binary search (16 steps, no block
-    // barriers); the keys with h >= t* are collected (typically little more
-    // than k) and ranked exactly.  If more than kCandCap keys qualify (heavy
-    // ties), select_by_histogram runs instead.
+    // memory and one warp finds t* (kth_largest_bound, no block barriers);
+    // the keys with h >= t* are collected (typically little more than k) and
+    // ranked exactly.  If more than kCandCap keys qualify (heavy ties),
+    // select_by_histogram runs instead.
     bool fast = false;
     if (ok) {
         uint32_t mt = 0;  // this thread's largest h (0 also when it has no key)
         static_assert(kSelectThreads / 4 == kSelectGroups, "groups of 4 threads");
         if (in_regs) {
 #pragma unroll
-            for (int m = 0; m < kKeysPerThread; ++m)
-                if (tid + (int64_t)m * kSelectThreads < N) mt = max(mt, (uint32_t)(kr[m] >> 48));
+            for (int m = 0; m < kKeysPerThread; ++m) mt = max(mt, (uint32_t)(kr[m] >> 48));
         } else {
             for (int64_t i = tid; i < N; i += kSelectThreads) mt = max(mt, (uint32_t)(__ldcg(keys + i) >> 48));
         }
@@ -904,25 +926,18 @@ select_kernel(const __grid_constant__ SelectParams p)
         if ((lane & 3) == 0) sm.hist[tid >> 2] = mt;
         __syncthreads();
         if (warp == 0) {
-            // t = 0 always qualifies here: with fewer than k groups holding
-            // keys it stays 0 and every key becomes a candidate
+            // t = 0 qualifies whenever fewer than k groups hold keys: then
+            // every key becomes a candidate
             uint32_t v[kSelectGroups / 32];
 #pragma unroll
             for (int i = 0; i < kSelectGroups / 32; ++i) v[i] = sm.hist[i * 32 + lane];
-            uint32_t lo = 0, hi = 1u << 16;
-            while (hi - lo > 1) {
-                const uint32_t mid = (lo + hi) >> 1;
-                uint32_t c = 0;
-#pragma unroll
-                for (int i = 0; i < kSelectGroups / 32; ++i) c += v[i] >= mid ? 1u : 0u;
-                if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)k) lo = mid;
-                else hi = mid;
-            }
-            if (lane == 0) sm.bucket = lo;
+            const uint32_t t_star = kth_largest_bound(v, (uint32_t)k);
+            if (lane == 0) sm.bucket = t_star;
         }
         __syncthreads();
         const uint32_t lo = sm.bucket;
         // this thread's qualifying keys go to one warp-aggregated slot range
+        // (keys past N are 0 and lo >= 1 unless every key is a candidate)
         uint32_t cnt = 0;
         if (in_regs) {
 #pragma unroll
@@ -984,8 +999,17 @@ select_kernel(const __grid_constant__ SelectParams p)
                 }
             }
         } else {
-            // the fallback starts from a zero histogram and empty lists
+            // the fallback starts from a zero histogram, empty lists and
+            // cleared outputs
             for (int b = tid; b < kHistBins; b += kSelectThreads) sm.hist[b] = 0;
+            for (int e = tid; e < KVI_MAX_K; e += kSelectThreads) {
+                sm.sure_key[e] = 0;
+                sm.sure_id[e] = -1;
+                sm.sure_len[e] = -1;
+                sm.out_key[e] = 0;
+                sm.out_id[e] = -1;
+                sm.out_len[e] = -1;
+            }
             if (tid == 0) sm.n_cand = 0;
         }
         __syncthreads();
@@ -1008,8 +1032,7 @@ select_kernel(const __grid_constant__ SelectParams p)
         if (!p.place && ok && sm.out_len[j] < 0) record_status(p.status, KVI_ERR_OUT_OF_RANGE);
     }
     if (p.place) {
-        if (tid < 32) place_request(p, sm, r, ok, st, start, tl);
-        else if (ok) fact_rows(p, sm, st, r, k);
+        place_parallel(p, sm, r, ok, st, start, tl);
         if (r == 0 && tid == 0) *p.work = 0ull;  // the inject kernel's work counter
     }
 }
@@ -1063,15 +1086,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_co
         uint32_t v[kSelectGroups / 32];
 #pragma unroll
         for (int i = 0; i < kSelectGroups / 32; ++i) v[i] = gmax[i * 32 + lane];
-        uint32_t a = 0, b = 1u << 16;  // t = 0 admits every fact
-        while (b - a > 1) {
-            const uint32_t mid = (a + b) >> 1;
-            uint32_t c = 0;
-#pragma unroll
-            for (int i = 0; i < kSelectGroups / 32; ++i) c += v[i] >= mid ? 1u : 0u;
-            if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)p.k) a = mid;
-            else b = mid;
-        }
+        const uint32_t a = kth_largest_bound(v, (uint32_t)p.k);  // t = 0 admits every fact
         if (lane == 0) t_star = a;
     }
     __syncthreads();
