@@ -139,6 +139,7 @@ struct CoarseParams {
     int32_t N, R, Rp, E;       // facts, queries, queries padded to 16, embedding dim
     int32_t stages, tmem_cols; // set by the launcher
     int32_t mt;                // accumulators (128-fact tiles) per CTA: 1 or 2
+    int32_t box_q;             // query rows per tensor copy (set by the launcher)
     int64_t stride;            // row stride of lo / hi
     float *lo, *hi;            // [R][stride]
     int32_t *status;

@@ -228,13 +228,16 @@ score_kernel(const __grid_constant__ ScoreParams p)
 // producer warp (all lanes issuing) streams the CTA's contiguous range of
 // fact rows into a ring
 // of shared-memory stages (one row per stage, 192 KB in all) with
-// cp.async.bulk, and twelve consumer warps take the rows round-robin, each
-// lane reading its float4 slots from shared memory and keeping four
-// independent Dot2 accumulators.  The extents of a warp's next 32 rows are
+// cp.async.bulk, and 24 consumer warps take the rows round-robin, each lane
+// reading its float4 slots from shared memory and keeping four independent
+// Dot2 accumulators.  The Dot2 arithmetic (about ten float32 operations per
+// element) is what limits the rate at which an SM retires rows, so the
+// consumers are as many warps as the registers allow (24 measured 1.2 us
+// faster than 12 on a 10k-fact store).  The extents of a warp's next 32 rows are
 // fetched together (one per lane), so validating them costs one round trip
 // per 32 rows.  The code is kept short: it is fetched cold on every launch.
 
-constexpr int kRingConsumers = 12;
+constexpr int kRingConsumers = 24;
 constexpr int kRingThreads = (kRingConsumers + 1) * 32;
 constexpr int kRingBytes = 192 * 1024;
 constexpr int kRingMaxStages = 96;

@@ -47,8 +47,11 @@ constexpr int kCoarseThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5
 constexpr int kStageBytesA = kTileM * kChunk * 4;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
-constexpr int kBoxRowsA = 32;  // fact rows per TMA box (4 boxes per stage)
-constexpr int kBoxRowsB = 16;  // query rows per TMA box (R padded to 16)
+// Rows per TMA box: a whole 128-fact accumulator tile per box (16 KB), and
+// up to 128 query rows per box.  Each tensor copy has a fixed cost in the
+// SM's copy unit, so fewer, larger boxes per stage move a stage sooner.
+constexpr int kBoxRowsA = 128;
+constexpr int kBoxRowsBMax = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct CoarseSmemTail {
@@ -172,11 +175,12 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     bool ok = true;
 
     if (warp == 0) {
-        // the stage is loaded as boxes of kBoxRowsA fact rows and kBoxRowsB
+        // the stage is loaded as boxes of kBoxRowsA fact rows and box_q
         // query rows, one box per lane (a single issuing thread caps the
         // copy rate far below the SM's share of HBM bandwidth)
         const uint32_t bytes = (uint32_t)(stage_a + stage_b);
-        const int na = MT * kTileM / kBoxRowsA, nb = p.Rp / kBoxRowsB;
+        const int bq = p.box_q;  // query rows per box
+        const int na = MT * kTileM / kBoxRowsA, nb = (p.Rp + bq - 1) / bq;
         int issued = 0;  // chunks whose copies went out
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % S;
@@ -199,8 +203,8 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                     tma_2d(saddr(a_st + (size_t)s * stage_a + (size_t)j * kBoxRowsA * 128), &tm_emb,
                            kc * kChunk, tile * MT * kTileM + j * kBoxRowsA, fb);
                 else
-                    tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * kBoxRowsB * 128), &tm_q,
-                           kc * kChunk, (j - na) * kBoxRowsB, fb);
+                    tma_2d(saddr(b_st + (size_t)s * stage_b + (size_t)(j - na) * bq * 128), &tm_q,
+                           kc * kChunk, (j - na) * bq, fb);
             }
             issued = kc + 1;
         }
@@ -397,7 +401,16 @@ cudaError_t launch_coarse(const CoarseParams &p0, const float *emb, int64_t n_fa
     CUtensorMap te, tq;
     cudaError_t e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, kBoxRowsA);
     if (e != cudaSuccess) return e;
-    e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, kBoxRowsB);
+    // query rows per box: 16 x the largest divisor d <= 8 of Rp / 16, so that
+    // the boxes tile the Rp padded rows of a stage exactly
+    {
+        const int m = p.Rp / 16;
+        int d = 1;
+        for (int c = 1; c * 16 <= kBoxRowsBMax; ++c)
+            if (m % c == 0) d = c;
+        p.box_q = 16 * d;
+    }
+    e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, (uint32_t)p.box_q);
     if (e != cudaSuccess) return e;
     const size_t smem = coarse_smem_bytes(p.Rp, p.mt);
     // the opt-in is made once per device, so it covers the largest ring any
