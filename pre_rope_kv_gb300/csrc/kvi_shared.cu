@@ -60,7 +60,7 @@ struct CoarseSmemTail {
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t pad;
-    float qn2[KVI_MAX_SHARED_QUERIES];
+    float qscale[KVI_MAX_SHARED_QUERIES];  // rel * |q_r| per query (see the epilogue)
 };
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -117,13 +117,18 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
-__device__ __forceinline__ float sq_row32(const float *row)
+// Sum of squares of one 128-byte row chunk.  Lane l starts at 16-byte column
+// l mod 8: the lanes of a warp read 32 different rows, whose same column
+// lies in the same four banks (rows are 128 bytes apart), so reading column
+// c in step c would be a 32-way bank conflict; rotated, each step touches
+// all eight columns and takes the minimum four shared-memory wavefronts.
+__device__ __forceinline__ float sq_row32(const float *row, int rot)
 {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < kChunk / 4; ++c) {
-        const float4 v = r4[c];
+        const float4 v = r4[(c + rot) & (kChunk / 4 - 1)];
         acc = fmaf(v.x, v.x, acc);
         acc = fmaf(v.y, v.y, acc);
         acc = fmaf(v.z, v.z, acc);
@@ -273,23 +278,26 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
             // a row's 128 bytes stay within its own 128-byte span under the
             // swizzle (only their 16-byte chunks are permuted), so a sum of
             // squares reads them in place
-            en2[0] += sq_row32(reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + L * 128));
+            en2[0] += sq_row32(reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + L * 128), lane);
             if (MT == 2)
                 en2[1] += sq_row32(
-                    reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + kStageBytesA + L * 128));
-            if (L < p.Rp) qa += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + L * 128));
+                    reinterpret_cast<const float *>(a_st + (size_t)s * stage_a + kStageBytesA + L * 128), lane);
+            if (L < p.Rp)
+                qa += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + L * 128), lane);
             if (L + 128 < p.Rp)
-                qb += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + (L + 128) * 128));
+                qb += sq_row32(reinterpret_cast<const float *>(b_st + (size_t)s * stage_b + (L + 128) * 128), lane);
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&tl.empty[s])) : "memory");
         }
-        if (L < p.Rp) tl.qn2[L] = qa;
-        if (L + 128 < p.Rp) tl.qn2[L + 128] = qb;
+        // the bound's per-query factor, once per query row instead of once
+        // per (fact, query) in the epilogue
+        const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
+        if (L < p.Rp) tl.qscale[L] = rel * sqrtf(qa);
+        if (L + 128 < p.Rp) tl.qscale[L + 128] = rel * sqrtf(qb);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const bool done = ok && wait_bar(saddr(&tl.mma_done), 0);
         if (__all_sync(0xffffffffu, done)) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
             for (int m = 0; m < MT; ++m) {
             const int64_t fact = ((int64_t)tile * MT + m) * kTileM + L;
             const float en = sqrtf(m == 0 ? en2[0] : en2[1]);
@@ -309,7 +317,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                         const int r = c0 + j;
                         if (r < p.R) {
                             const float c = __uint_as_float(v[j]);
-                            const float eps = __fmaf_ru(rel * sqrtf(tl.qn2[r]), en * 1.0001f, 7.9e-31f);
+                            const float eps = __fmaf_ru(tl.qscale[r], en * 1.0001f, 7.9e-31f);
                             p.lo[(int64_t)r * p.stride + fact] = __fsub_rd(c, eps);
                             p.hi[(int64_t)r * p.stride + fact] = __fadd_ru(c, eps);
                         }
