@@ -593,6 +593,19 @@ KVI_API kvi_status kvi_store_load(const char *path, void *kv, float *emb, int64_
 KVI_API kvi_status kvi_selftest_bounded_wait(uint64_t limit_ns, int32_t *d_status,
                                              int64_t *d_elapsed_ns, kvi_stream_t stream);
 
+/* Diagnostic: read `bytes` bytes at `src` with the SMs -- 16-byte loads from
+ * every thread of a grid of ctas_per_sm CTAs per SM, grid-stride, 8 loads in
+ * flight per thread -- and write one 64-bit checksum (the wrapping sum of
+ * the words read) to *d_sum.  `src` may be device memory or pinned host
+ * memory the device can address (cudaHostAlloc / cudaHostRegister): timed
+ * with events, it gives the rate at which the SMs read that memory, the
+ * ceiling of the inject kernel's host-resident pieces (KVI_STORE_KV_HOST),
+ * which are staged with the same 16-byte loads.  Asynchronous.  Errors:
+ * KVI_ERR_INVALID_ARG (NULL pointers, src not 16-byte aligned, bytes not a
+ * multiple of 16, ctas_per_sm outside [1, 8]), KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_selftest_stream_read(const void *src, size_t bytes, int32_t ctas_per_sm,
+                                            uint64_t *d_sum, kvi_stream_t stream);
+
 /* Tracing: when n_events == 3, the calling thread's next
  * kvi_retrieve_and_inject calls record events[0] before the first kernel,
  * events[1] once retrieval and placement are enqueued and events[2] after

@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "kvi_store_file_info_read", "kvi_store_load", "kvi_graph_build_workspace_bytes",
     "kvi_graph_build", "kvi_graph_search_workspace_bytes", "kvi_graph_search",
     "kvi_graph_retrieve_and_inject_workspace_bytes", "kvi_graph_retrieve_and_inject",
-    "kvi_selftest_bounded_wait",
+    "kvi_selftest_bounded_wait", "kvi_selftest_stream_read",
 )
 MAX_GRAPH_DEGREE = 128
 MAX_GRAPH_BEAM = 256
@@ -112,10 +112,16 @@ def load_library(path: str | None = None):
     global _lib
     if _lib is not None:
         return _lib
-    p = path or LIB_PATH
-    if not os.path.exists(p):
-        raise RuntimeError(f"libkvi is not built ({p} missing): run pre_rope_kv_gb300.build.build()")
-    lib = ctypes.CDLL(p)
+    _lib = open_library(path or LIB_PATH)
+    return _lib
+
+
+def open_library(path: str):
+    """Load and configure the library at `path` without making it the one
+    the functions of this module call (see use_library)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvi is not built ({path} missing): run pre_rope_kv_gb300.build.build()")
+    lib = ctypes.CDLL(path)
     P, i32, i64, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
                            ctypes.c_size_t)
     S = ctypes.c_int
@@ -165,6 +171,7 @@ def load_library(path: str | None = None):
                                               ctypes.POINTER(PagedCache), ctypes.POINTER(Rope), P, P,
                                               P, P, sz, P, P]),
         "kvi_selftest_bounded_wait": (S, [ctypes.c_uint64, P, P, P]),
+        "kvi_selftest_stream_read": (S, [P, sz, i32, P, P]),
         "kvi_status_str": (ctypes.c_char_p, [S]),
         "kvi_last_error": (ctypes.c_char_p, []),
     }
@@ -172,8 +179,47 @@ def load_library(path: str | None = None):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    if hasattr(lib, "kvi_debug_stall_scorer_row"):  # debug build only
+        lib.kvi_debug_stall_scorer_row.restype = S
+        lib.kvi_debug_stall_scorer_row.argtypes = [i64]
     return lib
+
+
+class use_library:
+    """Context manager: the functions of this module call `lib` (from
+    open_library, e.g. the debug build) inside the block."""
+
+    def __init__(self, lib):
+        self.lib = lib
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        self.saved = _lib
+        _lib = self.lib
+        return self.lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def kvi_selftest_stream_read(src_ptr: int, nbytes: int, ctas_per_sm: int, sum_out, stream=None) -> None:
+    """Diagnostic: the SMs read nbytes at src_ptr (device or pinned host
+    memory); one checksum goes to sum_out (a device uint64 tensor)."""
+    _check(load_library().kvi_selftest_stream_read(int(src_ptr), int(nbytes), int(ctas_per_sm),
+                                                   _ptr(sum_out), _stream(stream)),
+           "kvi_selftest_stream_read")
+
+
+def kvi_debug_stall_scorer_row(row: int) -> None:
+    """Debug build only (include/kvi_debug.h): make the scoring kernel skip
+    the copy of one flat row, so that a bounded wait runs out."""
+    lib = load_library()
+    if not hasattr(lib, "kvi_debug_stall_scorer_row"):
+        raise RuntimeError("kvi_debug_stall_scorer_row needs the debug build (build(debug=True))")
+    _check(lib.kvi_debug_stall_scorer_row(int(row)), "kvi_debug_stall_scorer_row")
 
 
 def _check(status: int, where: str):

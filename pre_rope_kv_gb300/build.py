@@ -4,6 +4,10 @@ Each translation unit is compiled in parallel with nvcc for
 ``arch=compute_103a,code=sm_103a`` only, then linked into one shared library
 with the CUDA runtime linked statically.  Nothing is installed: the library
 stays in the source tree, next to the binding that loads it.
+
+``build(debug=True)`` compiles the same sources with ``-DKVI_DEBUG_CHECKS``
+into ``_build/libkvi_debug.so``: the checks and the failure hook that
+``include/kvi_debug.h`` describes.  Only the tests use it.
 """
 from __future__ import annotations
 
@@ -18,11 +22,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkvi.so")
+DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libkvi_debug.so")
 SOURCES = ["kvi_host.cu", "kvi_retrieve.cu", "kvi_inject.cu", "kvi_noalloc.cu", "kvi_shared.cu",
            "kvi_store_io.cu", "kvi_graph.cu", "kvi_selftest.cu"]
 HEADERS = [os.path.join(CSRC, "kvi_internal.cuh"), os.path.join(CSRC, "kvi_dot2.cuh"),
            os.path.join(CSRC, "kvi_sync.cuh"),
-           os.path.join(INCLUDE, "kvi.h")]
+           os.path.join(INCLUDE, "kvi.h"), os.path.join(INCLUDE, "kvi_debug.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,28 +38,33 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkvi")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Build libkvi.so if it is missing or older than its sources."""
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Build libkvi.so (or, with debug, libkvi_debug.so) if it is missing or
+    older than its sources."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and not _stale(lib_path):
+        return lib_path
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()
     common = ["-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
+    if debug:
+        common += ["-DKVI_DEBUG_CHECKS"]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", f".{os.getpid()}.o"))
+        obj = os.path.join(OUT_DIR, src.replace(".cu", f"{'.dbg' if debug else ''}.{os.getpid()}.o"))
         objs.append(obj)
         cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -70,16 +80,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     for o in objs:
         os.remove(o)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

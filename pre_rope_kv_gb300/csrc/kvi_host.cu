@@ -644,6 +644,9 @@ kvi_status kvi_inject_paged_ex(const kvi_store_view *store, const int32_t *d_fac
     ip.pairing = rope->pairing;
     ip.status = d_status;
     for (int l = 0; l < ip.L; ++l) ip.layer_base[l] = cache->layer_base[l];
+#ifdef KVI_DEBUG_CHECKS
+    if (d_status) KVI_CUDA(launch_overlap_check(ip, s));
+#endif
     KVI_CUDA(launch_inject(ip, s, false));
     return KVI_OK;
 }
@@ -1360,6 +1363,17 @@ kvi_status kvi_selftest_bounded_wait(uint64_t limit_ns, int32_t *d_status, int64
     if (limit_ns < 1000 || limit_ns > 1000000000ull)
         return fail(KVI_ERR_INVALID_ARG, "limit_ns=%llu outside [1e3, 1e9]", (unsigned long long)limit_ns);
     KVI_CUDA(launch_bounded_wait(limit_ns, d_status, d_elapsed_ns, reinterpret_cast<cudaStream_t>(stream)));
+    return KVI_OK;
+}
+
+kvi_status kvi_selftest_stream_read(const void *src, size_t bytes, int32_t ctas_per_sm, uint64_t *d_sum,
+                                    kvi_stream_t stream)
+{
+    if (!src || !d_sum || !aligned(src, 16) || bytes % 16 || !aligned(d_sum, 8))
+        return fail(KVI_ERR_INVALID_ARG, "src (16-byte aligned), bytes (multiple of 16) and sum are required");
+    if (ctas_per_sm < 1 || ctas_per_sm > 8)
+        return fail(KVI_ERR_INVALID_ARG, "ctas_per_sm=%d outside [1, 8]", ctas_per_sm);
+    KVI_CUDA(launch_stream_read(src, bytes, ctas_per_sm, d_sum, reinterpret_cast<cudaStream_t>(stream)));
     return KVI_OK;
 }
 

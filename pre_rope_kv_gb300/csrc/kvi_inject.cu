@@ -709,7 +709,48 @@ inject_kernel(const __grid_constant__ InjectParams p)
     }
 }
 
+#ifdef KVI_DEBUG_CHECKS
+// Debug builds: do two of the split call's facts target overlapping
+// positions?  Fact j covers [pos[j], pos[j] + fact_len[ids[j]]) (facts with
+// an invalid id or length are reported by the inject kernel itself); each
+// thread compares its fact with every later one.
+__global__ void __launch_bounds__(256) overlap_check_kernel(const __grid_constant__ InjectParams p)
+{
+    const kvi_store_view &st = p.store.single;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    auto extent = [&](int j, int64_t &a, int64_t &b) {
+        const int32_t f = p.ids[j];
+        a = b = 0;
+        if (f < 0 || (int64_t)f >= st.n_facts) return;
+        const int32_t len = st.fact_len[f];
+        if (len <= 0) return;
+        a = p.pos[j];
+        b = a + len;
+    };
+    int64_t a0, b0;
+    extent(i, a0, b0);
+    if (b0 <= a0) return;
+    for (int j = i + 1; j < p.n; ++j) {
+        int64_t a1, b1;
+        extent(j, a1, b1);
+        if (b1 > a1 && a0 < b1 && a1 < b0) {
+            record_status(p.status, KVI_ERR_INVALID_ARG);
+            return;
+        }
+    }
+}
+#endif
+
 }  // namespace
+
+#ifdef KVI_DEBUG_CHECKS
+cudaError_t launch_overlap_check(const InjectParams &p, cudaStream_t s)
+{
+    overlap_check_kernel<<<(unsigned)((p.n + 255) / 256), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+#endif
 
 cudaError_t prepare_inject_kernel() { return smem_opt_in(inject_kernel, (int)sizeof(InjSmem)); }
 

@@ -209,6 +209,8 @@ cudaError_t launch_graph_search(const GraphSearchParams &p, cudaStream_t s);
 
 // Diagnostic: a wait on a barrier nothing completes, bounded by limit_ns.
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, int64_t *elapsed_ns, cudaStream_t s);
+// Diagnostic: the SMs read `bytes` at src (device or mapped host memory).
+cudaError_t launch_stream_read(const void *src, size_t bytes, int ctas_per_sm, uint64_t *sum, cudaStream_t s);
 
 // One-time per-device kernel attributes (shared-memory opt-in), made ahead
 // of a stream capture.
@@ -223,6 +225,11 @@ cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
 cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl);
 cudaError_t launch_place(const PlaceParams &p, cudaStream_t s);
 cudaError_t launch_inject(const InjectParams &p, cudaStream_t s, bool pdl);
+#ifdef KVI_DEBUG_CHECKS
+// Debug builds: record KVI_ERR_INVALID_ARG when two facts of a split inject
+// call target overlapping positions.
+cudaError_t launch_overlap_check(const InjectParams &p, cudaStream_t s);
+#endif
 
 // Record a message for kvi_last_error() on this thread and return `s`.
 kvi_status set_error(kvi_status s, const char *msg);

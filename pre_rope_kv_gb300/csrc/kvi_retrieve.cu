@@ -293,6 +293,12 @@ struct RowCursor {
     }
 };
 
+#ifdef KVI_DEBUG_CHECKS
+// Debug builds: flat row whose copy the scoring kernel skips (negative: none),
+// set by kvi_debug_stall_scorer_row to make a bounded wait run out.
+__device__ long long g_debug_stall_row = -1;
+#endif
+
 struct StoreCache {
     int32_t r;
     bool ok;
@@ -354,8 +360,16 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
                 } else {
                     sc.get(p, cur.r);
                     const uint32_t fb = smem_addr(&sm.full[s]);
-                    sm.issued[s] = (int32_t)round;
-                    if (sc.live(cur.i)) {
+#ifdef KVI_DEBUG_CHECKS
+                    // no copy and no arrival for this row: its consumer's
+                    // wait runs out
+                    const bool stall = g0 + j == g_debug_stall_row;
+#else
+                    constexpr bool stall = false;
+#endif
+                    if (stall) {
+                    } else if (sc.live(cur.i)) {
+                        sm.issued[s] = (int32_t)round;
                         if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
                                      "r"(row_bytes)
@@ -366,6 +380,7 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
                             "l"(sc.st.emb + cur.i * E), "r"(row_bytes), "r"(fb)
                             : "memory");
                     } else {
+                        sm.issued[s] = (int32_t)round;
                         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
                     }
                 }
@@ -415,6 +430,14 @@ score_ring_kernel(const __grid_constant__ ScoreParams p)
         const bool ok = ring_wait(smem_addr(&sm.full[s]), round & 1u);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
+            // the rows this warp will not score keep stale keys and lengths
+            // in the workspace: mark their lengths invalid, so that a fused
+            // call injects nothing from them (placement reports them)
+            for (int64_t jj = j + (int64_t)lane * kRingConsumers; jj < n; jj += 32 * (int64_t)kRingConsumers) {
+                RowCursor c;
+                c.init(g0 + jj, p.max_facts);
+                p.lens[(int64_t)c.r * p.key_stride + c.i] = -1;
+            }
             return;
         }
         sc.get(p, cur.r);
@@ -1295,3 +1318,15 @@ cudaError_t launch_place(const PlaceParams &p, cudaStream_t s)
 }
 
 }  // namespace kvi
+
+#ifdef KVI_DEBUG_CHECKS
+#include "kvi_debug.h"
+
+extern "C" kvi_status kvi_debug_stall_scorer_row(int64_t row)
+{
+    const long long v = row < 0 ? -1 : (long long)row;
+    const cudaError_t e = cudaMemcpyToSymbol(kvi::g_debug_stall_row, &v, sizeof v);
+    if (e != cudaSuccess) return kvi::set_error(KVI_ERR_CUDA, cudaGetErrorString(e));
+    return KVI_OK;
+}
+#endif

@@ -302,3 +302,35 @@ def test_rope_spec_validation():
     spec.scaling = 3
     with pytest.raises(kvi.KviError):
         kvi.kvi_prepare_rope_ex(spec, 64, 128)
+
+
+def _declared_in(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    return sorted(set(re.findall(r"KVI_API\s+[\w\s\*]+?\b(kvi_\w+)\s*\(", src)))
+
+
+def test_debug_build_exports_the_debug_hooks_too():
+    # build(debug=True): the same library with -DKVI_DEBUG_CHECKS, which adds
+    # exactly the symbols of include/kvi_debug.h; the release build has none
+    import subprocess
+    path = kbuild.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == set(_declared_in("kvi.h")) | set(_declared_in("kvi_debug.h"))
+    assert _declared_in("kvi_debug.h") == ["kvi_debug_stall_scorer_row"]
+    raw = ctypes.CDLL(kvi.LIB_PATH)
+    assert not hasattr(raw, "kvi_debug_stall_scorer_row")
+    # the release binding refuses the hook instead of calling a missing symbol
+    with pytest.raises(RuntimeError, match="debug build"):
+        kvi.kvi_debug_stall_scorer_row(0)
+
+
+def test_stream_read_validation(lib):
+    t = _FakeTensor()
+    f = lib.kvi_selftest_stream_read
+    assert f(None, 16, 1, t.data_ptr(), None) == kvi.ERR_INVALID_ARG
+    assert f(0x10008, 16, 1, t.data_ptr(), None) == kvi.ERR_INVALID_ARG   # misaligned
+    assert f(0x10000, 24, 1, t.data_ptr(), None) == kvi.ERR_INVALID_ARG   # not 16-byte words
+    assert f(0x10000, 16, 0, t.data_ptr(), None) == kvi.ERR_INVALID_ARG
+    assert f(0x10000, 16, 9, t.data_ptr(), None) == kvi.ERR_INVALID_ARG
+    assert f(0x10000, 16, 1, None, None) == kvi.ERR_INVALID_ARG

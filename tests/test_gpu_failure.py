@@ -50,3 +50,18 @@ def test_a_wait_that_never_completes_times_out_and_the_context_stays_usable(limi
     assert int(st.item()) == 0
     want = oracle.topk(oracle.scores(b.queries_np[0], b.stores[0].emb_np), 10)
     assert np.array_equal(ids.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("where", ["device", "pinned_host"])
+def test_stream_read_diagnostic_reads_every_word(where):
+    # the read diagnostic the bench uses for the host link's ceiling: its
+    # checksum is the wrapping sum of the 32-bit words read
+    n = (64 << 20) + 48  # not a multiple of the grid's stride
+    g = torch.Generator().manual_seed(5)
+    words = torch.randint(0, 2 ** 31 - 1, (n // 4,), generator=g, dtype=torch.int64).to(torch.int32)
+    buf = words.cuda() if where == "device" else words.pin_memory()
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    kvi.kvi_selftest_stream_read(buf.data_ptr(), n, 2, out)
+    torch.cuda.synchronize()
+    want = int(words.numpy().astype(np.uint32).astype(np.uint64).sum(dtype=np.uint64))
+    assert int(out.item()) & (2 ** 64 - 1) == want & (2 ** 64 - 1)
