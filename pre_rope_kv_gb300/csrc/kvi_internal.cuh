@@ -96,6 +96,7 @@ struct SelectParams {
     int64_t *rows;              // [R][k] first store row of each selected fact
     unsigned long long *work;   // inject work counter, zeroed here
     int32_t *status;
+    int32_t smem_keys;          // set by the launcher: keys the CTA may stage in shared memory
 };
 
 struct PlaceParams {

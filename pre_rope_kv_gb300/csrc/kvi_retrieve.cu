@@ -740,7 +740,14 @@ __device__ __noinline__ void select_by_histogram(SelectSmem &sm, const uint64_t 
     __syncthreads();
 }
 
+// Keys a selecting CTA can keep (16 bits each) in shared memory past
+// SelectSmem: stores of up to this many facts (or candidates) are read from
+// L2 once.
+constexpr int64_t kSmemKeysMax = 65536;
+static_assert(sizeof(SelectSmem) + 2 * kSmemKeysMax <= 227 * 1024, "select smem");
+
 constexpr int kWarmFacts = 8;
+constexpr int kStreamUnroll = 8;  // key loads in flight per thread when staging to shared memory
 constexpr int kSelectGroups = 256;
 
 // t* = the largest t such that at least k of the 256 values v (8 per lane of
@@ -916,6 +923,12 @@ select_kernel(const __grid_constant__ SelectParams p)
     // once, in one round trip, and kept in registers; larger stores stream
     // them from L2
     const bool in_regs = N <= (int64_t)kSelectThreads * kKeysPerThread;
+    // larger stores, up to the launcher's allowance: one pass keeps each
+    // key's top 16 bits in shared memory, so that the threshold and the
+    // candidates need no second read of the keys from L2 (candidates fetch
+    // their full key and length)
+    const bool in_smem = !in_regs && N <= (int64_t)p.smem_keys;
+    uint16_t *hs = reinterpret_cast<uint16_t *>(smem_raw + sizeof(SelectSmem));
     uint64_t kr[kKeysPerThread];
     int32_t lr[kKeysPerThread];
     if (in_regs) {
@@ -943,6 +956,25 @@ select_kernel(const __grid_constant__ SelectParams p)
         if (in_regs) {
 #pragma unroll
             for (int m = 0; m < kKeysPerThread; ++m) mt = max(mt, (uint32_t)(kr[m] >> 48));
+        } else if (in_smem) {
+            // kStreamUnroll loads in flight per thread
+            for (int64_t i0 = tid; i0 < N; i0 += (int64_t)kStreamUnroll * kSelectThreads) {
+                uint64_t v[kStreamUnroll];
+#pragma unroll
+                for (int u = 0; u < kStreamUnroll; ++u) {
+                    const int64_t i = i0 + (int64_t)u * kSelectThreads;
+                    v[u] = i < N ? __ldcg(keys + i) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kStreamUnroll; ++u) {
+                    const int64_t i = i0 + (int64_t)u * kSelectThreads;
+                    if (i < N) {
+                        const uint32_t h = (uint32_t)(v[u] >> 48);
+                        hs[i] = (uint16_t)h;
+                        mt = max(mt, h);
+                    }
+                }
+            }
         } else {
             for (int64_t i = tid; i < N; i += kSelectThreads) mt = max(mt, (uint32_t)(__ldcg(keys + i) >> 48));
         }
@@ -969,6 +1001,8 @@ select_kernel(const __grid_constant__ SelectParams p)
 #pragma unroll
             for (int m = 0; m < kKeysPerThread; ++m)
                 cnt += (tid + (int64_t)m * kSelectThreads < N && (uint32_t)(kr[m] >> 48) >= lo) ? 1u : 0u;
+        } else if (in_smem) {
+            for (int64_t i = tid; i < N; i += kSelectThreads) cnt += (uint32_t)hs[i] >= lo ? 1u : 0u;
         } else {
             for (int64_t i = tid; i < N; i += kSelectThreads)
                 cnt += ((uint32_t)(__ldcg(keys + i) >> 48) >= lo) ? 1u : 0u;
@@ -992,6 +1026,17 @@ select_kernel(const __grid_constant__ SelectParams p)
                             sm.cand_key[at] = kr[m];
                             sm.cand_id[at] = (int32_t)i;
                             sm.cand_len[at] = lr[m];
+                        }
+                        ++at;
+                    }
+                }
+            } else if (in_smem) {
+                for (int64_t i = tid; i < N; i += kSelectThreads) {
+                    if ((uint32_t)hs[i] >= lo) {
+                        if (at < (uint32_t)kCandCap) {
+                            sm.cand_key[at] = __ldcg(keys + i);
+                            sm.cand_id[at] = (int32_t)i;
+                            sm.cand_len[at] = __ldcg(lens + i);
                         }
                         ++at;
                     }
@@ -1275,14 +1320,18 @@ cudaError_t prepare_retrieval_kernels()
 {
     cudaError_t e = smem_opt_in(score_ring_kernel, (int)sizeof(ScoreRingSmem));
     if (e != cudaSuccess) return e;
-    return smem_opt_in(select_kernel, (int)sizeof(SelectSmem));
+    return smem_opt_in(select_kernel, (int)(sizeof(SelectSmem) + 2 * kSmemKeysMax));
 }
 
-cudaError_t launch_select(const SelectParams &p, cudaStream_t s, bool pdl)
+cudaError_t launch_select(const SelectParams &p0, cudaStream_t s, bool pdl)
 {
-    static_assert(sizeof(SelectSmem) <= 227 * 1024, "select smem");
-    const int smem = (int)sizeof(SelectSmem);
-    cudaError_t e = smem_opt_in(select_kernel, smem);
+    SelectParams p = p0;
+    // the row space of a request: its keys' stride (facts, or candidate
+    // slots of the shared-store path)
+    const int64_t rows = p.key_stride;
+    p.smem_keys = (rows > (int64_t)kSelectThreads * kKeysPerThread && rows <= kSmemKeysMax) ? (int32_t)rows : 0;
+    const int smem = (int)(sizeof(SelectSmem) + (((size_t)p.smem_keys * 2 + 15) & ~(size_t)15));
+    cudaError_t e = smem_opt_in(select_kernel, (int)(sizeof(SelectSmem) + 2 * kSmemKeysMax));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.R);
