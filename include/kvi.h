@@ -79,7 +79,7 @@ typedef enum {
     KVI_ERR_IO = 6            /* a store file could not be written or read, or is not a valid one */
 } kvi_status;
 
-/* Limits of this build. */
+/* Compile-time limits of the library. */
 #define KVI_MAX_LAYERS 128        /* L */
 #define KVI_MAX_K 256             /* facts retrieved per request */
 #define KVI_MAX_INJECT_FACTS 4096 /* facts per kvi_inject_paged call */

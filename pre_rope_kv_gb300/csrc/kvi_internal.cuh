@@ -238,7 +238,7 @@ kvi_status set_error(kvi_status s, const char *msg);
 kvi_status check_retrieval_store(const kvi_store_view *s);
 // The checks of a store used for retrieval and injection (emb, kv, extents).
 kvi_status check_full_store(const kvi_store_view *s);
-// The geometry limits of this build (records a message on failure).
+// The library's compile-time geometry limits (records a message on failure).
 kvi_status check_store_geometry(const kvi_geometry *g);
 
 // Device facts cached per device (SM count).

@@ -170,7 +170,7 @@ kvi_status read_header(FILE *f, const char *path, Header *out)
     o.n = get<int64_t>(h, 32);
     o.t = get<int64_t>(h, 40);
     if (check_store_geometry(&o.g) != KVI_OK)
-        return io_fail(KVI_ERR_IO, std::string(path) + ": geometry outside this build's limits");
+        return io_fail(KVI_ERR_IO, std::string(path) + ": geometry outside the library's compile-time limits");
     if (o.n < 1 || o.n > 0x7fffffff || o.t < 0 || o.t > (int64_t(1) << 40))
         return io_fail(KVI_ERR_IO, std::string(path) + ": fact or token count out of range");
     o.lay = layout_of(o.g, o.n, o.t);
