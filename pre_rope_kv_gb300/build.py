@@ -79,6 +79,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
         if pr.returncode:
             failed.append(src)
     if failed:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
         raise RuntimeError(f"nvcc failed for {failed}")
     tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
