@@ -141,6 +141,8 @@ struct CoarseParams {
     int32_t stages, tmem_cols; // set by the launcher
     int32_t mt;                // accumulators (128-fact tiles) per CTA: 1 or 2
     int32_t box_q;             // query rows per tensor copy (set by the launcher)
+    int32_t F;                 // split form: facts per tile (the MMA's N), a multiple of 16, <= 256
+    int32_t split;             // split form: CTAs (one cluster) sharing a tile, each a K range
     int64_t stride;            // row stride of lo / hi
     float *lo, *hi;            // [R][stride]
     int32_t *status;
