@@ -937,7 +937,7 @@ kvi_status shared_retrieve(const kvi_store_view *store, bool inject, int32_t R, 
     cd.k = k;
     cd.cand = reinterpret_cast<int32_t *>(ws + L.cand);
     cd.cand_n = reinterpret_cast<int32_t *>(ws + L.cand_n);
-    KVI_CUDA(launch_candidates(cd, s));
+    KVI_CUDA(launch_candidates(cd, s, true));
     RescoreParams rp{};
     rp.store = *store;
     rp.queries = d_queries;
@@ -947,7 +947,7 @@ kvi_status shared_retrieve(const kvi_store_view *store, bool inject, int32_t R, 
     rp.cand_n = cd.cand_n;
     rp.keys = reinterpret_cast<uint64_t *>(ws + L.w.keys);
     rp.lens = reinterpret_cast<int32_t *>(ws + L.w.lens);
-    KVI_CUDA(launch_rescore(rp, s));
+    KVI_CUDA(launch_rescore(rp, s, true));
     return KVI_OK;
 }
 
@@ -987,7 +987,7 @@ kvi_status kvi_retrieve_topk_shared(const kvi_store_view *store, int32_t R, cons
     SelectParams lp = shared_select_params(store, R, k, L, static_cast<char *>(d_ws), d_ids, d_scores);
     lp.place = 0;
     lp.status = d_status;
-    KVI_CUDA(launch_select(lp, s, false));
+    KVI_CUDA(launch_select(lp, s, true));
     return KVI_OK;
 }
 
@@ -1037,7 +1037,7 @@ kvi_status kvi_retrieve_and_inject_shared(const kvi_store_view *store, int32_t R
     lp.rows = reinterpret_cast<int64_t *>(ws + L.w.rows);
     lp.work = reinterpret_cast<unsigned long long *>(ws + L.w.work);
     lp.status = d_status;
-    KVI_CUDA(launch_select(lp, s, false));
+    KVI_CUDA(launch_select(lp, s, true));
     if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
 
     InjectParams ip{};
@@ -1210,7 +1210,7 @@ kvi_status kvi_graph_build(const kvi_store_view *store, int32_t degree, int32_t 
         SelectParams lp = shared_select_params(store, R, k, L, ws, ids, scores);
         lp.place = 0;
         lp.status = d_status;
-        KVI_CUDA(launch_select(lp, s, false));
+        KVI_CUDA(launch_select(lp, s, true));
         GraphRowsParams gp{ids, i0, R, degree, d_graph};
         KVI_CUDA(launch_graph_rows(gp, s));
     }
@@ -1317,7 +1317,7 @@ kvi_status kvi_graph_retrieve_and_inject(const kvi_store_view *store, const int3
     lp.rows = reinterpret_cast<int64_t *>(ws + L.w.rows);
     lp.work = reinterpret_cast<unsigned long long *>(ws + L.w.work);
     lp.status = d_status;
-    KVI_CUDA(launch_select(lp, s, false));
+    KVI_CUDA(launch_select(lp, s, true));
     if (trace) KVI_CUDA(cudaEventRecord(t_trace[1], s));
 
     InjectParams ip{};

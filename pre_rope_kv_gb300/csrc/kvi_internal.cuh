@@ -158,7 +158,7 @@ struct CandParams {
     int32_t N, R, k;
     int32_t *cand, *cand_n;
 };
-cudaError_t launch_candidates(const CandParams &p, cudaStream_t s);
+cudaError_t launch_candidates(const CandParams &p, cudaStream_t s, bool pdl);
 
 struct RescoreParams {
     kvi_store_view store;
@@ -169,7 +169,7 @@ struct RescoreParams {
     uint64_t *keys;
     int32_t *lens;
 };
-cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s);
+cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s, bool pdl);
 
 // Graph index: the neighbour rows of a build batch (a row's top degree + 1
 // ids without the row's own fact) and the beam search, one CTA per query.

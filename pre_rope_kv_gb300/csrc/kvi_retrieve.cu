@@ -1130,6 +1130,8 @@ __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_co
     constexpr int kWarps = kSelectThreads / 32;
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();  // the intervals of the coarse kernel
+    pdl_launch_dependents();
     const float *lo = p.lo + (int64_t)r * p.stride;
     const float *hi = p.hi + (int64_t)r * p.stride;
     const int64_t N = p.N;
@@ -1215,6 +1217,8 @@ __global__ void __launch_bounds__(kRescoreWarps * 32) rescore_kernel(const __gri
     const int r = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int E = p.store.g.embed_dim;
+    pdl_wait();  // the candidates
+    pdl_launch_dependents();
     const int32_t n = p.cand_n[r];
     const float4 *q4 = reinterpret_cast<const float4 *>(p.queries + (int64_t)r * E);
     for (int64_t j = (int64_t)blockIdx.x * kRescoreWarps + (threadIdx.x >> 5); j < n;
@@ -1348,16 +1352,38 @@ cudaError_t launch_select(const SelectParams &p0, cudaStream_t s, bool pdl)
     return cudaGetLastError();
 }
 
-cudaError_t launch_candidates(const CandParams &p, cudaStream_t s)
+namespace {
+
+// A launch that may begin while the previous kernel of the stream runs (it
+// waits for that kernel's memory itself).
+template <typename P>
+cudaError_t launch_pdl(void (*kernel)(P), const P &p, dim3 grid, dim3 block, cudaStream_t s, bool pdl)
 {
-    cand_kernel<<<p.R, kSelectThreads, 0, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s)
+}  // namespace
+
+cudaError_t launch_candidates(const CandParams &p, cudaStream_t s, bool pdl)
 {
-    rescore_kernel<<<dim3(kRescoreBlocksPerQuery, p.R), kRescoreWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(cand_kernel, p, dim3((unsigned)p.R), dim3(kSelectThreads), s, pdl);
+}
+
+cudaError_t launch_rescore(const RescoreParams &p, cudaStream_t s, bool pdl)
+{
+    return launch_pdl(rescore_kernel, p, dim3(kRescoreBlocksPerQuery, (unsigned)p.R), dim3(kRescoreWarps * 32), s,
+                      pdl);
 }
 
 cudaError_t launch_place(const PlaceParams &p, cudaStream_t s)

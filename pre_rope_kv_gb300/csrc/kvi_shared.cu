@@ -183,6 +183,7 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tl.tmem_base;
+    pdl_launch_dependents();  // the candidate kernel may be scheduled; it waits for this grid's end
     const int cols_acc = p.tmem_cols / MT;  // tensor-memory columns per accumulator
     bool ok = true;
 
@@ -508,6 +509,7 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tl.tmem_base;
+    pdl_launch_dependents();  // the candidate kernel may be scheduled; it waits for this grid's end
     bool ok = true, acc_ready = false;
     const int L = 32 * (warp & 3) + lane;  // warps 2-5: tensor-memory lane = query row
 
