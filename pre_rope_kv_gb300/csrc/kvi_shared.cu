@@ -382,13 +382,16 @@ constexpr int kQTile = 128;               // MMA M: query rows (at most 128 of t
 constexpr int kSlotQ = kQTile * kChunk * 4;
 constexpr int kMaxF = 256;                // MMA N: facts per tile
 constexpr int kMaxSplit = 4;
+// warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 norms; after the K loop all eight
+// warps take part, two per tensor-memory subpartition
+constexpr int kSplitThreads = 256;
 
 struct SplitSmemTail {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t mma_done;
     uint32_t tmem_base;
-    uint32_t pad;
+    uint32_t acc_ok;       // the MMA thread saw every MMA complete
     float en2[kMaxF];      // this CTA's squared fact norms over its K range
     float qa2[kQTile];     // and squared query norms
     float fnorm[kMaxF];    // |e| per fact of the tile (all K)
@@ -405,10 +408,10 @@ __host__ __device__ constexpr size_t split_part_bytes(int Rp, int F, int P)
 {
     return (((size_t)split_groups_owned(F, P) * 32 * Rp + kMaxF + kQTile) * 4 + 15) & ~(size_t)15;
 }
-// After the parts, each epilogue warp's output staging: a lo and a hi box of
+// After the parts, each warp's output staging: a lo and a hi box of
 // 32 x 32 floats, 1024-byte aligned for the 128-byte swizzle
 constexpr int kOutBoxBytes = 32 * 32 * 4;
-constexpr size_t kOutStageBytes = 4 * 2 * kOutBoxBytes;
+constexpr size_t kOutStageBytes = 8 * 2 * kOutBoxBytes;
 __host__ __device__ constexpr size_t split_out_offset(int P, size_t part)
 {
     return ((size_t)(P - 1) * part + 1023) & ~(size_t)1023;
@@ -472,7 +475,7 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kCoarseThreads, 1)
+__global__ void __launch_bounds__(kSplitThreads, 1)
 coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_lo, const __grid_constant__ CUtensorMap tm_hi,
                     const __grid_constant__ CoarseParams p)
@@ -510,8 +513,8 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tl.tmem_base;
     pdl_launch_dependents();  // the candidate kernel may be scheduled; it waits for this grid's end
-    bool ok = true, acc_ready = false;
-    const int L = 32 * (warp & 3) + lane;  // warps 2-5: tensor-memory lane = query row
+    bool ok = true;
+    const int L = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = query row
 
     if (warp == 0) {
         // per chunk: the query rows as boxes of box_q rows (they tile Rp
@@ -587,9 +590,11 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                              saddr(&tl.mma_done))
                          : "memory");
-            if (!wait_bar(saddr(&tl.mma_done), 0)) record_status(p.status, KVI_ERR_TIMEOUT);
+            const bool done = ok && wait_bar(saddr(&tl.mma_done), 0);
+            if (!done) record_status(p.status, KVI_ERR_TIMEOUT);
+            tl.acc_ok = done ? 1u : 0u;
         }
-    } else {
+    } else if (warp < 6) {
         // warps 2-5: squared norms of fact rows L and L + 128 and of query
         // row L over this CTA's chunks, read from the same stages
         float ea = 0.f, eb = 0.f, qa = 0.f;
@@ -617,43 +622,50 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
         tl.en2[L] = ea;
         tl.en2[L + 128] = eb;
         tl.qa2[L] = qa;
-        acc_ready = __all_sync(0xffffffffu, ok && wait_bar(saddr(&tl.mma_done), 0));
-        if (!acc_ready && lane == 0) record_status(p.status, KVI_ERR_TIMEOUT);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     }
 
-    const bool epi = warp >= 2;
     const int G = F / 32;                      // 32-column groups of the tile
     const int gown = split_groups_owned(F, P);  // most groups one CTA finalizes
     const size_t part = split_part_bytes(p.Rp, F, P);
     const uint32_t ring = saddr(base);
-    // this warp's tensor-memory lanes hold query rows 32 (warp % 4) .. + 31
-    const int row0 = 32 * (warp & 3);
-    const bool rows_here = epi && row0 < p.R;
+    // from here every warp takes part: its tensor-memory lanes hold query
+    // rows 32 (warp % 4) .. + 31, and the two warps of a subpartition take
+    // alternate column groups (half = warp / 4)
+    const int row0 = 32 * (warp & 3), half = warp >> 2;
+    const bool rows_here = row0 < p.R;
+    const bool norm_warp = warp >= 2 && warp < 6;
     const uint32_t tm_rows = tmem + ((uint32_t)row0 << 16);
-    if (P > 1) {
+    if (P > 1)
         cluster_sync_all();  // every CTA's MMAs are done and every ring is idle
-        if (epi) {
-            // partials of the groups that other CTAs finalize, into their
-            // rings; lanes are consecutive rows, so each store is 128 bytes
-            if (rows_here && acc_ready) {
-                for (int g = 0; g < G; ++g) {
-                    const int o = g % P;
-                    if (o == rank) continue;
-                    const int sidx = rank < o ? rank : rank - 1;  // this CTA among o's senders
-                    const uint32_t dst =
-                        cluster_addr(ring, (uint32_t)o) + (uint32_t)(sidx * part) + (uint32_t)((g / P) * 32 * p.Rp * 4);
-                    __syncwarp();
-                    uint32_t v[32];
-                    tmem_ld32(tm_rows + (uint32_t)(32 * g), v);
-                    if (L < p.R) {
+    else
+        __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // (after a timeout the status word is set and no interval is written)
+    const bool acc_ok = tl.acc_ok != 0;
+    if (P > 1) {
+        // partials of the groups that other CTAs finalize, into their
+        // rings; lanes are consecutive rows, so each store is 128 bytes
+        if (rows_here && acc_ok) {
+            int i = 0;  // index among the groups that others finalize
+            for (int g = 0; g < G; ++g) {
+                const int o = g % P;
+                if (o == rank) continue;
+                if ((i++ & 1) != half) continue;
+                const int sidx = rank < o ? rank : rank - 1;  // this CTA among o's senders
+                const uint32_t dst =
+                    cluster_addr(ring, (uint32_t)o) + (uint32_t)(sidx * part) + (uint32_t)((g / P) * 32 * p.Rp * 4);
+                __syncwarp();
+                uint32_t v[32];
+                tmem_ld32(tm_rows + (uint32_t)(32 * g), v);
+                if (L < p.R) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            st_cluster_f32(dst + (uint32_t)((j * p.Rp + L) * 4), __uint_as_float(v[j]));
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        st_cluster_f32(dst + (uint32_t)((j * p.Rp + L) * 4), __uint_as_float(v[j]));
                 }
             }
-            // squared norms over this CTA's K range, to every other CTA
+        }
+        // squared norms over this CTA's K range, to every other CTA
+        if (norm_warp) {
             for (int o = 0; o < P; ++o) {
                 if (o == rank) continue;
                 const int sidx = rank < o ? rank : rank - 1;
@@ -665,11 +677,8 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
             }
         }
         cluster_sync_all();  // the parts are in place
-    } else if (epi) {
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four warps' norms
     }
-
-    if (epi) {
+    if (norm_warp) {
         // totals over the cluster's K ranges: |e| per fact, rel |q| per query
         const float rel = (0.001953125f + (float)p.E * 1.1920929e-7f) * 4.0f;  // 4 (2^-9 + E 2^-23)
         float e_a = tl.en2[L], e_b = tl.en2[L + 128], q_a = tl.qa2[L];
@@ -682,62 +691,63 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
         tl.fnorm[L] = sqrtf(e_a) * 1.0001f;
         tl.fnorm[L + 128] = sqrtf(e_b) * 1.0001f;
         tl.qscale[L] = rel * sqrtf(q_a);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        // (a CTA whose accumulator was not ready has set the status word;
-        // its parts are then stale and so are these intervals)
-        if (rows_here && acc_ready) {
-            const float qs = L < p.R ? tl.qscale[L] : 0.f;
-            const uint32_t fn = saddr(tl.fnorm);
-            const uint32_t stg = ring + (uint32_t)split_out_offset(P, part) + (uint32_t)((warp - 2) * kOutBoxBytes * 2);
-            for (int g = rank; g < G; g += P) {
-                const int c = 32 * g;
-                __syncwarp();
-                uint32_t v[32];
-                tmem_ld32(tm_rows + (uint32_t)c, v);
-                float val[32];
+    }
+    __syncthreads();
+    if (rows_here && acc_ok) {
+        const float qs = L < p.R ? tl.qscale[L] : 0.f;
+        const uint32_t fn = saddr(tl.fnorm);
+        const uint32_t stg = ring + (uint32_t)split_out_offset(P, part) + (uint32_t)(warp * kOutBoxBytes * 2);
+        bool staged = false;
+        for (int g = rank, i = 0; g < G; g += P, ++i) {
+            if ((i & 1) != half) continue;
+            const int c = 32 * g;
+            __syncwarp();
+            uint32_t v[32];
+            tmem_ld32(tm_rows + (uint32_t)c, v);
+            float val[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(v[j]);
-                if (L < p.R) {
-                    for (int q = 0; q < P - 1; ++q) {
-                        const uint32_t pr = ring + (uint32_t)(q * part) + (uint32_t)(((g / P) * 32 * p.Rp + L) * 4);
+            for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(v[j]);
+            if (L < p.R) {
+                for (int q = 0; q < P - 1; ++q) {
+                    const uint32_t pr = ring + (uint32_t)(q * part) + (uint32_t)(((g / P) * 32 * p.Rp + L) * 4);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) val[j] += lds_f32(pr + (uint32_t)(j * p.Rp * 4));
-                    }
-                }
-                float eps[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) eps[j] = lds_f32(fn + 4u * (c + j));
-                // the previous boxes' tensor stores must have read the staging
-                if (g > rank) {
-                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    __syncwarp();
-                }
-                // lane = row: its 16-byte chunk q of 8 goes to q ^ (row % 8)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float lo4[4], hi4[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float e = __fmaf_ru(qs, eps[4 * q + u], 7.9e-31f);
-                        lo4[u] = __fsub_rd(val[4 * q + u], e);
-                        hi4[u] = __fadd_ru(val[4 * q + u], e);
-                    }
-                    const uint32_t at = stg + (uint32_t)(lane * 128 + ((q ^ (lane & 7)) * 16));
-                    sts_v4(at, lo4[0], lo4[1], lo4[2], lo4[3]);
-                    sts_v4(at + kOutBoxBytes, hi4[0], hi4[1], hi4[2], hi4[3]);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                // facts past N and rows past R fall outside the maps: not written
-                if (lane == 0) {
-                    tma_store_2d(&tm_lo, stg, (int)(f0 + c), row0);
-                    tma_store_2d(&tm_hi, stg + kOutBoxBytes, (int)(f0 + c), row0);
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    for (int j = 0; j < 32; ++j) val[j] += lds_f32(pr + (uint32_t)(j * p.Rp * 4));
                 }
             }
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            float eps[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) eps[j] = lds_f32(fn + 4u * (c + j));
+            // the previous boxes' tensor stores must have read the staging
+            if (staged) {
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+            }
+            // lane = row: its 16-byte chunk q of 8 goes to q ^ (row % 8)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float lo4[4], hi4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float e = __fmaf_ru(qs, eps[4 * q + u], 7.9e-31f);
+                    lo4[u] = __fsub_rd(val[4 * q + u], e);
+                    hi4[u] = __fadd_ru(val[4 * q + u], e);
+                }
+                const uint32_t at = stg + (uint32_t)(lane * 128 + ((q ^ (lane & 7)) * 16));
+                sts_v4(at, lo4[0], lo4[1], lo4[2], lo4[3]);
+                sts_v4(at + kOutBoxBytes, hi4[0], hi4[1], hi4[2], hi4[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
+            // facts past N and rows past R fall outside the maps: not written
+            if (lane == 0) {
+                tma_store_2d(&tm_lo, stg, (int)(f0 + c), row0);
+                tma_store_2d(&tm_hi, stg + kOutBoxBytes, (int)(f0 + c), row0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+            staged = true;
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -850,7 +860,7 @@ int split_max_clusters(int P, int F)
     if (it != cache.end()) return it->second;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P);
-    cfg.blockDim = dim3(kCoarseThreads);
+    cfg.blockDim = dim3(kSplitThreads);
     cfg.dynamicSmemBytes = split_smem_bytes(F);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -903,7 +913,7 @@ cudaError_t launch_coarse_split(CoarseParams p, const float *emb, int64_t n_fact
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(pl.tiles * pl.P));
-    cfg.blockDim = dim3(kCoarseThreads);
+    cfg.blockDim = dim3(kSplitThreads);
     cfg.dynamicSmemBytes = split_smem_bytes(pl.F);
     cfg.stream = s;
     cudaLaunchAttribute at[1];
