@@ -403,6 +403,9 @@ struct SplitSmemTail {
 // split - 1 CTAs, a part in its (idle) ring: that CTA's partial accumulator
 // of the groups this one finalizes, column by column ([groups][32][Rp]
 // floats), then its squared norms ([256] facts, [128] queries).
+// Fact rows per tensor copy: no copy exceeds 128 rows of 128 bytes (F is a
+// multiple of 32, so F / 2 is a multiple of 16)
+__host__ __device__ constexpr int split_fact_box(int F) { return F > 128 ? F / 2 : F; }
 __host__ __device__ constexpr int split_groups_owned(int F, int P) { return (F / 32 + P - 1) / P; }
 __host__ __device__ constexpr size_t split_part_bytes(int Rp, int F, int P)
 {
@@ -521,6 +524,8 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
         // exactly) and the tile's F fact rows as one box, one box per lane
         const uint32_t bytes = (uint32_t)((p.Rp + F) * kChunk * 4);
         const int bq = p.box_q, nb = p.Rp / bq;
+        // facts in boxes of at most 128 rows (16 KB): one, or two halves
+        const int bf = split_fact_box(F), nfb = F / bf;
         int issued = 0, s = 0, round = 0;
         for (int kc = k0; kc < k1; ++kc) {
             bool go = true;
@@ -536,11 +541,12 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
             }
             __syncwarp();
-            for (int j = lane; j <= nb; j += 32) {
+            for (int j = lane; j < nb + nfb; j += 32) {
                 if (j < nb)
                     tma_2d(saddr(q_st + (size_t)s * kSlotQ + (size_t)j * bq * 128), &tm_q, kc * kChunk, j * bq, fb);
                 else
-                    tma_2d(saddr(f_st + (size_t)s * stage_f), &tm_emb, kc * kChunk, (int)f0, fb);
+                    tma_2d(saddr(f_st + (size_t)s * stage_f + (size_t)(j - nb) * bf * 128), &tm_emb, kc * kChunk,
+                           (int)f0 + (j - nb) * bf, fb);
             }
             ++issued;
             if (++s == S) {
@@ -901,7 +907,7 @@ cudaError_t launch_coarse_split(CoarseParams p, const float *emb, int64_t n_fact
         p.box_q = 16 * d;
     }
     CUtensorMap te, tq;
-    e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, (uint32_t)pl.F);
+    e = tmap_f32(&te, emb, (uint64_t)p.E, (uint64_t)n_facts, (uint64_t)p.E * 4, (uint32_t)split_fact_box(pl.F));
     if (e != cudaSuccess) return e;
     e = tmap_f32(&tq, queries, (uint64_t)p.E, (uint64_t)p.R, (uint64_t)p.E * 4, (uint32_t)p.box_q);
     if (e != cudaSuccess) return e;
