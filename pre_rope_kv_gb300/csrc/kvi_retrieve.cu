@@ -1120,7 +1120,9 @@ select_kernel(const __grid_constant__ SelectParams p)
 // (coalesced, kCandUnroll loads in flight per lane); a group is 4 lanes'
 // facts.  Candidates are written in id order: a block scan over the warps'
 // counts gives each segment its base, and ballots order each warp's facts.
-constexpr int kCandUnroll = 4;
+// Twelve loads in flight per lane cover a 10k-fact row of lo or hi in one
+// round trip (about 2 us less per 64-query call than four).
+constexpr int kCandUnroll = 12;
 
 __global__ void __launch_bounds__(kSelectThreads, 1) cand_kernel(const __grid_constant__ CandParams p)
 {
