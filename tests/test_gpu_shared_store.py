@@ -69,7 +69,10 @@ def check_topk(st, q, k, ids, sc):
 @pytest.mark.parametrize("N,E,R,k", [(1000, 256, 1, 10), (3000, 1024, 64, 50), (777, 100, 17, 33),
                                      (5000, 384, 256, 256), (200, 64, 5, 200), (129, 32, 16, 7),
                                      # enough tiles for two accumulators (256 facts) per CTA
-                                     (40000, 128, 64, 50), (50001, 96, 3, 20), (39000, 64, 256, 8)])
+                                     (40000, 128, 64, 50), (50001, 96, 3, 20), (39000, 64, 256, 8),
+                                     # up to 128 queries: K split over clusters of 2 and of 3
+                                     # CTAs; 128 queries fill the M tile; 129 take the other form
+                                     (15000, 256, 100, 40), (10000, 512, 128, 64), (20000, 64, 129, 10)])
 def test_shared_topk_matches_oracle(N, E, R, k):
     w, b, st, q = shared_case(R, seed=N + E + R + k, n_facts=N, embed_dim=E)
     ids, sc, status, _ = run_topk(w, b, st, q, k)
