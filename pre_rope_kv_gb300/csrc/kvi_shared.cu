@@ -398,14 +398,15 @@ struct SplitSmemTail {
     float qscale[kQTile];  // rel * |q| per query (all K)
 };
 
+// Fact rows per tensor copy: no copy exceeds 128 rows of 128 bytes (F is a
+// multiple of 32, so F / 2 is a multiple of 16)
+__host__ __device__ constexpr int split_fact_box(int F) { return F > 128 ? F / 2 : F; }
+
 // The tile's 32-column groups are finalized round robin: group g by the
 // cluster's CTA g % split.  Each CTA receives, from each of the other
 // split - 1 CTAs, a part in its (idle) ring: that CTA's partial accumulator
 // of the groups this one finalizes, column by column ([groups][32][Rp]
 // floats), then its squared norms ([256] facts, [128] queries).
-// Fact rows per tensor copy: no copy exceeds 128 rows of 128 bytes (F is a
-// multiple of 32, so F / 2 is a multiple of 16)
-__host__ __device__ constexpr int split_fact_box(int F) { return F > 128 ? F / 2 : F; }
 __host__ __device__ constexpr int split_groups_owned(int F, int P) { return (F / 32 + P - 1) / P; }
 __host__ __device__ constexpr size_t split_part_bytes(int Rp, int F, int P)
 {
@@ -420,9 +421,8 @@ __host__ __device__ constexpr size_t split_out_offset(int P, size_t part)
     return ((size_t)(P - 1) * part + 1023) & ~(size_t)1023;
 }
 
-// Shared-memory accesses by 32-bit shared address.  Through a generic
-// pointer, a load that follows a global store may wait for it (the two could
-// alias as far as the hardware knows); these cannot.
+// Shared-memory accesses by 32-bit shared address (ld/st.shared): the
+// compiler cannot take them for global accesses that they might alias.
 __device__ __forceinline__ float lds_f32(uint32_t a)
 {
     float v;
@@ -497,6 +497,9 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
     const int k0 = rank * nk / P, k1 = (rank + 1) * nk / P;  // this CTA's K chunks
 
     if (tid == 0) {
+        // the copy descriptors are fetched while the barriers are set up
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_emb)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
         for (int s = 0; s < S; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&tl.full[s])) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 5;" ::"r"(saddr(&tl.empty[s])) : "memory");
