@@ -13,8 +13,8 @@
  *     as KVI_ERR_INVALID_ARG in *d_status; the injection still runs and its
  *     result on the overlapping slots is unspecified, as in the release
  *     build, which does not check.
- *   - it exports the hook below, which lets a test make one of the scoring
- *     kernel's bounded waits run out without a fault.
+ *   - it exports the hooks below, which let a test make one of the scoring
+ *     kernels' bounded waits run out without a fault.
  *
  * Only the debug library exports the symbols declared here.
  */
@@ -39,6 +39,19 @@ extern "C" {
  * Synchronous (it writes a device variable of the current device).
  * Errors: KVI_ERR_CUDA. */
 KVI_API kvi_status kvi_debug_stall_scorer_row(int64_t row);
+
+/* Failure hook (debug build only).  From the next call on, the tensor-core
+ * kernel of the shared-store path (kvi_retrieve_topk_shared,
+ * kvi_retrieve_and_inject_shared, the graph build) loads nothing for K chunk
+ * `chunk` (32 floats of E) in its CTA `cta`: the waits on that stage give up
+ * after the kernel's one-second bound, the call's status word reads
+ * KVI_ERR_TIMEOUT and its outputs are not valid.  Every copy the CTA did
+ * issue is waited for before it exits, and every CTA of a thread-block
+ * cluster still reaches the cluster's barriers: nothing faults or hangs and
+ * the context stays usable.  A (cta, chunk) that the launch does not have
+ * changes nothing; cta < 0 turns the hook off.  Synchronous (it writes
+ * device variables of the current device).  Errors: KVI_ERR_CUDA. */
+KVI_API kvi_status kvi_debug_stall_coarse_chunk(int32_t cta, int32_t chunk);
 
 #ifdef __cplusplus
 }

@@ -27,5 +27,5 @@ from ._binding import (  # noqa: F401
     kvi_graph_build_workspace_bytes, kvi_graph_build, kvi_graph_search_workspace_bytes,
     kvi_graph_search, graph_search_params, kvi_graph_retrieve_and_inject_workspace_bytes,
     kvi_graph_retrieve_and_inject, kvi_selftest_bounded_wait, open_library, use_library,
-    kvi_debug_stall_scorer_row, kvi_selftest_stream_read,
+    kvi_debug_stall_scorer_row, kvi_debug_stall_coarse_chunk, kvi_selftest_stream_read,
 )

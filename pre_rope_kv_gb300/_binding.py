@@ -182,6 +182,8 @@ def open_library(path: str):
     if hasattr(lib, "kvi_debug_stall_scorer_row"):  # debug build only
         lib.kvi_debug_stall_scorer_row.restype = S
         lib.kvi_debug_stall_scorer_row.argtypes = [i64]
+        lib.kvi_debug_stall_coarse_chunk.restype = S
+        lib.kvi_debug_stall_coarse_chunk.argtypes = [ctypes.c_int32, ctypes.c_int32]
     return lib
 
 
@@ -220,6 +222,16 @@ def kvi_debug_stall_scorer_row(row: int) -> None:
     if not hasattr(lib, "kvi_debug_stall_scorer_row"):
         raise RuntimeError("kvi_debug_stall_scorer_row needs the debug build (build(debug=True))")
     _check(lib.kvi_debug_stall_scorer_row(int(row)), "kvi_debug_stall_scorer_row")
+
+
+def kvi_debug_stall_coarse_chunk(cta: int, chunk: int) -> None:
+    """Debug build only (include/kvi_debug.h): make the shared-store path's
+    tensor-core kernel load nothing for K chunk `chunk` in CTA `cta`, so
+    that the waits on that stage run out (cta < 0: off)."""
+    lib = load_library()
+    if not hasattr(lib, "kvi_debug_stall_coarse_chunk"):
+        raise RuntimeError("kvi_debug_stall_coarse_chunk needs the debug build (build(debug=True))")
+    _check(lib.kvi_debug_stall_coarse_chunk(int(cta), int(chunk)), "kvi_debug_stall_coarse_chunk")
 
 
 def _check(status: int, where: str):

@@ -46,6 +46,14 @@
 #include "kvi_internal.cuh"
 
 namespace kvi {
+
+#ifdef KVI_DEBUG_CHECKS
+// Debug builds: the (CTA, K chunk) whose stage the coarse kernels do not
+// load (CTA < 0: none), set by kvi_debug_stall_coarse_chunk.
+__device__ int g_debug_stall_cta = -1;
+__device__ int g_debug_stall_chunk = -1;
+#endif
+
 namespace {
 
 constexpr int kTileM = 128;          // facts per CTA (MMA M)
@@ -207,12 +215,19 @@ coarse_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_constant_
                 break;
             }
             const uint32_t fb = saddr(&tl.full[s]);
-            if (lane == 0) {
+#ifdef KVI_DEBUG_CHECKS
+            // no expect-tx and no copy for this chunk: the waits on its
+            // stage run out
+            const bool stall = (int)blockIdx.x == g_debug_stall_cta && kc == g_debug_stall_chunk;
+#else
+            constexpr bool stall = false;
+#endif
+            if (lane == 0 && !stall) {
                 if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
             }
             __syncwarp();
-            for (int j = lane; j < na + nb; j += 32) {
+            for (int j = lane; j < (stall ? 0 : na + nb); j += 32) {
                 if (j < na)
                     tma_2d(saddr(a_st + (size_t)s * stage_a + (size_t)j * kBoxRowsA * 128), &tm_emb,
                            kc * kChunk, tile * MT * kTileM + j * kBoxRowsA, fb);
@@ -539,12 +554,19 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
                 break;
             }
             const uint32_t fb = saddr(&tl.full[s]);
-            if (lane == 0) {
+#ifdef KVI_DEBUG_CHECKS
+            // no expect-tx and no copy for this chunk: the waits on its
+            // stage run out
+            const bool stall = (int)blockIdx.x == g_debug_stall_cta && kc == g_debug_stall_chunk;
+#else
+            constexpr bool stall = false;
+#endif
+            if (lane == 0 && !stall) {
                 if (round > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
             }
             __syncwarp();
-            for (int j = lane; j < nb + nfb; j += 32) {
+            for (int j = lane; j < (stall ? 0 : nb + nfb); j += 32) {
                 if (j < nb)
                     tma_2d(saddr(q_st + (size_t)s * kSlotQ + (size_t)j * bq * 128), &tm_q, kc * kChunk, j * bq, fb);
                 else
@@ -997,3 +1019,16 @@ cudaError_t launch_coarse(const CoarseParams &p0, const float *emb, int64_t n_fa
 }
 
 }  // namespace kvi
+
+#ifdef KVI_DEBUG_CHECKS
+#include "kvi_debug.h"
+
+extern "C" kvi_status kvi_debug_stall_coarse_chunk(int32_t cta, int32_t chunk)
+{
+    const int c = cta < 0 ? -1 : (int)cta, k = cta < 0 ? -1 : (int)chunk;
+    cudaError_t e = cudaMemcpyToSymbol(kvi::g_debug_stall_cta, &c, sizeof c);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(kvi::g_debug_stall_chunk, &k, sizeof k);
+    if (e != cudaSuccess) return kvi::set_error(KVI_ERR_CUDA, cudaGetErrorString(e));
+    return KVI_OK;
+}
+#endif

@@ -317,12 +317,15 @@ def test_debug_build_exports_the_debug_hooks_too():
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
     assert exported == set(_declared_in("kvi.h")) | set(_declared_in("kvi_debug.h"))
-    assert _declared_in("kvi_debug.h") == ["kvi_debug_stall_scorer_row"]
+    assert _declared_in("kvi_debug.h") == ["kvi_debug_stall_coarse_chunk", "kvi_debug_stall_scorer_row"]
     raw = ctypes.CDLL(kvi.LIB_PATH)
     assert not hasattr(raw, "kvi_debug_stall_scorer_row")
-    # the release binding refuses the hook instead of calling a missing symbol
+    assert not hasattr(raw, "kvi_debug_stall_coarse_chunk")
+    # the release binding refuses the hooks instead of calling a missing symbol
     with pytest.raises(RuntimeError, match="debug build"):
         kvi.kvi_debug_stall_scorer_row(0)
+    with pytest.raises(RuntimeError, match="debug build"):
+        kvi.kvi_debug_stall_coarse_chunk(0, 0)
 
 
 def test_stream_read_validation(lib):

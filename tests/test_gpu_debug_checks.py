@@ -9,6 +9,9 @@
    one-second bound.  The status word of kvi_retrieve_topk (and of the fused
    call) then reads KVI_ERR_TIMEOUT, and the next call on the same context
    matches the oracle again.
+3. The same for the shared-store path's tensor-core kernels: one CTA loads
+   nothing for one K chunk, in the cluster form (up to 128 queries) and in
+   the form with facts on M (more queries).
 """
 import time
 
@@ -32,6 +35,7 @@ def dbg():
     with kvi.use_library(lib):
         yield lib
         kvi.kvi_debug_stall_scorer_row(-1)
+        kvi.kvi_debug_stall_coarse_chunk(-1, -1)
 
 
 def _w(seed, **kw):
@@ -123,3 +127,39 @@ def test_a_scorer_timeout_in_the_fused_call_injects_nothing_unscored(dbg):
     orc = kc.oracle_select(b)
     kc.check_selection(ids, scores, pos, orc)
     kc.check_pool_full(b, kc.placements_from_oracle(orc))
+
+
+@pytest.mark.parametrize("R", [64, 200])
+def test_a_coarse_kernel_wait_that_runs_out_surfaces_in_the_shared_status(dbg, R):
+    # 3000 facts, E = 1024: 64 queries take the cluster form (12 tiles of
+    # 256 facts, K split over 4 CTAs: CTA 0 owns chunks 0-7); 200 take the
+    # form with facts on M (24 CTAs, all 32 chunks each)
+    b = synth.build_workload(_w(74, n_facts=3000, embed_dim=1024), with_pool=False)
+    st = b.stores[0]
+    q = synth.query_rows(np.random.default_rng(75), R, b.w.embed_dim)
+    k = 16
+    view = kc.views_of(b)[0]
+    dq = torch.from_numpy(np.ascontiguousarray(q, np.float32)).cuda()
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvi.kvi_workspace_bytes_shared(R, b.w.n_facts, k), dtype=torch.uint8, device="cuda")
+
+    def call():
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvi.kvi_retrieve_topk_shared(view, R, dq, k, ids, sc, ws, status)
+        torch.cuda.synchronize()
+        return int(status.item())
+
+    def matches():
+        got = ids.cpu().numpy()
+        return all(np.array_equal(got[r], oracle.topk(oracle.scores(q[r], st.emb_np), k)) for r in range(R))
+
+    assert call() == 0 and matches()
+    kvi.kvi_debug_stall_coarse_chunk(0, 1)
+    t0 = time.perf_counter()
+    status = call()
+    waited = time.perf_counter() - t0
+    assert status == kvi.ERR_TIMEOUT
+    assert 0.9 < waited < 60.0, waited  # the one-second bounds, not a hang
+    kvi.kvi_debug_stall_coarse_chunk(-1, -1)
+    assert call() == 0 and matches()
