@@ -80,11 +80,12 @@ def test_shared_topk_matches_oracle(N, E, R, k):
     check_topk(st, q, k, ids, sc)
 
 
-@pytest.mark.parametrize("N,E,R,k", [(2000, 1024, 48, 30), (40000, 256, 40, 30)])
+@pytest.mark.parametrize("N,E,R,k", [(2000, 1024, 48, 30), (40000, 256, 40, 30), (3000, 256, 200, 20)])
 def test_tensor_core_intervals_contain_exact_scores(N, E, R, k):
     # white box: the workspace holds the plain regions, then lo and hi
     # planes [R][key_stride] float32 (256-byte aligned regions); 40k facts
-    # take the two-accumulator tiles
+    # take the split form without a cluster, 200 queries the form with facts
+    # on M
     w, b, st, q = shared_case(R, seed=711, n_facts=N, embed_dim=E)
     ids, sc, status, ws = run_topk(w, b, st, q, k)
     assert status == 0
