@@ -72,7 +72,10 @@ def check_topk(st, q, k, ids, sc):
                                      (40000, 128, 64, 50), (50001, 96, 3, 20), (39000, 64, 256, 8),
                                      # up to 128 queries: K split over clusters of 2 and of 3
                                      # CTAs; 128 queries fill the M tile; 129 take the other form
-                                     (15000, 256, 100, 40), (10000, 512, 128, 64), (20000, 64, 129, 10)])
+                                     (15000, 256, 100, 40), (10000, 512, 128, 64), (20000, 64, 129, 10),
+                                     # the widest and the narrowest embeddings: 256 chunks of
+                                     # K split over 4 CTAs; one partial chunk of 4 floats
+                                     (3000, 8192, 64, 20), (500, 4, 10, 5), (600, 4, 200, 5)])
 def test_shared_topk_matches_oracle(N, E, R, k):
     w, b, st, q = shared_case(R, seed=N + E + R + k, n_facts=N, embed_dim=E)
     ids, sc, status, _ = run_topk(w, b, st, q, k)
