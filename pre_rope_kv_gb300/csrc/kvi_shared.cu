@@ -397,7 +397,7 @@ constexpr int kQTile = 128;               // MMA M: query rows (at most 128 of t
 constexpr int kSlotQ = kQTile * kChunk * 4;
 constexpr int kMaxF = 256;                // MMA N: facts per tile
 constexpr int kMaxSplit = 4;
-// warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 norms; after the K loop all eight
+// warp 0 TMA, warp 1 MMA + TMEM, warps 2-7 norms; after the K loop all eight
 // warps take part, two per tensor-memory subpartition
 constexpr int kSplitThreads = 256;
 
@@ -517,12 +517,16 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
         for (int s = 0; s < S; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&tl.full[s])) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 5;" ::"r"(saddr(&tl.empty[s])) : "memory");
+            // the MMA commit plus one arrival from each of the six norm warps
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 7;" ::"r"(saddr(&tl.empty[s])) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&tl.mma_done)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    // rows that no norm thread owns (facts past F, queries past Rp) stay 0
+    tl.en2[tid] = 0.f;
+    if (tid < kQTile) tl.qa2[tid] = 0.f;
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tl.tmem_base)),
                      "r"((uint32_t)p.tmem_cols)
@@ -625,10 +629,13 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
             if (!done) record_status(p.status, KVI_ERR_TIMEOUT);
             tl.acc_ok = done ? 1u : 0u;
         }
-    } else if (warp < 6) {
-        // warps 2-5: squared norms of fact rows L and L + 128 and of query
-        // row L over this CTA's chunks, read from the same stages
-        float ea = 0.f, eb = 0.f, qa = 0.f;
+    } else {
+        // warps 2-7 (192 threads): squared norms over this CTA's chunks of
+        // the F fact rows and then the Rp query rows of each stage; thread t
+        // owns rows t and t + 192 of that list (consecutive rows per warp)
+        const int t = tid - 64;
+        const int nrows = F + p.Rp;
+        float a0 = 0.f, a1 = 0.f;
         int s = 0;
         uint32_t ph = 0;
         for (int kc = k0; kc < k1; ++kc) {
@@ -639,10 +646,13 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
                 break;
             }
             const uint8_t *fs = f_st + (size_t)s * stage_f;
-            if (L < F) ea += sq_row32(reinterpret_cast<const float *>(fs + L * 128), lane);
-            if (L + 128 < F) eb += sq_row32(reinterpret_cast<const float *>(fs + (L + 128) * 128), lane);
-            if (L < p.Rp)
-                qa += sq_row32(reinterpret_cast<const float *>(q_st + (size_t)s * kSlotQ + L * 128), lane);
+            const uint8_t *qs = q_st + (size_t)s * kSlotQ;
+            if (t < nrows)
+                a0 += sq_row32(reinterpret_cast<const float *>(t < F ? fs + t * 128 : qs + (t - F) * 128), lane);
+            if (t + 192 < nrows)
+                a1 += sq_row32(
+                    reinterpret_cast<const float *>(t + 192 < F ? fs + (t + 192) * 128 : qs + (t + 192 - F) * 128),
+                    lane);
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&tl.empty[s])) : "memory");
             if (++s == S) {
@@ -650,9 +660,8 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
                 ph ^= 1u;
             }
         }
-        tl.en2[L] = ea;
-        tl.en2[L + 128] = eb;
-        tl.qa2[L] = qa;
+        if (t < nrows) (t < F ? tl.en2[t] : tl.qa2[t - F]) = a0;
+        if (t + 192 < nrows) (t + 192 < F ? tl.en2[t + 192] : tl.qa2[t + 192 - F]) = a1;
     }
 
     const int G = F / 32;                      // 32-column groups of the tile
