@@ -543,7 +543,8 @@ coarse_split_kernel(const __grid_constant__ CUtensorMap tm_emb, const __grid_con
 
     if (warp == 0) {
         // per chunk: the query rows as boxes of box_q rows (they tile Rp
-        // exactly) and the tile's F fact rows as one box, one box per lane
+        // exactly) and the tile's F fact rows as one or two boxes, one box
+        // per lane
         const uint32_t bytes = (uint32_t)((p.Rp + F) * kChunk * 4);
         const int bq = p.box_q, nb = p.Rp / bq;
         // facts in boxes of at most 128 rows (16 KB): one, or two halves
