@@ -5,7 +5,7 @@ k = 50; "InferScale: GPU-Native KV Injection for Personalized LLM
 Serving" serving setting) through the paths beside the plain fused call:
 the rotary variants (Section 5.1 under the engines' conventions), the K/V
 store in pinned host memory (review Summary: offload to host DRAM) and 64
-concurrent queries over the one store (Section 6.4).  Every injected
+or 256 concurrent queries over the one store (Section 6.4).  Every injected
 element is compared with the float64 oracle (V bit-exact, K within
 2^-8|x| + 1e-6) and every other pool row must keep its canary, as in
 tests/test_gpu_configs.py.
@@ -94,10 +94,12 @@ def test_host_resident_store_full_size(b):
     del host
 
 
-def test_shared_store_64_queries_full_size(b):
-    # 64 requests over the one 10k-fact store: tensor-core coarse scores,
-    # exact rescoring, and the 64 injections into one pool
-    w, R = b.w, 64
+@pytest.mark.parametrize("R", [64, 256])
+def test_shared_store_queries_full_size(b, R):
+    # R requests over the one 10k-fact store: tensor-core coarse scores (64:
+    # the cluster form; 256: facts on M), exact rescoring, and the R
+    # injections into one pool
+    w = b.w
     st = b.stores[0]
     view = kc.views_of(b)[0]
     rng = np.random.default_rng(w.seed + 31)
